@@ -1,0 +1,2 @@
+"""CPU fp64 oracle (test infrastructure only; see flce_oracle)."""
+from .flce_oracle import capped_logits, flce_oracle, oracle_grad_W_rows, oracle_rows  # noqa: F401

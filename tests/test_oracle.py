@@ -1,0 +1,355 @@
+"""Pins for the CPU fp64 oracle, checked against things other than itself:
+closed forms, textbook library routines (torch cross_entropy and autograd in
+fp64), brute force on tiny inputs, central finite differences and invariants.
+Each is chosen so that a plausible slip in the oracle (a dropped term, a wrong
+sign or index, a transposed operand, m or T in the wrong place) fails one."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import flce_oracle, oracle_grad_W_rows, oracle_rows
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(n, h, v, seed, ign=1, scale=1.0):
+    rng = np.random.default_rng(seed)
+    hh = rng.standard_normal((n, h))
+    W = rng.standard_normal((v, h)) * scale
+    lab = rng.integers(0, v, n)
+    lab[:ign] = -100
+    return hh, W, lab
+
+
+# --- 1. W = 0: every logit is 0, loss = ln V, closed-form gradients ---------------
+@pytest.mark.parametrize("T", [0.0, 30.0])
+@pytest.mark.parametrize("m", [1.0, 0.5])
+def test_zero_weight_closed_form(T, m):
+    N, H, V = 9, 6, 37
+    h, _, lab = _rand(N, H, V, 1, ign=2)
+    W = np.zeros((V, H))
+    out = flce_oracle(h, W, lab, softcap=T, out_mult=m)
+    assert out["loss"] == pytest.approx(math.log(V), rel=1e-14)
+    assert np.all(out["grad_h"] == 0.0)
+    # grad_W_j = m * sum_valid (1/V - [y_i = j]) h_i / n_valid
+    valid = lab != -100
+    nv = valid.sum()
+    exp = np.zeros((V, H))
+    for i in range(N):
+        if not valid[i]:
+            continue
+        for j in range(V):
+            exp[j] += m * ((1.0 / V) - (1.0 if lab[i] == j else 0.0)) * h[i] / nv
+    np.testing.assert_allclose(out["grad_W"], exp, rtol=0, atol=1e-14)
+    # all logits tie: argmax is the lowest index, 0
+    assert np.all(out["predicted"] == 0)
+
+
+def test_zero_weight_ln_v_for_the_five_heads():
+    # the loss value the GPU must reproduce on W = 0 for each head's vocab
+    for name, w in workloads.WORKLOADS.items():
+        out = flce_oracle(np.ones((2, 8)), np.zeros((w.vocab, 8)), np.array([0, w.vocab - 1]),
+                          need_grad_h=False, need_grad_W=False, block_rows=1)
+        assert out["loss"] == pytest.approx(math.log(w.vocab), rel=1e-13), name
+
+
+# --- 2. row sums of dlogits vanish (T = 0): read dz off grad_W with h = I ----------
+def test_dlogit_row_sums_zero():
+    N, V = 7, 23
+    rng = np.random.default_rng(2)
+    h = np.eye(N)                       # H = N, m = 1: grad_W[j, i] = dz_ij
+    W = rng.standard_normal((V, N))
+    lab = rng.integers(0, V, N)
+    lab[3] = -100
+    out = flce_oracle(h, W, lab)
+    dz = out["grad_W"].T                # [N, V]
+    np.testing.assert_allclose(dz.sum(axis=1), 0.0, atol=1e-15)
+    assert np.all(dz[3] == 0.0)
+    # the label column carries (p - 1)/n_valid < 0, all others p/n_valid > 0
+    for i in range(N):
+        if lab[i] == -100:
+            continue
+        assert dz[i, lab[i]] < 0 and np.all(np.delete(dz[i], lab[i]) > 0)
+
+
+def test_grad_W_column_sums_vanish_without_softcap():
+    h, W, lab = _rand(11, 5, 19, 3, ign=2)
+    out = flce_oracle(h, W, lab, out_mult=0.5)
+    np.testing.assert_allclose(out["grad_W"].sum(axis=0), 0.0, atol=1e-14)
+
+
+# --- 3. large softcap T matches no softcap ----------------------------------------
+def test_large_softcap_matches_none():
+    h, W, lab = _rand(12, 8, 31, 4, ign=2, scale=0.3)
+    a = flce_oracle(h, W, lab, softcap=0.0)
+    b = flce_oracle(h, W, lab, softcap=1e6)
+    zmax = np.abs(h @ W.T).max()
+    tol = 10 * (zmax / 1e6) ** 2 + 1e-13
+    assert b["loss"] == pytest.approx(a["loss"], rel=tol)
+    np.testing.assert_allclose(b["grad_h"], a["grad_h"], rtol=0, atol=tol * np.abs(a["grad_h"]).max())
+    np.testing.assert_allclose(b["grad_W"], a["grad_W"], rtol=0, atol=tol * np.abs(a["grad_W"]).max())
+    # a small cap changes the result (the cap is really applied)
+    c = flce_oracle(h, W, lab, softcap=0.5)
+    assert abs(c["loss"] - a["loss"]) > 1e-3
+
+
+# --- 4. m identity: (m h) W^T = m (h W^T) ------------------------------------------
+@pytest.mark.parametrize("T", [0.0, 2.5])
+def test_out_mult_identity(T):
+    h, W, lab = _rand(10, 6, 17, 5, ign=1)
+    a = flce_oracle(h, W, lab, softcap=T, out_mult=0.5)
+    b = flce_oracle(0.5 * h, W, lab, softcap=T, out_mult=1.0)
+    assert a["loss"] == b["loss"]           # exact: 0.5 is a power of two
+    np.testing.assert_array_equal(a["grad_W"], b["grad_W"])
+    np.testing.assert_array_equal(a["grad_h"], 0.5 * b["grad_h"])   # chain rule through h' = m h
+    # and m is really applied (not dropped)
+    c = flce_oracle(h, W, lab, softcap=T, out_mult=1.0)
+    assert abs(c["loss"] - a["loss"]) > 1e-6
+
+
+# --- 5. central finite differences on tiny fp64 inputs ----------------------------
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (2.5, 1.0), (0.0, 0.5), (2.5, 0.5)])
+@pytest.mark.parametrize("red", ["mean", "sum"])
+def test_finite_differences(T, m, red):
+    N, H, V = 4, 5, 9
+    h, W, lab = _rand(N, H, V, 6, ign=1, scale=0.7)
+    g = 1.7
+    out = flce_oracle(h, W, lab, softcap=T, out_mult=m, reduction=red, grad_scale=g)
+    eps = 1e-6
+
+    def L(hh, WW):
+        return g * flce_oracle(hh, WW, lab, softcap=T, out_mult=m, reduction=red,
+                               need_grad_h=False, need_grad_W=False)["loss"]
+
+    fd_h = np.zeros_like(h)
+    for i in range(N):
+        for k in range(H):
+            hp = h.copy(); hp[i, k] += eps
+            hm = h.copy(); hm[i, k] -= eps
+            fd_h[i, k] = (L(hp, W) - L(hm, W)) / (2 * eps)
+    fd_W = np.zeros_like(W)
+    for j in range(V):
+        for k in range(H):
+            Wp = W.copy(); Wp[j, k] += eps
+            Wm = W.copy(); Wm[j, k] -= eps
+            fd_W[j, k] = (L(h, Wp) - L(h, Wm)) / (2 * eps)
+    np.testing.assert_allclose(out["grad_h"], fd_h, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(out["grad_W"], fd_W, rtol=1e-6, atol=1e-9)
+    assert np.all(out["grad_h"][0] == 0.0)      # ignored row
+
+
+# --- 6. all rows ignored ------------------------------------------------------------
+def test_all_ignored():
+    h, W, lab = _rand(6, 4, 11, 7, ign=6)
+    G0 = np.random.default_rng(0).standard_normal((11, 4))
+    out = flce_oracle(h, W, lab, softcap=3.0, grad_W0=G0)
+    assert out["loss"] == 0.0 and out["token_accuracy"] == 0.0 and out["n_valid"] == 0
+    assert np.all(out["grad_h"] == 0.0)
+    np.testing.assert_array_equal(out["grad_W"], G0)
+
+
+# --- 7. textbook routine: torch cross_entropy and autograd in fp64 ------------------
+def test_matches_torch_cross_entropy_tiny_head():
+    w = workloads.WORKLOADS["tiny"]
+    h, W, lab = workloads.make_inputs(w)
+    out = flce_oracle(h, W, lab)
+    ht = h.double().requires_grad_(True)
+    Wt = W.double().requires_grad_(True)
+    loss = torch.nn.functional.cross_entropy(ht @ Wt.T, lab, ignore_index=-100)
+    loss.backward()
+    assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    np.testing.assert_allclose(out["grad_h"], ht.grad.numpy(), rtol=0,
+                               atol=1e-10 * ht.grad.abs().max().item())
+    np.testing.assert_allclose(out["grad_W"], Wt.grad.numpy(), rtol=0,
+                               atol=1e-10 * Wt.grad.abs().max().item())
+
+
+def test_softcap_gradients_match_autograd():
+    N, H, V = 16, 12, 40
+    h, W, lab = _rand(N, H, V, 8, ign=3, scale=0.8)
+    T, m = 2.0, 0.5
+    out = flce_oracle(h, W, lab, softcap=T, out_mult=m)
+    ht = torch.tensor(h, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    # HF's capped logits: T * tanh(logits * m / T)
+    logits = T * torch.tanh((ht @ Wt.T) * m / T)
+    loss = torch.nn.functional.cross_entropy(logits, torch.tensor(lab), ignore_index=-100)
+    loss.backward()
+    assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    np.testing.assert_allclose(out["grad_h"], ht.grad.numpy(), rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(out["grad_W"], Wt.grad.numpy(), rtol=1e-10, atol=1e-14)
+
+
+# --- brute force with scalar loops on a tiny case -----------------------------------
+def test_brute_force_scalar_loops():
+    N, H, V = 3, 2, 5
+    h, W, lab = _rand(N, H, V, 9, ign=1)
+    T, m = 1.5, 0.5
+    tot, nv, corr = 0.0, 0, 0
+    for i in range(N):
+        s = []
+        for j in range(V):
+            z = sum(m * h[i, k] * W[j, k] for k in range(H))
+            s.append(T * math.tanh(z / T))
+        best = 0
+        for j in range(1, V):
+            if s[j] > s[best]:
+                best = j
+        lse = math.log(sum(math.exp(x) for x in s))
+        if lab[i] != -100:
+            nv += 1
+            tot += lse - s[lab[i]]
+            corr += int(best == lab[i])
+    out = flce_oracle(h, W, lab, softcap=T, out_mult=m)
+    assert out["loss"] == pytest.approx(tot / nv, rel=1e-13)
+    assert out["correct"] == corr and out["token_accuracy"] == pytest.approx(corr / nv)
+
+
+# --- 8. shift invariance (T = 0) -----------------------------------------------------
+def test_shift_invariance():
+    h, W, lab = _rand(8, 5, 13, 10, ign=1)
+    a = flce_oracle(h, W, lab)
+    h2 = np.concatenate([h, np.ones((8, 1))], axis=1)
+    W2 = np.concatenate([W, np.full((13, 1), 3.25)], axis=1)
+    b = flce_oracle(h2, W2, lab)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-13)
+    np.testing.assert_allclose(b["grad_h"][:, :5], a["grad_h"], atol=1e-14)
+    np.testing.assert_allclose(b["grad_W"][:, :5], a["grad_W"], atol=1e-14)
+    np.testing.assert_array_equal(b["predicted"], a["predicted"])
+
+
+# --- 9. permutation equivariance -----------------------------------------------------
+def test_permutation_equivariance():
+    N, H, V = 10, 6, 21
+    h, W, lab = _rand(N, H, V, 11, ign=2)
+    a = flce_oracle(h, W, lab, softcap=4.0)
+    rng = np.random.default_rng(5)
+    pv = rng.permutation(V)                 # new row j holds old row pv[j]
+    inv = np.argsort(pv)
+    lab2 = np.where(lab == -100, -100, inv[np.where(lab == -100, 0, lab)])
+    b = flce_oracle(h, W[pv], lab2, softcap=4.0)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-13)
+    np.testing.assert_allclose(b["grad_W"], a["grad_W"][pv], atol=1e-15)
+    np.testing.assert_allclose(b["grad_h"], a["grad_h"], atol=1e-15)
+    np.testing.assert_array_equal(pv[b["predicted"]], a["predicted"])
+    pr = rng.permutation(N)
+    c = flce_oracle(h[pr], W, lab[pr], softcap=4.0)
+    assert c["loss"] == pytest.approx(a["loss"], rel=1e-13)
+    np.testing.assert_allclose(c["grad_h"], a["grad_h"][pr], atol=1e-15)
+    np.testing.assert_allclose(c["grad_W"], a["grad_W"], atol=1e-15)
+    np.testing.assert_array_equal(c["lse"], a["lse"][pr])
+
+
+# --- 10. closed-form grad_h (T = 0) ---------------------------------------------------
+def test_closed_form_grad_h():
+    N, H, V = 9, 7, 15
+    h, W, lab = _rand(N, H, V, 12, ign=2)
+    m = 0.5
+    out = flce_oracle(h, W, lab, out_mult=m)
+    p = torch.softmax(torch.tensor(m * h @ W.T), dim=1).numpy()
+    nv = (lab != -100).sum()
+    for i in range(N):
+        if lab[i] == -100:
+            np.testing.assert_array_equal(out["grad_h"][i], 0.0)
+        else:
+            exp = m * (p[i] @ W - W[lab[i]]) / nv
+            np.testing.assert_allclose(out["grad_h"][i], exp, atol=1e-14)
+
+
+# --- 11. planted accuracy --------------------------------------------------------------
+def test_planted_accuracy():
+    N, H, V = 64, 8, 50
+    h, W, lab = _rand(N, H, V, 13, ign=6)
+    pred = flce_oracle(h, W, lab, need_grad_h=False, need_grad_W=False)["predicted"]
+    valid = np.nonzero(lab != -100)[0]
+    rng = np.random.default_rng(1)
+    plant = rng.choice(valid, size=len(valid) // 2, replace=False)
+    lab2 = lab.copy()
+    lab2[plant] = pred[plant]
+    out = flce_oracle(h, W, lab2, need_grad_h=False, need_grad_W=False)
+    natural = int(np.sum((lab2 == pred) & (lab2 != -100)))
+    assert out["correct"] == natural >= len(plant)
+    assert out["token_accuracy"] == pytest.approx(natural / len(valid))
+    assert out["token_accuracy"] >= 0.5
+
+
+def test_argmax_ties_lowest_index():
+    W = np.array([[1.0, 0.0], [2.0, 0.0], [2.0, 0.0], [0.0, 1.0]])
+    h = np.array([[1.0, 0.0], [0.0, 1.0]])
+    out = flce_oracle(h, W, np.array([2, 3]), need_grad_h=False, need_grad_W=False)
+    assert list(out["predicted"]) == [1, 3]
+    assert out["correct"] == 1                      # row 0's label 2 ties with 1; lowest wins
+
+
+# --- 12. += semantics of the fp32 accumulator ----------------------------------------
+def test_grad_W_accumulates():
+    h, W, lab = _rand(8, 4, 10, 14, ign=1)
+    G0 = np.random.default_rng(3).standard_normal((10, 4))
+    a = flce_oracle(h, W, lab)
+    b = flce_oracle(h, W, lab, grad_W0=G0)
+    np.testing.assert_allclose(b["grad_W"], G0 + a["grad_W"], atol=1e-15)
+
+
+def test_sum_reduction_and_grad_scale():
+    h, W, lab = _rand(8, 4, 10, 15, ign=3)
+    a = flce_oracle(h, W, lab)
+    b = flce_oracle(h, W, lab, reduction="sum", grad_scale=2.0)
+    nv = a["n_valid"]
+    assert b["loss"] == pytest.approx(a["loss"] * nv, rel=1e-14)
+    np.testing.assert_allclose(b["grad_h"], a["grad_h"] * nv * 2.0, rtol=1e-13)
+
+
+def test_invalid_label_rejected():
+    h, W, lab = _rand(4, 3, 5, 16, ign=0)
+    lab[1] = 5
+    with pytest.raises(ValueError):
+        flce_oracle(h, W, lab)
+
+
+# --- the sampled helpers agree with the full oracle ----------------------------------
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (30.0, 0.5)])
+def test_sampled_helpers_agree_with_full(T, m):
+    N, H, V = 40, 16, 70
+    h, W, lab = _rand(N, H, V, 17, ign=4)
+    full = flce_oracle(h, W, lab, softcap=T, out_mult=m)
+    rows = np.array([0, 5, 17, 39])
+    r = oracle_rows(h[rows], W, lab[rows], full["n_valid"], softcap=T, out_mult=m)
+    np.testing.assert_allclose(r["lse"], full["lse"][rows], rtol=1e-15)
+    np.testing.assert_allclose(r["grad_h"], full["grad_h"][rows], atol=1e-16)
+    np.testing.assert_array_equal(r["predicted"], full["predicted"][rows])
+    ids = np.array([0, 3, lab[7], 69])
+    gw = oracle_grad_W_rows(h, W, lab, ids, full["lse"], full["n_valid"], softcap=T, out_mult=m,
+                            block_rows=7)
+    np.testing.assert_allclose(gw, full["grad_W"][ids], atol=1e-16)
+
+
+# --- the pages' printed accumulator sizes pin fp32 [V, H] ----------------------------
+def test_page_accumulator_sizes():
+    with open(os.path.join(GOLDEN, "page_figures.json")) as f:
+        figs = json.load(f)["fp32_grad_weight_accumulator"]
+    for fg in figs:
+        nbytes = fg["vocab"] * fg["hidden"] * 4
+        assert round(nbytes / fg["unit_bytes"], fg["decimals"]) == fg["value_printed"]
+        if "bf16_value_printed" in fg:
+            assert round(nbytes / 2 / fg["unit_bytes"], fg["decimals"]) == fg["bf16_value_printed"]
+
+
+def test_workload_recipe_is_deterministic_and_shaped():
+    w = workloads.WORKLOADS["tiny"]
+    h1, W1, l1 = workloads.make_inputs(w)
+    h2, W2, l2 = workloads.make_inputs(w)
+    assert torch.equal(h1, h2) and torch.equal(W1, W2) and torch.equal(l1, l2)
+    assert h1.dtype == torch.bfloat16 and W1.shape == (4096, 512)
+    assert int((l1 == -100).sum()) == round(0.10 * 256)
+    assert abs(W1.float().std().item() - 0.02) < 1e-3
+    z = workloads.make_labels(20000, 1000, 3, 0.03, "zipf", 1.1)
+    zv = z[z != -100]
+    assert int((z == -100).sum()) == 600
+    # Zipf(1.1): id 0 is the most frequent, about 1/H_{1000,1.1} of the draws
+    hz = sum((k + 1) ** -1.1 for k in range(1000))
+    assert abs(float((zv == 0).float().mean()) - 1 / hz) < 0.02
