@@ -1,0 +1,157 @@
+/*
+ * flce.h - C ABI of the GB300 fused linear cross-entropy (FLCE) library.
+ *
+ * The operation is the loss of a language-model head computed without keeping
+ * the [tokens, vocab] logits (Liger-Kernel, "Muse Glimmer" support, section
+ * Summary item 1; DeepSeek-V3 support, section Summary: "logits are never
+ * materialized", and section Memory: logits replaced by chunked transients and
+ * a fixed fp32 weight-gradient accumulator).
+ *
+ * For rows i = 0..N-1 with hidden states h_i (bf16, length H), the lm-head
+ * weight W (bf16, [V, H]) and labels y_i (int64, ignore_index marks rows that
+ * do not count):
+ *
+ *   z_i   = m (h_i W^T)                 m = out_mult, folded into h (Muse Glimmer
+ *                                        page, Details / Softcap)
+ *   s_i   = T tanh(z_i / T) if T > 0, else z_i        T = softcap (same section)
+ *   lse_i = log sum_j exp(s_ij)
+ *   loss  = sum over valid rows of (lse_i - s_{i,y_i}) / n_valid   (MEAN)
+ *           or the plain sum (SUM); 0 when n_valid = 0
+ *   predicted_i   = argmax_j s_ij (lowest index on ties), every row
+ *   token_accuracy = #{valid i : predicted_i = y_i} / n_valid, 0 when n_valid = 0
+ *                    (Muse Glimmer page, Summary item 2 and Testing Done)
+ *   dz_ij = c (softmax(s_i)_j - [j = y_i]) (1 - (s_ij/T)^2 if T > 0),
+ *           c = grad_scale / n_valid (MEAN) or grad_scale (SUM), 0 on ignored rows;
+ *           dz is rounded to bf16 before the two backward products
+ *   grad_h_i = m sum_j dz_ij W_j                      (bf16 output, fp32 accumulate)
+ *   grad_W_j += m sum_i dz_ij h_i                     (fp32, ACCUMULATED in place;
+ *           the Muse Glimmer and DeepSeek-V3 pages, section Memory, keep this
+ *           accumulator in fp32; NULL means a frozen projection, as in the
+ *           SpecForge DSpine PR, section Changes)
+ *
+ * flce_ce_only is the cheap CE-only pass of the SpecForge DSpine PR (section
+ * Changes: only the backbone CE during the graph-free accumulation prepass).
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller. The library
+ *    allocates nothing and keeps no state between calls except a launch
+ *    counter and optional profiling events.
+ *  - Row-major layouts: h [N, ld_h] (ld_h >= H), W [V, ld_w] (ld_w >= H),
+ *    grad_h [N, H] contiguous, grad_W [V, H] contiguous, labels/predicted/
+ *    row_lse [N] contiguous. h, W and the workspace must be 16-byte aligned,
+ *    ld_h and ld_w multiples of 8 elements, H a multiple of 8.
+ *  - Scalars (loss, token_accuracy) are written to DEVICE memory, so calls
+ *    never synchronise the host. They run asynchronously on `stream` (a
+ *    cudaStream_t; NULL = legacy default stream).
+ *  - The return value is FLCE_OK or a host-detected error, returned before
+ *    any launch. Errors found on the device (bad labels, a bounded wait that
+ *    gave up) are OR-ed into a status word in the workspace; read it with
+ *    flce_get_status. On any error the outputs are unspecified.
+ *  - Nothing traps, prints or throws across this boundary.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-detected return codes. */
+#define FLCE_OK 0
+#define FLCE_ERR_ARG 1          /* null pointer, bad size, negative softcap, bad reduction */
+#define FLCE_ERR_ALIGN 2        /* pointer or row stride not 16-byte aligned, H % 8 != 0 */
+#define FLCE_ERR_WORKSPACE 3    /* workspace smaller than flce_workspace_size() */
+#define FLCE_ERR_UNSUPPORTED 4  /* device is not sm_103 / sm_100 family, or size limits */
+#define FLCE_ERR_CUDA 5         /* a CUDA runtime call or launch failed */
+/* Device-detected bits of the status word (flce_get_status). */
+#define FLCE_ERR_LABEL 16       /* a label is neither ignore_index nor in [0, V) */
+#define FLCE_ERR_TIMEOUT 32     /* a bounded pipeline wait gave up; the kernel returned early */
+
+/* Modes for flce_workspace_size. */
+#define FLCE_MODE_CE_ONLY 0
+#define FLCE_MODE_FORWARD 1
+#define FLCE_MODE_FORWARD_BACKWARD 2
+
+#define FLCE_REDUCTION_MEAN 0
+#define FLCE_REDUCTION_SUM 1
+
+/* Flags (flce_params.flags). */
+#define FLCE_FLAG_SIMT_GEMM 1        /* debug: plain fp32-FMA GEMMs instead of tcgen05 */
+#define FLCE_FLAG_TEST_STALL 2       /* test hook: the forward GEMM's loader issues no copies,
+                                        so its bounded waits run out (FLCE_ERR_TIMEOUT) */
+
+typedef struct flce_params {
+  int64_t n_rows;        /* N >= 0 */
+  int64_t hidden;        /* H > 0, multiple of 8 */
+  int64_t vocab;         /* V > 0, < 2^31 */
+  int64_t ld_h;          /* row stride of h in elements (0 => H) */
+  int64_t ld_w;          /* row stride of W in elements (0 => H) */
+  float softcap;         /* T >= 0; 0 => no softcap */
+  float out_mult;        /* m, the output multiplier folded into h */
+  int64_t ignore_index;  /* rows with this label do not count (default -100) */
+  int32_t reduction;     /* FLCE_REDUCTION_MEAN (default) or FLCE_REDUCTION_SUM */
+  float grad_scale;      /* g: upstream dL/dloss multiplying every gradient (default 1) */
+  int64_t chunk_rows;    /* rows per chunk C (0 => library default); rounded up to 128 */
+  int32_t flags;         /* FLCE_FLAG_* */
+  int64_t timeout_ns;    /* limit of each bounded device wait (0 => 2 s) */
+} flce_params;
+
+/* Fills the defaults: softcap 0, out_mult 1, ignore_index -100, MEAN,
+ * grad_scale 1, chunk_rows 0, flags 0, timeout 0; sizes and strides 0. */
+void flce_default_params(flce_params* p);
+
+/* Bytes of device workspace a call needs. mode is FLCE_MODE_*; need_grad_h and
+ * need_grad_W (0/1) matter for FORWARD_BACKWARD only. Depends on C, H and V
+ * but not on N beyond min(N, C): the transient memory is O(C * V).
+ * Returns 0 for invalid parameters. */
+size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W);
+
+/* CE-only pass: loss and (optionally) token_accuracy, no gradients, no saved
+ * state. loss: device float scalar; token_accuracy: device float scalar or NULL. */
+int flce_ce_only(const flce_params* p, const void* h, const void* W, const int64_t* labels,
+                 float* loss, float* token_accuracy,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward: as flce_ce_only, plus optional per-row outputs predicted [N]
+ * (int64, argmax for every row) and row_lse [N] (fp32 log-sum-exp of s_i). */
+int flce_forward(const flce_params* p, const void* h, const void* W, const int64_t* labels,
+                 float* loss, float* token_accuracy, int64_t* predicted, float* row_lse,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward + backward: the forward outputs plus grad_h (bf16 [N, H], written;
+ * NULL => not computed) and grad_W (fp32 [V, H], ACCUMULATED: grad_W += dL/dW;
+ * NULL => frozen W, skipped). */
+int flce_forward_backward(const flce_params* p, const void* h, const void* W,
+                          const int64_t* labels, float* loss, float* token_accuracy,
+                          int64_t* predicted, void* grad_h, float* grad_W,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream` and returns (in *status) the device status word of the
+ * last call that used this workspace: 0 or FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT.
+ * Return value: FLCE_OK or FLCE_ERR_ARG / FLCE_ERR_CUDA. */
+int flce_get_status(const void* workspace, void* stream, int32_t* status);
+
+/* Static text for a return code or status bit set. Never NULL. */
+const char* flce_status_string(int code);
+
+/* Number of kernels this library has launched in this process. */
+int64_t flce_launch_count(void);
+
+/* Per-kernel timing with CUDA events recorded on the launching stream around
+ * each launch. flce_profile_begin(1) starts collecting (clears old records),
+ * flce_profile_begin(0) stops. flce_profile_read synchronises the recorded
+ * events and fills, for kernel ids 0..n-1, the launch count and the summed
+ * milliseconds; it returns the number of kernel ids (FLCE_NUM_KERNELS). */
+#define FLCE_NUM_KERNELS 10
+int flce_profile_begin(int enable);
+int flce_profile_read(int64_t* launches, double* total_ms, int n);
+const char* flce_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

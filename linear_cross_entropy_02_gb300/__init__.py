@@ -1,0 +1,219 @@
+"""GB300 fused linear cross-entropy (FLCE): Python binding of libflce.so.
+
+The loss of a language-model head, mean over non-ignored rows of
+CE(softcap(m * h W^T), label), with token accuracy, predicted tokens, grad_h
+and an fp32 grad_W accumulator, computed by hand-written sm_103a kernels
+without keeping the [tokens, vocab] logits (Liger-Kernel, "Muse Glimmer"
+support, Summary and Details / Softcap; DeepSeek-V3 support, Summary and
+Memory; SpecForge DSpine PR, Changes: flattened frozen projection and the
+CE-only prepass).
+
+This module only marshals arguments: it checks dtypes and devices, flattens
+leading row dimensions ([B, k, S, H] -> [N, H], the DSpine page's flattened
+proposal rows), allocates outputs and a cached workspace with torch, and calls
+the C ABI on torch's current CUDA stream. Every step of the computation runs
+in the library's kernels; CPU tensors are rejected, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,  # noqa: F401
+                   FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
+
+__all__ = [
+    "flce_ce_only", "flce_forward", "flce_forward_backward", "flce_workspace_size", "flce_get_status",
+    "flce_launch_count", "flce_profile_begin", "flce_profile_read", "FlceError",
+]
+
+_REDUCTIONS = {"mean": FLCE_REDUCTION_MEAN, "sum": FLCE_REDUCTION_SUM}
+_workspaces: dict = {}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _params(n_rows: int, hidden: int, vocab: int, ld_h: int, ld_w: int, softcap: float, out_mult: float,
+            ignore_index: int, reduction: str, grad_scale: float, chunk_rows: int, flags: int,
+            timeout_ns: int) -> FlceParams:
+    if reduction not in _REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
+    p = FlceParams()
+    _lib.lib().flce_default_params(ctypes.byref(p))
+    p.n_rows, p.hidden, p.vocab = n_rows, hidden, vocab
+    p.ld_h, p.ld_w = ld_h, ld_w
+    p.softcap, p.out_mult = float(softcap), float(out_mult)
+    p.ignore_index = int(ignore_index)
+    p.reduction = _REDUCTIONS[reduction]
+    p.grad_scale = float(grad_scale)
+    p.chunk_rows = int(chunk_rows)
+    p.flags = int(flags)
+    p.timeout_ns = int(timeout_ns)
+    return p
+
+
+def _rows2d(h: torch.Tensor, H: int) -> torch.Tensor:
+    h2 = h.reshape(-1, H)
+    if h2.stride(1) != 1 or h2.stride(0) % 8 != 0 or h2.data_ptr() % 16 != 0:
+        h2 = h2.contiguous()
+    return h2
+
+
+def _check(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor):
+    for name, t in (("h", h), ("W", W), ("labels", labels)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("h and W must be bfloat16")
+    if labels.dtype != torch.int64:
+        raise ValueError("labels must be int64")
+    if W.dim() != 2 or h.shape[-1] != W.shape[1]:
+        raise ValueError("W must be [V, H] and h [..., H]")
+    if labels.shape != h.shape[:-1]:
+        raise ValueError("labels must have h's leading shape")
+    if h.device != W.device or h.device != labels.device:
+        raise ValueError("h, W and labels must be on one device")
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        _workspaces.pop(key, None)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _raise(rc: int, what: str):
+    if rc != 0:
+        raise FlceError(rc, what)
+
+
+def flce_workspace_size(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_MODE_FORWARD_BACKWARD,
+                        need_grad_h: bool = True, need_grad_W: bool = True, chunk_rows: int = 0,
+                        flags: int = 0) -> int:
+    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0)
+    return int(_lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
+
+
+def _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags,
+             timeout_ns, mode, need_gh, need_gw):
+    _check(h, W, labels)
+    H = W.shape[1]
+    V = W.shape[0]
+    h2 = _rows2d(h, H)
+    if W.stride(1) != 1 or W.stride(0) % 8 != 0 or W.data_ptr() % 16 != 0:
+        W = W.contiguous()
+    lab = labels.reshape(-1).contiguous()
+    p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
+                grad_scale, chunk_rows, flags, timeout_ns)
+    nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_gh), int(need_gw))
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
+    ws = _workspace(h.device, nbytes)
+    return p, h2, W, lab, ws, nbytes
+
+
+def flce_ce_only(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                 chunk_rows=0, flags=0, timeout_ns=0):
+    """CE-only pass (no gradients, no saved state). Returns (loss, token_accuracy)
+    as 0-d fp32 CUDA tensors."""
+    p, h2, W, lab, ws, nbytes = _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, 1.0,
+                                         chunk_rows, flags, timeout_ns, FLCE_MODE_CE_ONLY, False, False)
+    loss = torch.empty((), dtype=torch.float32, device=h.device)
+    acc = torch.empty((), dtype=torch.float32, device=h.device)
+    rc = _lib.lib().flce_ce_only(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+                                 _ptr(ws), nbytes, _stream_handle(h.device))
+    _raise(rc, "flce_ce_only")
+    return loss, acc
+
+
+def flce_forward(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                 return_predicted=True, return_lse=False, chunk_rows=0, flags=0, timeout_ns=0):
+    """Forward only. Returns dict(loss, token_accuracy, predicted, lse); per-row
+    outputs have h's leading shape."""
+    p, h2, W, lab, ws, nbytes = _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, 1.0,
+                                         chunk_rows, flags, timeout_ns, FLCE_MODE_FORWARD, False, False)
+    dev = h.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
+    lse = torch.empty(h2.shape[0], dtype=torch.float32, device=dev) if return_lse else None
+    rc = _lib.lib().flce_forward(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+                                 _ptr(pred), _ptr(lse), _ptr(ws), nbytes, _stream_handle(dev))
+    _raise(rc, "flce_forward")
+    lead = h.shape[:-1]
+    return {"loss": loss, "token_accuracy": acc,
+            "predicted": None if pred is None else pred.view(lead),
+            "lse": None if lse is None else lse.view(lead)}
+
+
+def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None, need_grad_h=True,
+                          softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean", grad_scale=1.0,
+                          return_predicted=False, chunk_rows=0, flags=0, timeout_ns=0):
+    """Forward + backward. grad_W: fp32 [V, H] CUDA tensor ACCUMULATED in place
+    (grad_W += dL/dW), or None for a frozen W. Returns dict(loss,
+    token_accuracy, predicted, grad_h, grad_W); grad_h (bf16) has h's shape."""
+    if grad_W is not None:
+        if grad_W.dtype != torch.float32 or grad_W.shape != W.shape or not grad_W.is_contiguous():
+            raise ValueError("grad_W must be a contiguous fp32 tensor shaped like W")
+        if grad_W.device != W.device:
+            raise ValueError("grad_W must be on W's device")
+    p, h2, W, lab, ws, nbytes = _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale,
+                                         chunk_rows, flags, timeout_ns, FLCE_MODE_FORWARD_BACKWARD,
+                                         need_grad_h, grad_W is not None)
+    dev = h.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
+    gh = torch.empty((h2.shape[0], W.shape[1]), dtype=torch.bfloat16, device=dev) if need_grad_h else None
+    rc = _lib.lib().flce_forward_backward(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+                                          _ptr(pred), _ptr(gh), _ptr(grad_W), _ptr(ws), nbytes,
+                                          _stream_handle(dev))
+    _raise(rc, "flce_forward_backward")
+    lead = h.shape[:-1]
+    return {"loss": loss, "token_accuracy": acc,
+            "predicted": None if pred is None else pred.view(lead),
+            "grad_h": None if gh is None else gh.view(h.shape), "grad_W": grad_W}
+
+
+def flce_get_status(device=None) -> int:
+    """Synchronises the current stream and returns the device status word of
+    the last call on this device's cached workspace (0 = no device error)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    ws = _workspaces.get(dev.index)
+    if ws is None:
+        return 0
+    st = ctypes.c_int32(0)
+    _raise(_lib.lib().flce_get_status(_ptr(ws), _stream_handle(dev), ctypes.byref(st)), "flce_get_status")
+    return int(st.value)
+
+
+def flce_launch_count() -> int:
+    return int(_lib.lib().flce_launch_count())
+
+
+def flce_profile_begin(enable: bool = True) -> None:
+    _lib.lib().flce_profile_begin(int(enable))
+
+
+def flce_profile_read() -> dict:
+    """{kernel name: (launches, total ms)} of the launches recorded since flce_profile_begin(True)."""
+    n = _lib.FLCE_NUM_KERNELS
+    launches = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    rc = _lib.lib().flce_profile_read(launches, ms, n)
+    if rc < 0:
+        raise FlceError(-rc, "flce_profile_read")
+    L = _lib.lib()
+    return {L.flce_kernel_name(i).decode(): (int(launches[i]), float(ms[i])) for i in range(n) if launches[i]}

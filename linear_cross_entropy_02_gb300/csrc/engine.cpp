@@ -1,0 +1,543 @@
+// Host engine behind the C ABI of include/flce.h: argument checks, workspace
+// carving, tensor-map encoding, and the stream-ordered launch sequence of the
+// row-chunk loop. No allocation, no host synchronisation (except in
+// flce_get_status and flce_profile_read, which exist to synchronise).
+//
+// Launch sequence of flce_forward_backward (one stream):
+//   prologue                               labels -> n_valid, status, sums = 0
+//   [W^T transpose]                        when grad_h is wanted
+//   for each chunk of C rows:
+//     forward GEMM + statistics epilogue   z = m h_c W^T, s = cap(z) stored
+//     merge                                lse, argmax, row loss, chunk sums
+//     dlogits                              dz (bf16), and dz^T when grad_W
+//     grad_h GEMM                          grad_h_c = m dz W
+//     [h_c^T transpose] + grad_W GEMM      grad_W += m dz^T h_c
+//   finish                                 loss, token accuracy
+// The logits of a chunk are the only O(C * V) transient (the Liger-Kernel
+// DeepSeek-V3 page, section Memory: chunked transients instead of the full
+// logits).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "flce_internal.h"
+
+using namespace flce;
+
+namespace {
+
+constexpr int64_t kDefaultChunkRows = 8192;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::atomic<int64_t> g_launches{0};
+
+// ------------------------------------------------------------ profiling
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+
+struct LaunchScope {
+  int kernel;
+  cudaStream_t stream;
+  cudaEvent_t start = nullptr, stop = nullptr;
+  LaunchScope(int k, cudaStream_t s) : kernel(k), stream(s) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on && cudaEventCreate(&start) == cudaSuccess && cudaEventCreate(&stop) == cudaSuccess) {
+      cudaEventRecord(start, stream);
+    } else {
+      start = stop = nullptr;
+    }
+  }
+  ~LaunchScope() {
+    g_launches.fetch_add(1);
+    if (start) {
+      cudaEventRecord(stop, stream);
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      g_prof.push_back({kernel, start, stop});
+    }
+  }
+};
+
+const char* const kKernelNames[FLCE_NUM_KERNELS] = {
+    "prologue", "fwd_gemm_stats", "merge", "dlogits", "grad_h_gemm",
+    "grad_W_gemm", "transpose_W", "transpose_h", "finish", "simt_stats"};
+
+// ------------------------------------------------------------ device info
+int g_sm_count[kMaxDevices] = {0};
+int g_cc[kMaxDevices] = {0};
+
+int device_info(int* sms, int* cc) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLCE_ERR_CUDA;
+  if (g_sm_count[dev] == 0) {
+    int n = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+    g_cc[dev] = major * 10 + minor;
+    g_sm_count[dev] = n;
+  }
+  *sms = g_sm_count[dev];
+  *cc = g_cc[dev];
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 [outer][inner] with row stride `ld` elements; box = 64 x box_rows, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ layout
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct Layout {
+  int64_t C;        // rows per chunk (multiple of 128)
+  int64_t n_vtiles; // vocab tiles of 256
+  int64_t ldp, ldz, ldd, ldt, ldwt, ldht;
+  int64_t merge_blocks;
+  bool need_z, need_dz, need_dzt, need_wt, need_ht;
+  size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_dz, off_dzt, off_wt,
+      off_ht, total;
+};
+
+struct Norm {
+  flce_params p;
+  int64_t ld_h, ld_w;
+};
+
+int normalise(const flce_params* in, Norm* out) {
+  if (!in) return FLCE_ERR_ARG;
+  Norm n;
+  n.p = *in;
+  const flce_params& p = n.p;
+  if (p.n_rows < 0 || p.hidden <= 0 || p.vocab <= 0 || p.vocab >= (int64_t(1) << 31) - 512) return FLCE_ERR_ARG;
+  if (p.n_rows >= (int64_t(1) << 31) - 512 || p.hidden >= (int64_t(1) << 24)) return FLCE_ERR_ARG;
+  if (!(p.softcap >= 0.f) || !std::isfinite(p.softcap) || !std::isfinite(p.out_mult) ||
+      !std::isfinite(p.grad_scale))
+    return FLCE_ERR_ARG;
+  if (p.reduction != FLCE_REDUCTION_MEAN && p.reduction != FLCE_REDUCTION_SUM) return FLCE_ERR_ARG;
+  if (p.chunk_rows < 0 || p.timeout_ns < 0) return FLCE_ERR_ARG;
+  if (p.hidden % 8 != 0) return FLCE_ERR_ALIGN;
+  n.ld_h = p.ld_h == 0 ? p.hidden : p.ld_h;
+  n.ld_w = p.ld_w == 0 ? p.hidden : p.ld_w;
+  if (n.ld_h < p.hidden || n.ld_w < p.hidden) return FLCE_ERR_ARG;
+  if (n.ld_h % 8 != 0 || n.ld_w % 8 != 0) return FLCE_ERR_ALIGN;
+  *out = n;
+  return FLCE_OK;
+}
+
+void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
+  const flce_params& p = n.p;
+  const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
+  const bool bwd = mode == FLCE_MODE_FORWARD_BACKWARD && (gh || gw);
+  int64_t c = p.chunk_rows > 0 ? p.chunk_rows : kDefaultChunkRows;
+  c = std::min<int64_t>(c, std::max<int64_t>(p.n_rows, 1));
+  L->C = round_up(c, kBM);
+  L->n_vtiles = (p.vocab + kVTile - 1) / kVTile;
+  L->ldp = L->C;
+  L->ldz = L->n_vtiles * kVTile;
+  L->ldd = round_up(p.vocab, 8);
+  L->ldt = L->C;
+  L->ldwt = round_up(p.vocab, 8);
+  L->ldht = L->C;
+  L->merge_blocks = (L->C + 127) / 128;
+  L->need_z = bwd || simt;
+  L->need_dz = bwd && gh;
+  L->need_dzt = bwd && gw;
+  L->need_wt = bwd && gh;
+  L->need_ht = bwd && gw;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  L->off_hdr = take(sizeof(Header));
+  L->off_bl = take(sizeof(double) * L->merge_blocks);
+  L->off_bc = take(sizeof(int64_t) * L->merge_blocks);
+  L->off_pmax = take(sizeof(float) * L->n_vtiles * L->ldp);
+  L->off_psum = take(sizeof(float) * L->n_vtiles * L->ldp);
+  L->off_pidx = take(sizeof(int32_t) * L->n_vtiles * L->ldp);
+  L->off_tgt = take(sizeof(float) * L->C);
+  L->off_lse = take(sizeof(float) * L->C);
+  L->off_z = L->need_z ? take(sizeof(float) * L->C * L->ldz) : 0;
+  L->off_dz = L->need_dz ? take(sizeof(uint16_t) * L->C * L->ldd) : 0;
+  L->off_dzt = L->need_dzt ? take(sizeof(uint16_t) * round_up(p.vocab, kBM) * L->ldt) : 0;
+  L->off_wt = L->need_wt ? take(sizeof(uint16_t) * p.hidden * L->ldwt) : 0;
+  L->off_ht = L->need_ht ? take(sizeof(uint16_t) * p.hidden * L->ldht) : 0;
+  L->total = off;
+}
+
+inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+#define FLCE_LAUNCH(kid, expr)                         \
+  do {                                                 \
+    LaunchScope _scope((kid), stream);                 \
+    if ((expr) != cudaSuccess) return FLCE_ERR_CUDA;   \
+  } while (0)
+
+struct Call {
+  int mode;
+  const void* h;
+  const void* W;
+  const int64_t* labels;
+  float* loss;
+  float* acc;
+  int64_t* predicted;
+  float* row_lse;
+  void* grad_h;
+  float* grad_W;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+int run(const flce_params* params, const Call& c) {
+  Norm n;
+  int rc = normalise(params, &n);
+  if (rc != FLCE_OK) return rc;
+  const flce_params& p = n.p;
+  const bool gh = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_h != nullptr;
+  const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
+  if (!c.loss || !c.ws || !c.W) return FLCE_ERR_ARG;
+  if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
+  if (!aligned16(c.ws) || (c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
+  if (gh && !aligned16(c.grad_h)) return FLCE_ERR_ALIGN;
+  if (gw && !aligned16(c.grad_W)) return FLCE_ERR_ALIGN;
+  Layout L;
+  make_layout(n, c.mode, gh, gw, &L);
+  if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  int sms = 0, cc = 0;
+  rc = device_info(&sms, &cc);
+  if (rc != FLCE_OK) return rc;
+  const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
+  if (cc != 103) return FLCE_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
+  if (!simt && !load_encoder()) return FLCE_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = c.stream;
+  uint8_t* ws = static_cast<uint8_t*>(c.ws);
+  Header* hdr = reinterpret_cast<Header*>(ws + L.off_hdr);
+  float* pmax = reinterpret_cast<float*>(ws + L.off_pmax);
+  float* psum = reinterpret_cast<float*>(ws + L.off_psum);
+  int32_t* pidx = reinterpret_cast<int32_t*>(ws + L.off_pidx);
+  float* tgt = reinterpret_cast<float*>(ws + L.off_tgt);
+  float* lse = reinterpret_cast<float*>(ws + L.off_lse);
+  float* zbuf = L.need_z ? reinterpret_cast<float*>(ws + L.off_z) : nullptr;
+  uint16_t* dz = L.need_dz ? reinterpret_cast<uint16_t*>(ws + L.off_dz) : nullptr;
+  uint16_t* dzt = L.need_dzt ? reinterpret_cast<uint16_t*>(ws + L.off_dzt) : nullptr;
+  uint16_t* wt = L.need_wt ? reinterpret_cast<uint16_t*>(ws + L.off_wt) : nullptr;
+  uint16_t* ht = L.need_ht ? reinterpret_cast<uint16_t*>(ws + L.off_ht) : nullptr;
+  const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
+  const int N = static_cast<int>(p.n_rows), H = static_cast<int>(p.hidden), V = static_cast<int>(p.vocab);
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(c.labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+
+  CUtensorMap map_h, map_w, map_wt;
+  if (!simt && N > 0) {
+    if (!encode_bf16(&map_h, c.h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+    if (!encode_bf16(&map_w, c.W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+  }
+  if (L.need_wt && N > 0) {
+    FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_bf16(static_cast<const uint16_t*>(c.W), n.ld_w, V, H, wt, L.ldwt,
+                                                     stream));
+    if (!simt && !encode_bf16(&map_wt, wt, V, H, L.ldwt, kBN)) return FLCE_ERR_UNSUPPORTED;
+  }
+
+  for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
+    const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
+    const int64_t* lab_c = c.labels + r0;
+
+    // ---- forward GEMM with the statistics epilogue
+    GemmParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.M = rows;
+    g.N = V;
+    g.K = H;
+    g.m_tiles = (rows + kBM - 1) / kBM;
+    g.n_tiles = static_cast<int>(L.n_vtiles);
+    g.k_iters = (H + kBK - 1) / kBK;
+    g.group_m = std::min(g.m_tiles, 16);
+    g.a_row0 = static_cast<int>(r0);
+    g.b_row0 = 0;
+    g.alpha = p.out_mult;
+    g.M_valid = rows;
+    g.N_valid = V;
+    g.softcap = p.softcap;
+    g.inv_softcap = inv_cap;
+    g.labels = lab_c;
+    g.ignore_index = p.ignore_index;
+    g.part_max = pmax;
+    g.part_sum = psum;
+    g.part_idx = pidx;
+    g.tgt = tgt;
+    g.ldp = static_cast<int>(L.ldp);
+    g.zbuf = zbuf;
+    g.ldz = L.ldz;
+    g.status = &hdr->status;
+    g.timeout_ns = timeout;
+    g.debug_flags = p.flags;
+    const bool store = L.need_z;
+    if (simt) {
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_simt(EPI_STATS, c.h, n.ld_h, c.W, n.ld_w, g, stream));
+      FLCE_LAUNCH(K_SIMT_STATS, launch_stats_from_z(g, rows, store, stream));
+    } else {
+      const int tiles = g.m_tiles * g.n_tiles;
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, &map_h, &map_w, g,
+                                             std::min(tiles, sms), stream));
+    }
+
+    // ---- merge of the vocab-tile statistics
+    MergeParams mp;
+    mp.rows = rows;
+    mp.n_vtiles = static_cast<int>(L.n_vtiles);
+    mp.ldp = static_cast<int>(L.ldp);
+    mp.part_max = pmax;
+    mp.part_sum = psum;
+    mp.part_idx = pidx;
+    mp.tgt = tgt;
+    mp.labels = lab_c;
+    mp.ignore_index = p.ignore_index;
+    mp.lse = lse;
+    mp.predicted = c.predicted ? c.predicted + r0 : nullptr;
+    mp.row_lse = c.row_lse ? c.row_lse + r0 : nullptr;
+    mp.block_loss = reinterpret_cast<double*>(ws + L.off_bl);
+    mp.block_correct = reinterpret_cast<int64_t*>(ws + L.off_bc);
+    mp.hdr = hdr;
+    FLCE_LAUNCH(K_MERGE, launch_merge(mp, stream));
+
+    if (!gh && !gw) continue;
+
+    // ---- dlogits
+    DlogitParams dp;
+    dp.rows = rows;
+    dp.vocab = V;
+    dp.s = zbuf;
+    dp.lds = L.ldz;
+    dp.lse = lse;
+    dp.labels = lab_c;
+    dp.ignore_index = p.ignore_index;
+    dp.softcap = p.softcap;
+    dp.inv_softcap = inv_cap;
+    dp.grad_scale = p.grad_scale;
+    dp.reduction = p.reduction;
+    dp.hdr = hdr;
+    dp.dz = dz;
+    dp.ldd = L.ldd;
+    dp.dzt = dzt;
+    dp.ldt = L.ldt;
+    FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
+
+    // ---- grad_h = m dz W
+    if (gh) {
+      GemmParams b;
+      std::memset(&b, 0, sizeof(b));
+      b.M = rows;
+      b.N = H;
+      b.K = V;
+      b.m_tiles = (rows + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (V + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 8);
+      b.alpha = p.out_mult;
+      b.M_valid = rows;
+      b.N_valid = H;
+      b.out = static_cast<uint16_t*>(c.grad_h) + r0 * H;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      if (simt) {
+        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_simt(EPI_BF16, dz, L.ldd, wt, L.ldwt, b, stream));
+      } else {
+        CUtensorMap map_dz;
+        if (!encode_bf16(&map_dz, dz, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
+        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, &map_dz, &map_wt, b,
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream));
+      }
+    }
+
+    // ---- grad_W += m dz^T h_c
+    if (gw) {
+      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_bf16(static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, n.ld_h,
+                                                       rows, H, ht, L.ldht, stream));
+      GemmParams b;
+      std::memset(&b, 0, sizeof(b));
+      b.M = V;
+      b.N = H;
+      b.K = rows;
+      b.m_tiles = (V + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (rows + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = V;
+      b.N_valid = H;
+      b.out = c.grad_W;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      if (simt) {
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_simt(EPI_ACC_F32, dzt, L.ldt, ht, L.ldht, b, stream));
+      } else {
+        CUtensorMap map_dzt, map_ht;
+        if (!encode_bf16(&map_dzt, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
+        if (!encode_bf16(&map_ht, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, &map_dzt, &map_ht, b,
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream));
+      }
+    }
+  }
+
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void flce_default_params(flce_params* p) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+  p->softcap = 0.f;
+  p->out_mult = 1.f;
+  p->ignore_index = -100;
+  p->reduction = FLCE_REDUCTION_MEAN;
+  p->grad_scale = 1.f;
+}
+
+size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W) {
+  Norm n;
+  if (normalise(p, &n) != FLCE_OK) return 0;
+  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_FORWARD_BACKWARD) return 0;
+  Layout L;
+  make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
+  return L.total;
+}
+
+int flce_ce_only(const flce_params* p, const void* h, const void* W, const int64_t* labels, float* loss,
+                 float* token_accuracy, void* workspace, size_t workspace_bytes, void* stream) {
+  Call c{FLCE_MODE_CE_ONLY, h, W, labels, loss, token_accuracy, nullptr, nullptr, nullptr, nullptr,
+         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run(p, c);
+}
+
+int flce_forward(const flce_params* p, const void* h, const void* W, const int64_t* labels, float* loss,
+                 float* token_accuracy, int64_t* predicted, float* row_lse, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  Call c{FLCE_MODE_FORWARD, h, W, labels, loss, token_accuracy, predicted, row_lse, nullptr, nullptr,
+         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run(p, c);
+}
+
+int flce_forward_backward(const flce_params* p, const void* h, const void* W, const int64_t* labels, float* loss,
+                          float* token_accuracy, int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  Call c{FLCE_MODE_FORWARD_BACKWARD, h, W, labels, loss, token_accuracy, predicted, nullptr, grad_h, grad_W,
+         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run(p, c);
+}
+
+int flce_get_status(const void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return FLCE_ERR_ARG;
+  int32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FLCE_ERR_CUDA;
+  *status = v;
+  return FLCE_OK;
+}
+
+const char* flce_status_string(int code) {
+  switch (code) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_ARG: return "invalid argument";
+    case FLCE_ERR_ALIGN: return "misaligned pointer, stride or hidden size";
+    case FLCE_ERR_WORKSPACE: return "workspace too small";
+    case FLCE_ERR_UNSUPPORTED: return "unsupported device or tensor layout";
+    case FLCE_ERR_CUDA: return "CUDA runtime error";
+    case FLCE_ERR_LABEL: return "label outside [0, V) that is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT: return "bad label and device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int64_t flce_launch_count(void) { return g_launches.load(); }
+
+int flce_profile_begin(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof.clear();
+  g_prof_on = enable != 0;
+  return FLCE_OK;
+}
+
+int flce_profile_read(int64_t* launches, double* total_ms, int n) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < n; ++i) {
+    if (launches) launches[i] = 0;
+    if (total_ms) total_ms[i] = 0.0;
+  }
+  int rc = FLCE_NUM_KERNELS;
+  for (auto& r : g_prof) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+      rc = -FLCE_ERR_CUDA;
+    }
+    if (r.kernel >= 0 && r.kernel < n) {
+      if (launches) launches[r.kernel] += 1;
+      if (total_ms) total_ms[r.kernel] += ms;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof.clear();
+  return rc;
+}
+
+const char* flce_kernel_name(int id) {
+  if (id < 0 || id >= FLCE_NUM_KERNELS) return "unknown";
+  return kKernelNames[id];
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Per-row forward statistics shared by the tensor-core GEMM epilogue and the
+// debug path: softcap, running max / sum of exponentials, argmax and the
+// label's capped logit over one 256-column vocab tile of one row.
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+namespace flce {
+
+// Capped logit (Liger-Kernel "Muse Glimmer" page, Details / Softcap): the fused
+// path sees z = m (h W^T) with m applied as the GEMM scale, and caps it as
+// T tanh(z / T). T = 0 leaves z unchanged. Columns at or past V get -inf so
+// they drop out of the max, the sum and the argmax.
+__device__ __forceinline__ float cap_logit(float z, float softcap, float inv_softcap, bool in_vocab) {
+  const float s = softcap > 0.f ? softcap * tanhf(z * inv_softcap) : z;
+  return in_vocab ? s : -INFINITY;
+}
+
+struct RowStats {
+  float mx;    // running max of s over the tile so far (= value at the argmax)
+  float sum;   // sum of exp(s - mx)
+  int arg;     // vocab index of the first maximum
+  float tgt;   // s at the label column, when the label falls in this tile
+};
+
+__device__ __forceinline__ void row_stats_init(RowStats& st, int col0) {
+  st.mx = -INFINITY;
+  st.sum = 0.f;
+  st.arg = col0;
+  st.tgt = 0.f;
+}
+
+// One level of the pairwise argmax tree: slot j takes the larger of slots j and
+// j + W; on equal values the lower column wins.
+template <int W>
+__device__ __forceinline__ void tree_level(float (&v)[16], int (&ix)[16]) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    const bool right = (v[j + W] > v[j]) || (v[j + W] == v[j] && ix[j + W] < ix[j]);
+    v[j] = right ? v[j + W] : v[j];
+    ix[j] = right ? ix[j + W] : ix[j];
+  }
+}
+
+// Folds 32 consecutive columns col0 .. col0+31 of one row into `st`.
+// Ties keep the lower column (pairwise tree that prefers the left operand,
+// and a strict comparison against the running max of earlier columns).
+__device__ __forceinline__ void row_stats_update32(RowStats& st, const float (&s)[32], int col0,
+                                                   int64_t label) {
+  float v[16];
+  int ix[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool right = s[j + 16] > s[j];
+    v[j] = right ? s[j + 16] : s[j];
+    ix[j] = right ? j + 16 : j;
+  }
+  tree_level<8>(v, ix);
+  tree_level<4>(v, ix);
+  tree_level<2>(v, ix);
+  tree_level<1>(v, ix);
+  const float cm = v[0];
+  if (cm > st.mx) {
+    st.sum *= __expf(st.mx - cm);
+    st.mx = cm;
+    st.arg = col0 + ix[0];
+  }
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    a0 += __expf(s[j + 0] - st.mx);
+    a1 += __expf(s[j + 1] - st.mx);
+    a2 += __expf(s[j + 2] - st.mx);
+    a3 += __expf(s[j + 3] - st.mx);
+  }
+  st.sum += (a0 + a1) + (a2 + a3);
+  // Label gather without a dynamically indexed (local-memory) array: a
+  // predicated select per column.
+  const int64_t d64 = label - col0;
+  const int d = (d64 >= 0 && d64 < 32) ? static_cast<int>(d64) : -1;
+  float t = st.tgt;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool hit = (j == d);
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q mov.f32 %0, %1;\n\t}\n"
+        : "+f"(t)
+        : "f"(s[j]), "r"(static_cast<uint32_t>(hit)));
+  }
+  st.tgt = t;
+}
+
+}  // namespace flce

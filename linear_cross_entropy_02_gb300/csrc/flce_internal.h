@@ -1,0 +1,140 @@
+// Internal interface between the host engine and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "flce.h"
+
+namespace flce {
+
+// Tile of the tensor-core GEMMs: 128 rows of D per CTA (one TMEM lane per row),
+// 256 columns (fp32 accumulator = 256 TMEM columns, two buffers = all 512),
+// 64-element K slices (one 128-byte swizzle row per operand row).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: epilogue
+constexpr int kAStageBytes = kBM * kBK * 2;
+constexpr int kBStageBytes = kBN * kBK * 2;
+constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
+
+// Vocab columns per forward statistics partial (= the GEMM's N tile).
+constexpr int kVTile = kBN;
+
+// Workspace header (offset 0 of every workspace).
+struct Header {
+  int32_t status;    // FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT bits
+  uint32_t ticket;   // last-block election in the merge kernel
+  int64_t n_valid;   // rows whose label is not ignore_index
+  double loss_sum;   // sum of row losses over finished chunks (fixed order)
+  int64_t correct;   // valid rows whose argmax equals the label
+};
+
+enum KernelId {
+  K_PROLOGUE = 0,
+  K_FWD_GEMM = 1,
+  K_MERGE = 2,
+  K_DLOGITS = 3,
+  K_GRADH_GEMM = 4,
+  K_GRADW_GEMM = 5,
+  K_TRANSPOSE_W = 6,
+  K_TRANSPOSE_H = 7,
+  K_FINISH = 8,
+  K_SIMT_STATS = 9,
+};
+
+enum EpiMode {
+  EPI_STATS = 0,        // forward statistics partials only
+  EPI_STATS_STORE = 1,  // statistics partials + capped logits s stored (fp32)
+  EPI_BF16 = 2,         // out = bf16(alpha * acc)
+  EPI_ACC_F32 = 3,      // out += alpha * acc (fp32)
+};
+
+struct GemmParams {
+  // D [M, N] = A [M, K] * B [N, K]^T, both operands K-major bf16.
+  int M, N, K;
+  int m_tiles, n_tiles, k_iters, group_m;
+  int a_row0, b_row0;  // row offsets added to the TMA row coordinates
+  float alpha;
+  int M_valid;  // rows of D that are written
+  int N_valid;  // columns of D that are valid
+  // statistics epilogue
+  float softcap, inv_softcap;
+  const int64_t* labels;  // labels of D's rows (already offset to row 0 of D)
+  int64_t ignore_index;
+  float* part_max;  // [n_tiles][ldp]
+  float* part_sum;  // [n_tiles][ldp]
+  int32_t* part_idx;  // [n_tiles][ldp]
+  float* tgt;       // [ldp]  capped logit at the label
+  int ldp;
+  float* zbuf;  // capped logits [rows][ldz] (STATS_STORE, and the SIMT path)
+  int64_t ldz;
+  // plain epilogues
+  void* out;
+  int64_t ldo;
+  // control
+  int32_t* status;
+  uint64_t timeout_ns;
+  int debug_flags;
+};
+
+// Tensor-core GEMM (tcgen05 + TMA + TMEM), persistent over `grid` CTAs.
+cudaError_t launch_gemm_tc(int mode, const CUtensorMap* a, const CUtensorMap* b, const GemmParams& p,
+                           int grid, cudaStream_t s);
+// Debug GEMM on the fp32 FMA pipes; writes alpha*acc to zbuf for the statistics
+// modes (then run launch_stats_from_z) and behaves like the tensor-core GEMM
+// for the plain modes.
+cudaError_t launch_gemm_simt(int mode, const void* A, int64_t lda, const void* B, int64_t ldb,
+                             const GemmParams& p, cudaStream_t s);
+cudaError_t launch_stats_from_z(const GemmParams& p, int rows, bool store, cudaStream_t s);
+
+cudaError_t launch_prologue(const int64_t* labels, int64_t n, int64_t vocab, int64_t ignore_index,
+                            Header* hdr, cudaStream_t s);
+struct MergeParams {
+  int rows;            // rows in this chunk
+  int n_vtiles;
+  int ldp;
+  const float* part_max;
+  const float* part_sum;
+  const int32_t* part_idx;
+  const float* tgt;
+  const int64_t* labels;  // chunk labels
+  int64_t ignore_index;
+  float* lse;             // [rows] chunk workspace
+  int64_t* predicted;     // global output offset to the chunk, or null
+  float* row_lse;         // global output offset to the chunk, or null
+  double* block_loss;     // [blocks]
+  int64_t* block_correct; // [blocks]
+  Header* hdr;
+};
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+
+struct DlogitParams {
+  int rows, vocab;
+  const float* s;   // capped logits [rows][lds]
+  int64_t lds;
+  const float* lse; // [rows]
+  const int64_t* labels;
+  int64_t ignore_index;
+  float softcap, inv_softcap;
+  float grad_scale;
+  int reduction;
+  const Header* hdr;
+  uint16_t* dz;     // bf16 [rows][ldd] or null
+  int64_t ldd;
+  uint16_t* dzt;    // bf16 [vocab][ldt] or null
+  int64_t ldt;
+};
+cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s);
+
+// out [cols][ldo] = in [rows][ldi]^T, bf16.
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int cols, uint16_t* out,
+                                  int64_t ldo, cudaStream_t s);
+
+cudaError_t launch_finish(const Header* hdr, int reduction, float* loss, float* token_accuracy,
+                          cudaStream_t s);
+
+}  // namespace flce

@@ -1,0 +1,438 @@
+// The bandwidth-bound and bookkeeping kernels of the fused linear cross-entropy
+// path, plus the debug fp32-FMA GEMM:
+//   prologue      label check, n_valid, reset of the device scalars
+//   merge         per-row merge of the vocab-tile statistics: lse, argmax,
+//                 row loss; fixed-order reduction into the batch sums
+//   dlogits       dz = c (softmax - onehot) (1 - (s/T)^2) in bf16, written
+//                 row-major (A operand of grad_h) and transposed (A operand of
+//                 grad_W)
+//   transpose     bf16 transposes that give the backward GEMMs K-major operands
+//   finish        loss and token accuracy scalars
+//   simt gemm     fp32 FMA GEMM + statistics from stored logits (debug path)
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "flce_epilogue.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  const __nv_bfloat16 v = __float2bfloat16_rn(f);
+  return *reinterpret_cast<const uint16_t*>(&v);
+}
+
+// ------------------------------------------------------------------ prologue
+// One block: counts rows whose label is not ignore_index, flags labels outside
+// [0, V), and resets the batch sums. Deterministic (no atomics).
+__global__ void __launch_bounds__(1024) prologue_kernel(const int64_t* __restrict__ labels, int64_t n,
+                                                        int64_t vocab, int64_t ignore_index, Header* hdr) {
+  __shared__ long long s_cnt[32];
+  __shared__ int s_bad[32];
+  long long cnt = 0;
+  int bad = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t y = labels[i];
+    if (y != ignore_index) {
+      ++cnt;
+      if (y < 0 || y >= vocab) bad = 1;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    s_cnt[w] = cnt;
+    s_bad[w] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    int b = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      c += s_cnt[i];
+      b |= s_bad[i];
+    }
+    hdr->status = b ? FLCE_ERR_LABEL : 0;
+    hdr->ticket = 0;
+    hdr->n_valid = c;
+    hdr->loss_sum = 0.0;
+    hdr->correct = 0;
+  }
+}
+
+cudaError_t launch_prologue(const int64_t* labels, int64_t n, int64_t vocab, int64_t ignore_index, Header* hdr,
+                            cudaStream_t s) {
+  prologue_kernel<<<1, 1024, 0, s>>>(labels, n, vocab, ignore_index, hdr);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ merge
+constexpr int kMergeThreads = 128;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  __shared__ double s_loss[kMergeThreads / 32];
+  __shared__ long long s_corr[kMergeThreads / 32];
+  __shared__ bool s_last;
+  const int row = blockIdx.x * kMergeThreads + threadIdx.x;
+  double loss_i = 0.0;
+  long long corr_i = 0;
+  if (row < p.rows) {
+    float mx = -INFINITY, sum = 0.f;
+    int arg = 0;
+    for (int t = 0; t < p.n_vtiles; ++t) {
+      const int64_t o = static_cast<int64_t>(t) * p.ldp + row;
+      const float pm = p.part_max[o];
+      const float ps = p.part_sum[o];
+      if (pm > mx) {
+        sum = sum * expf(mx - pm) + ps;
+        mx = pm;
+        arg = p.part_idx[o];
+      } else {
+        sum += ps * expf(pm - mx);
+      }
+    }
+    const float lse = mx + logf(sum);
+    p.lse[row] = lse;
+    const int64_t y = p.labels[row];
+    if (y != p.ignore_index) {
+      loss_i = static_cast<double>(lse) - static_cast<double>(p.tgt[row]);
+      corr_i = (static_cast<int64_t>(arg) == y) ? 1 : 0;
+    }
+    if (p.predicted) p.predicted[row] = arg;
+    if (p.row_lse) p.row_lse[row] = lse;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    loss_i += __shfl_xor_sync(0xffffffffu, loss_i, o);
+    corr_i += __shfl_xor_sync(0xffffffffu, corr_i, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    s_loss[w] = loss_i;
+    s_corr[w] = corr_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double bl = 0.0;
+    long long bc = 0;
+    for (int i = 0; i < kMergeThreads / 32; ++i) {
+      bl += s_loss[i];
+      bc += s_corr[i];
+    }
+    p.block_loss[blockIdx.x] = bl;
+    p.block_correct[blockIdx.x] = bc;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(&p.hdr->ticket, 1u);
+    s_last = (ticket == gridDim.x - 1);
+  }
+  __syncthreads();
+  // The last block to finish adds the block sums in block order, so the result
+  // does not depend on which block finished when.
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    double tl = 0.0;
+    long long tc = 0;
+    for (unsigned int b = 0; b < gridDim.x; ++b) {
+      tl += reinterpret_cast<volatile double*>(p.block_loss)[b];
+      tc += reinterpret_cast<volatile long long*>(p.block_correct)[b];
+    }
+    p.hdr->loss_sum += tl;
+    p.hdr->correct += tc;
+    p.hdr->ticket = 0;
+  }
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
+  const int blocks = (p.rows + kMergeThreads - 1) / kMergeThreads;
+  if (blocks == 0) return cudaSuccess;
+  merge_kernel<<<blocks, kMergeThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dlogits
+// 64x64 tile per 256-thread block. Thread (ty, tx) handles rows ty + 16 k and
+// columns 4 tx .. 4 tx + 3, so reads of s (fp32) and writes of dz (bf16) are
+// contiguous along a row; the transposed copy goes through shared memory.
+constexpr int kDzTile = 64;
+
+__global__ void __launch_bounds__(256) dlogits_kernel(const DlogitParams p) {
+  __shared__ uint16_t tile[kDzTile][kDzTile + 2];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = blockIdx.y * kDzTile, c0 = blockIdx.x * kDzTile;
+  const int64_t n_valid = p.hdr->n_valid;
+  float coef;
+  if (n_valid == 0) {
+    coef = 0.f;
+  } else {
+    coef = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lr = ty + 16 * k;
+    const int r = r0 + lr;
+    const int c = c0 + tx * 4;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < p.rows) {
+      const int64_t y = p.labels[r];
+      const bool valid = y != p.ignore_index;
+      const float ci = valid ? coef : 0.f;
+      const float lse = p.lse[r];
+      const float* srow = p.s + static_cast<int64_t>(r) * p.lds;
+      if (c + 3 < p.vocab) {
+        const float4 v = *reinterpret_cast<const float4*>(srow + c);
+        const float sv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float q = ci * (__expf(sv[j] - lse) - ((c + j) == y ? 1.f : 0.f));
+          if (p.softcap > 0.f) {
+            const float u = sv[j] * p.inv_softcap;
+            q *= (1.f - u * u);
+          }
+          d[j] = q;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (c + j < p.vocab) {
+            const float sv = srow[c + j];
+            float q = ci * (__expf(sv - lse) - ((c + j) == y ? 1.f : 0.f));
+            if (p.softcap > 0.f) {
+              const float u = sv * p.inv_softcap;
+              q *= (1.f - u * u);
+            }
+            d[j] = q;
+          }
+        }
+      }
+    }
+    uint16_t b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      b[j] = float_to_bf16_bits(d[j]);
+      tile[lr][tx * 4 + j] = b[j];
+    }
+    if (p.dz && r < p.rows && c < p.vocab) {
+      uint16_t* drow = p.dz + static_cast<int64_t>(r) * p.ldd;
+      if (c + 3 < p.vocab) {
+        uint2 pk;
+        pk.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
+        pk.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
+        *reinterpret_cast<uint2*>(drow + c) = pk;
+      } else {
+        for (int j = 0; j < 4; ++j)
+          if (c + j < p.vocab) drow[c + j] = b[j];
+      }
+    }
+  }
+  if (!p.dzt) return;
+  __syncthreads();
+  // dzt [vocab][ldt]: row = vocab column, contiguous along the chunk rows.
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lc = ty + 16 * k;
+    const int c = c0 + lc;
+    const int r = r0 + tx * 4;
+    if (c < p.vocab && r < p.rows) {
+      uint16_t* trow = p.dzt + static_cast<int64_t>(c) * p.ldt;
+      if (r + 3 < p.rows) {
+        uint2 pk;
+        pk.x = static_cast<uint32_t>(tile[tx * 4 + 0][lc]) | (static_cast<uint32_t>(tile[tx * 4 + 1][lc]) << 16);
+        pk.y = static_cast<uint32_t>(tile[tx * 4 + 2][lc]) | (static_cast<uint32_t>(tile[tx * 4 + 3][lc]) << 16);
+        *reinterpret_cast<uint2*>(trow + r) = pk;
+      } else {
+        for (int j = 0; j < 4; ++j)
+          if (r + j < p.rows) trow[r + j] = tile[tx * 4 + j][lc];
+      }
+    }
+  }
+}
+
+cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s) {
+  if (p.rows <= 0 || p.vocab <= 0) return cudaSuccess;
+  dim3 grid((p.vocab + kDzTile - 1) / kDzTile, (p.rows + kDzTile - 1) / kDzTile);
+  dlogits_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ transpose
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t ldi,
+                                                             int rows, int cols, uint16_t* __restrict__ out,
+                                                             int64_t ldo) {
+  __shared__ uint16_t tile[64][66];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lr = ty + 16 * k;
+    const int r = r0 + lr;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + tx * 4 + j;
+      tile[lr][tx * 4 + j] = (r < rows && c < cols) ? in[static_cast<int64_t>(r) * ldi + c] : 0;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lc = ty + 16 * k;
+    const int c = c0 + lc;
+    if (c >= cols) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = r0 + tx * 4 + j;
+      if (r < rows) out[static_cast<int64_t>(c) * ldo + r] = tile[tx * 4 + j][lc];
+    }
+  }
+}
+
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int cols, uint16_t* out, int64_t ldo,
+                                  cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid((cols + 63) / 64, (rows + 63) / 64);
+  transpose_bf16_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ finish
+__global__ void finish_kernel(const Header* hdr, int reduction, float* loss, float* token_accuracy) {
+  const int64_t nv = hdr->n_valid;
+  float l = 0.f, a = 0.f;
+  if (nv > 0) {
+    l = reduction == FLCE_REDUCTION_MEAN ? static_cast<float>(hdr->loss_sum / static_cast<double>(nv))
+                                         : static_cast<float>(hdr->loss_sum);
+    a = static_cast<float>(static_cast<double>(hdr->correct) / static_cast<double>(nv));
+  }
+  if (loss) *loss = l;
+  if (token_accuracy) *token_accuracy = a;
+}
+
+cudaError_t launch_finish(const Header* hdr, int reduction, float* loss, float* token_accuracy, cudaStream_t s) {
+  finish_kernel<<<1, 1, 0, s>>>(hdr, reduction, loss, token_accuracy);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ debug SIMT GEMM
+// 64x64 tile per 256-thread block, 4x4 outputs per thread, fp32 FMA.
+template <int MODE>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const uint16_t* __restrict__ A, int64_t lda,
+                                                        const uint16_t* __restrict__ B, int64_t ldb,
+                                                        const GemmParams p) {
+  __shared__ float As[32][65];
+  __shared__ float Bs[32][65];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < p.K; k0 += 32) {
+    for (int e = threadIdx.x; e < 64 * 32; e += 256) {
+      const int r = e >> 5, c = e & 31;
+      const int gm = m0 + r, gn = n0 + r, gk = k0 + c;
+      As[c][r] = (gm < p.M_valid && gk < p.K)
+                     ? bf16_bits_to_float(A[static_cast<int64_t>(p.a_row0 + gm) * lda + gk])
+                     : 0.f;
+      Bs[c][r] = (gn < p.N && gk < p.K) ? bf16_bits_to_float(B[static_cast<int64_t>(p.b_row0 + gn) * ldb + gk])
+                                       : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm >= p.M_valid) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx * 4 + j;
+      if (gn >= p.N_valid) continue;
+      const float v = acc[i][j] * p.alpha;
+      if (MODE == EPI_STATS || MODE == EPI_STATS_STORE) {
+        p.zbuf[static_cast<int64_t>(gm) * p.ldz + gn] = v;
+      } else if (MODE == EPI_BF16) {
+        static_cast<uint16_t*>(p.out)[static_cast<int64_t>(gm) * p.ldo + gn] = float_to_bf16_bits(v);
+      } else {
+        static_cast<float*>(p.out)[static_cast<int64_t>(gm) * p.ldo + gn] += v;
+      }
+    }
+  }
+}
+
+cudaError_t launch_gemm_simt(int mode, const void* A, int64_t lda, const void* B, int64_t ldb, const GemmParams& p,
+                             cudaStream_t s) {
+  if (p.M_valid <= 0 || p.N <= 0) return cudaSuccess;
+  dim3 grid((p.N + 63) / 64, (p.M_valid + 63) / 64);
+  const uint16_t* a = static_cast<const uint16_t*>(A);
+  const uint16_t* b = static_cast<const uint16_t*>(B);
+  switch (mode) {
+    case EPI_STATS:
+    case EPI_STATS_STORE: gemm_simt_kernel<EPI_STATS><<<grid, 256, 0, s>>>(a, lda, b, ldb, p); break;
+    case EPI_BF16: gemm_simt_kernel<EPI_BF16><<<grid, 256, 0, s>>>(a, lda, b, ldb, p); break;
+    case EPI_ACC_F32: gemm_simt_kernel<EPI_ACC_F32><<<grid, 256, 0, s>>>(a, lda, b, ldb, p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// Statistics of one 256-column vocab tile per thread-row from the logits the
+// SIMT GEMM stored (z = m h W^T in zbuf); optionally overwrites them with the
+// capped logits s for the dlogits pass.
+__global__ void __launch_bounds__(128) stats_from_z_kernel(const GemmParams p, int rows, int store) {
+  const int nb = blockIdx.x;
+  const int row = blockIdx.y * 128 + threadIdx.x;
+  if (row >= rows) return;
+  const int n0 = nb * kVTile;
+  const int64_t label = p.labels[row];
+  const bool has_label = label != p.ignore_index && label >= n0 && label < n0 + kVTile;
+  float* zrow = p.zbuf + static_cast<int64_t>(row) * p.ldz;
+  RowStats st;
+  row_stats_init(st, n0);
+  for (int c = 0; c < kVTile / 32; ++c) {
+    float s[32];
+    const int col0 = n0 + c * 32;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const bool in = col0 + j < p.N_valid;
+      s[j] = cap_logit(in ? zrow[col0 + j] : 0.f, p.softcap, p.inv_softcap, in);
+    }
+    if (store) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N_valid) zrow[col0 + j] = s[j];
+    }
+    row_stats_update32(st, s, col0, has_label ? label : -1);
+  }
+  const int64_t o = static_cast<int64_t>(nb) * p.ldp + row;
+  p.part_max[o] = st.mx;
+  p.part_sum[o] = st.sum;
+  p.part_idx[o] = st.arg;
+  if (has_label) p.tgt[row] = st.tgt;
+}
+
+cudaError_t launch_stats_from_z(const GemmParams& p, int rows, bool store, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  dim3 grid(p.n_tiles, (rows + 127) / 128);
+  stats_from_z_kernel<<<grid, 128, 0, s>>>(p, rows, store ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/flce.h declares, sizes its workspace independently of
+N beyond one chunk, and rejects bad arguments with status codes before any
+device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_cross_entropy_02_gb300 import _lib
+    return _lib.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "flce.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert "flce_forward_backward" in names and "flce_ce_only" in names and "flce_forward" in names
+    for n in names:
+        assert hasattr(L, n), n
+    from linear_cross_entropy_02_gb300 import _lib
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_header_constants_match_binding():
+    from linear_cross_entropy_02_gb300 import _lib
+    with open(os.path.join(ROOT, "include", "flce.h")) as f:
+        src = f.read()
+    for name, val in re.findall(r"#define (FLCE_[A-Z0-9_]+) (\d+)", src):
+        assert getattr(_lib, name) == int(val), name
+
+
+def _params(L, N=4096, H=512, V=4096, **kw):
+    from linear_cross_entropy_02_gb300._lib import FlceParams
+    p = FlceParams()
+    L.flce_default_params(ctypes.byref(p))
+    p.n_rows, p.hidden, p.vocab = N, H, V
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_default_params(L):
+    p = _params(L)
+    assert p.out_mult == 1.0 and p.softcap == 0.0 and p.ignore_index == -100
+    assert p.grad_scale == 1.0 and p.reduction == 0 and p.chunk_rows == 0
+
+
+def test_workspace_independent_of_n_beyond_a_chunk(L):
+    sizes = []
+    for N in (8192, 16384, 32768, 65536):
+        p = _params(L, N=N, H=7168, V=129280, chunk_rows=8192)
+        sizes.append(L.flce_workspace_size(ctypes.byref(p), 2, 1, 1))
+    assert len(set(sizes)) == 1 and sizes[0] > 0
+    # transient is O(C V): far below a [N, V] fp32 logits tensor at N = 32768
+    assert sizes[0] < 32768 * 129280 * 4
+    # CE-only keeps no logits at all: only per-tile statistics
+    p = _params(L, N=131072, H=4096, V=151936)
+    ce = L.flce_workspace_size(ctypes.byref(p), 0, 0, 0)
+    assert 0 < ce < 100e6
+    # frozen W (no grad_W) needs no transposed dlogits
+    p = _params(L, N=32768, H=7168, V=129280)
+    assert L.flce_workspace_size(ctypes.byref(p), 2, 1, 0) < L.flce_workspace_size(ctypes.byref(p), 2, 1, 1)
+
+
+@pytest.mark.parametrize("field,value", [("hidden", 0), ("vocab", 0), ("n_rows", -1), ("softcap", -1.0),
+                                         ("reduction", 7), ("chunk_rows", -5), ("ld_h", 100)])
+def test_workspace_size_rejects_bad_params(L, field, value):
+    p = _params(L, **{field: value})
+    assert L.flce_workspace_size(ctypes.byref(p), 2, 1, 1) == 0
+
+
+def test_host_errors_before_any_device_work(L):
+    from linear_cross_entropy_02_gb300 import _lib as B
+    fake = ctypes.c_void_p(1 << 20)          # never dereferenced: every call below fails on the host
+    p = _params(L)
+    # too-small workspace
+    rc = L.flce_forward_backward(ctypes.byref(p), fake, fake, fake, fake, None, None, fake, fake, fake, 256, None)
+    assert rc == B.FLCE_ERR_WORKSPACE
+    # null loss
+    rc = L.flce_ce_only(ctypes.byref(p), fake, fake, fake, None, None, fake, 1 << 40, None)
+    assert rc == B.FLCE_ERR_ARG
+    # misaligned h
+    rc = L.flce_ce_only(ctypes.byref(p), ctypes.c_void_p((1 << 20) + 2), fake, fake, fake, None, fake, 1 << 40,
+                        None)
+    assert rc == B.FLCE_ERR_ALIGN
+    # H not a multiple of 8
+    p2 = _params(L, H=100)
+    rc = L.flce_ce_only(ctypes.byref(p2), fake, fake, fake, fake, None, fake, 1 << 40, None)
+    assert rc == B.FLCE_ERR_ALIGN
+    # negative softcap
+    p3 = _params(L, softcap=-2.0)
+    rc = L.flce_forward(ctypes.byref(p3), fake, fake, fake, fake, None, None, None, fake, 1 << 40, None)
+    assert rc == B.FLCE_ERR_ARG
+    # null params
+    assert L.flce_ce_only(None, fake, fake, fake, fake, None, fake, 1 << 40, None) == B.FLCE_ERR_ARG
+
+
+def test_status_strings(L):
+    for code in (0, 1, 2, 3, 4, 5, 16, 32, 48, 999):
+        s = L.flce_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert L.flce_status_string(32) == b"bounded device wait timed out"
+
+
+def test_kernel_names(L):
+    names = [L.flce_kernel_name(i).decode() for i in range(10)]
+    assert names[1] == "fwd_gemm_stats" and names[4] == "grad_h_gemm" and names[5] == "grad_W_gemm"
+    assert L.flce_kernel_name(99) == b"unknown"
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import linear_cross_entropy_02_gb300 as flce
+    h = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(16, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA"):
+        flce.flce_ce_only(h, W, y)
