@@ -1,0 +1,345 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused linear cross-entropy (FLCE) forward+backward on GB300.
+
+One step = one flce_forward_backward call over the whole batch of a synthetic
+LM-head workload (default: the DeepSeek-V3-shaped head, N=32768 rows, H=7168,
+V=129280, Zipf(1.1) labels with 3% ignored, fp32 grad_W accumulator): forward
+GEMM with the fused statistics epilogue, merge, dlogits, grad_h GEMM and grad_W
+GEMM for every row chunk. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dsv3] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+single-GPU path has no exchange step); rank 0 prints the whole-job line.
+`--impl reference` times the CPU fp64 oracle on bounded row samples of the
+same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s and TFLOP/s (6·N·H·V) as % of GB300 bf16 tensor peak"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _config(w: workloads.Workload, chunk_rows: int):
+    return {"workload": f"{w.name}: N={w.n_rows} H={w.hidden} V={w.vocab} "
+                        f"{'zipf(%g)' % w.zipf_s if w.labels == 'zipf' else 'uniform'} labels, "
+                        f"{int(round(w.ignore_frac * 100))}% ignored, T={w.softcap}, m={w.out_mult}, "
+                        f"mode={w.mode}",
+            "n_rows": w.n_rows, "hidden": w.hidden, "vocab": w.vocab, "softcap": w.softcap,
+            "out_mult": w.out_mult, "mode": w.mode, "chunk_rows": chunk_rows,
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    try:
+                        rows.append((float(parts[1]), float(parts[2]), float(parts[3]) if parts[3] not in
+                                     ("[N/A]", "N/A") else 0.0, parts[5:9]))
+                    except ValueError:
+                        pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return ws, rank, local, dist
+    return 1, 0, 0, None
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def weight_f64(W_cpu: torch.Tensor) -> np.ndarray:
+    return W_cpu.float().numpy().astype(np.float64)
+
+
+def cpu_oracle_rate(w: workloads.Workload, W64: np.ndarray, h_rows: torch.Tensor, lab_rows: torch.Tensor,
+                    steps: int = 1):
+    """The CPU fp64 oracle, as it stands, on bounded row samples of the workload:
+    full forward+backward (logits over all V, grad_h rows, grad_W) for the sampled rows."""
+    from oracle import flce_oracle
+    times = []
+    R = h_rows.shape[0]
+    need_w = w.mode == "fwd_bwd"
+    need_h = w.mode != "ce_only"
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        flce_oracle(h_rows, W64, lab_rows, softcap=w.softcap, out_mult=w.out_mult,
+                    need_grad_h=need_h, need_grad_W=need_w)
+        times.append(time.perf_counter() - t0)
+    return R, times
+
+
+def run_reference(args, w):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    h, W, lab = workloads.make_inputs(w, n_rows=args.sample_rows * (args.steps + args.warmup))
+    W64 = weight_f64(W)
+    R = args.sample_rows
+    times = []
+    for s in range(args.warmup + args.steps):
+        hs, ls = h[s * R:(s + 1) * R], lab[s * R:(s + 1) * R]
+        _, t = cpu_oracle_rate(w, W64, hs, ls)
+        if s >= args.warmup:
+            times.append(t[0])
+    total = sum(times)
+    value = R * len(times) / total
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(w, 0),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{R} rows of the {w.name} head per step (all {w.vocab} logits, "
+                                       f"grad_h and grad_W), numpy fp64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    world, rank, local, dist = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import linear_cross_entropy_02_gb300 as flce
+
+    h_cpu, W_cpu, lab_cpu = workloads.make_inputs(w)
+    h = h_cpu.to(dev)
+    W = W_cpu.to(dev)
+    lab = lab_cpu.to(dev)
+    gW = torch.zeros(W.shape, dtype=torch.float32, device=dev) if w.mode == "fwd_bwd" else None
+    kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+
+    def step():
+        if w.mode == "ce_only":
+            return flce.flce_ce_only(h, W, lab, **kw)
+        return flce.flce_forward_backward(h, W, lab, grad_W=gW, need_grad_h=True,
+                                          return_predicted=w.return_predicted, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if flce.flce_get_status() != 0:
+        raise RuntimeError(f"device status {flce.flce_get_status()} after warm-up")
+
+    stream = torch.cuda.current_stream(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    launches0 = flce.flce_launch_count()
+    flce.flce_profile_begin(True)
+    with ClockSampler(local) as clk:
+        _barrier(dist)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+    kernels = flce.flce_profile_read()
+    flce.flce_profile_begin(False)
+    launches = flce.flce_launch_count() - launches0
+    ms = start.elapsed_time(stop) / args.steps
+    if flce.flce_get_status() != 0:
+        raise RuntimeError(f"device status {flce.flce_get_status()} after timed steps")
+    ms_max = _max_over_ranks(dist, ms)
+    rows_total = _sum_over_ranks(dist, float(w.n_rows))
+    value = rows_total / (ms_max / 1e3)
+
+    # end to end through the public API: inputs from pinned host memory, loss read back
+    h_pin = h_cpu.pin_memory()
+    lab_pin = lab_cpu.pin_memory()
+    res_pin = torch.empty(2, dtype=torch.float32).pin_memory()
+    h_dev = torch.empty_like(h)
+    lab_dev = torch.empty_like(lab)
+
+    def e2e_step():
+        h_dev.copy_(h_pin, non_blocking=True)
+        lab_dev.copy_(lab_pin, non_blocking=True)
+        if w.mode == "ce_only":
+            loss, acc = flce.flce_ce_only(h_dev, W, lab_dev, **kw)
+        else:
+            o = flce.flce_forward_backward(h_dev, W, lab_dev, grad_W=gW, need_grad_h=True,
+                                           return_predicted=w.return_predicted, **kw)
+            loss, acc = o["loss"], o["token_accuracy"]
+        res_pin[0:1].copy_(loss.view(1), non_blocking=True)
+        res_pin[1:2].copy_(acc.view(1), non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_step()
+    _barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_max = _max_over_ranks(dist, e2e_s)
+    e2e_value = rows_total / e2e_max
+
+    peaks = _peaks()
+    flops = w.flops
+    tflops = flops / (ms / 1e3) / 1e12
+    line = None
+    if rank == 0:
+        # roofline of the dominant kernel, from the per-launch events of the timed region
+        gemm_flops = {"fwd_gemm_stats": 2.0 * w.n_rows * w.hidden * w.vocab,
+                      "grad_h_gemm": 2.0 * w.n_rows * w.hidden * w.vocab,
+                      "grad_W_gemm": 2.0 * w.n_rows * w.hidden * w.vocab}
+        total_ms = sum(v[1] for v in kernels.values()) or 1.0
+        dom = max(kernels.items(), key=lambda kv: kv[1][1])[0] if kernels else None
+        roof = None
+        if dom in gemm_flops:
+            n_launch, tms = kernels[dom]
+            per_launch_flops = gemm_flops[dom] * args.steps / n_launch
+            achieved = per_launch_flops / (tms / n_launch / 1e3) / 1e12
+            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+                    "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
+                    "traffic": None, "algorithmic_flops_per_launch": per_launch_flops,
+                    "avg_launch_ms": tms / n_launch}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            R = args.sample_rows
+            n, t = cpu_oracle_rate(w, weight_f64(W_cpu), h_cpu[:R], lab_cpu[:R])
+            cpu = {"value": n / t[0], "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                   "sample": f"first {R} rows of the workload, full fp64 forward+backward over all "
+                             f"{w.vocab} logits (numpy)", "seconds": t[0]}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w, args.chunk_rows),
+            "tflops": tflops, "pct_of_peak": 100.0 * tflops / peaks["bf16_sustained"],
+            "peak_tflops": peaks["bf16_sustained"], "peak_source": peaks["source"],
+            "flops_per_step": flops,
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": h.numel() * 2 + lab.numel() * 8, "d2h_bytes_per_step": 8},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "kernels": {k: {"launches": v[0], "ms": v[1], "share": v[1] / total_ms} for k, v in kernels.items()},
+            "workspace_bytes": flce.flce_workspace_size(w.n_rows, w.hidden, w.vocab, chunk_rows=args.chunk_rows,
+                                                        need_grad_W=w.mode == "fwd_bwd"),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--sample-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

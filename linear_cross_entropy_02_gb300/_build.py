@@ -55,10 +55,24 @@ def _compile(src: str, ptxas_verbose: bool) -> str:
 
 
 def build(force: bool = False, ptxas_verbose: bool = True, quiet: bool = False) -> str:
-    """Compile every CUDA/C++ source of the library and link libflce.so."""
+    """Compile every CUDA/C++ source of the library and link libflce.so.
+    Several processes (one per rank) may call this at once: a file lock makes
+    one of them build and the others wait for it."""
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    import fcntl
+    with open(os.path.join(BUILD, ".lock"), "w") as lk:
+        fcntl.flock(lk, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale():
+                return LIB
+            return _build_locked(ptxas_verbose, quiet)
+        finally:
+            fcntl.flock(lk, fcntl.LOCK_UN)
+
+
+def _build_locked(ptxas_verbose: bool, quiet: bool) -> str:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, ptxas_verbose), SOURCES))
     tmp = LIB + ".tmp"
