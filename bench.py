@@ -329,10 +329,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--chunk-rows", type=int, default=0)
-    ap.add_argument("--sample-rows", type=int, default=64)
+    ap.add_argument("--sample-rows", type=int, default=16)
+    ap.add_argument("--rows", type=int, default=0, help="override N (profiling captures only)")
+    ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
+    if args.rows or args.vocab:
+        # a smaller case of the same head (used for profiler captures, never for the bench line)
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}-small", n_rows=args.rows or w.n_rows,
+                                vocab=args.vocab or w.vocab)
     if args.impl == "reference":
         run_reference(args, w)
     else:
