@@ -115,6 +115,23 @@ int flce_ce_only(const flce_params* p, const void* h, const void* W, const int64
                  float* loss, float* token_accuracy,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* CE-only pass that allocates nothing and takes no workspace: for callers that
+ * cannot allocate device memory where they need the loss (code inside an
+ * allocator's callbacks, hooks that run while a framework's allocator is
+ * locked, embeddings that forbid device allocations after start-up). The pages
+ * have no counterpart of this entry point; it exists only for such callers.
+ * Same computation and outputs as flce_ce_only; device_status (device int32,
+ * nullable) receives the call's status word (0, FLCE_ERR_LABEL, FLCE_ERR_TIMEOUT).
+ * Scratch is a fixed 64 MiB device array inside the library, reserved on every
+ * GPU that loads it until the process exits. chunk_rows = 0 picks the largest
+ * chunk (8192 down to 128 rows) that fits; FLCE_ERR_WORKSPACE means the
+ * vocabulary (or the given chunk_rows) needs more than 64 MiB. The first call
+ * on a device looks up the array's address and should come before any stream
+ * capture. All calls share the array: calls that overlap on the GPU race, so
+ * serialise them. No call allocates device memory. */
+int flce_ce_only_noalloc(const flce_params* p, const void* h, const void* W, const int64_t* labels,
+                         float* loss, float* token_accuracy, int32_t* device_status, void* stream);
+
 /* Forward: as flce_ce_only, plus optional per-row outputs predicted [N]
  * (int64, argmax for every row) and row_lse [N] (fp32 log-sum-exp of s_i). */
 int flce_forward(const flce_params* p, const void* h, const void* W, const int64_t* labels,

@@ -26,7 +26,7 @@ from ._lib import (FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL, FLCE_MODE_CE_ONLY,
                    FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
 
 __all__ = [
-    "flce_ce_only", "flce_forward", "flce_forward_backward", "flce_workspace_size", "flce_get_status",
+    "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward", "flce_workspace_size", "flce_get_status",
     "flce_launch_count", "flce_profile_begin", "flce_profile_read", "FlceError",
 ]
 
@@ -136,6 +136,30 @@ def flce_ce_only(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, 
                                  _ptr(ws), nbytes, _stream_handle(h.device))
     _raise(rc, "flce_ce_only")
     return loss, acc
+
+
+def flce_ce_only_noalloc(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                         chunk_rows=0, flags=0, timeout_ns=0):
+    """CE-only pass through the entry point that allocates no device memory in the
+    library (its scratch is a fixed 64 MiB device array), for callers that cannot
+    allocate. Returns (loss, token_accuracy, status) as 0-d CUDA tensors; the
+    outputs themselves are allocated here by torch, as any caller would."""
+    _check(h, W, labels)
+    H = W.shape[1]
+    h2 = _rows2d(h, H)
+    if W.stride(1) != 1 or W.stride(0) % 8 != 0 or W.data_ptr() % 16 != 0:
+        W = W.contiguous()
+    lab = labels.reshape(-1).contiguous()
+    p = _params(h2.shape[0], H, W.shape[0], h2.stride(0), W.stride(0), softcap, out_mult, ignore_index,
+                reduction, 1.0, chunk_rows, flags, timeout_ns)
+    dev = h.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    status = torch.zeros((), dtype=torch.int32, device=dev)
+    rc = _lib.lib().flce_ce_only_noalloc(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+                                         _ptr(status), _stream_handle(dev))
+    _raise(rc, "flce_ce_only_noalloc")
+    return loss, acc, status
 
 
 def flce_forward(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",

@@ -30,7 +30,7 @@ FLCE_FLAG_TEST_STALL = 2
 FLCE_NUM_KERNELS = 10
 
 EXPORTED = [
-    "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_forward",
+    "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
     "flce_forward_backward", "flce_get_status", "flce_status_string", "flce_launch_count",
     "flce_profile_begin", "flce_profile_read", "flce_kernel_name",
 ]
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.flce_workspace_size.restype = _sz
         L.flce_ce_only.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.flce_ce_only.restype = ctypes.c_int
+        L.flce_ce_only_noalloc.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.flce_ce_only_noalloc.restype = ctypes.c_int
         L.flce_forward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.flce_forward.restype = ctypes.c_int
         L.flce_forward_backward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
