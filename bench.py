@@ -193,24 +193,56 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+KERNEL_SOURCES = ["gemm_tc.cu", "flce_device.cuh", "flce_epilogue.cuh", "flce_internal.h", "kernels_aux.cu",
+                  "kernels_ce.cu"]
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the kernel sources: a recorded DRAM traffic figure is only
+    reported while the kernels are the ones it was measured on."""
+    import hashlib
+    hsh = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "linear_cross_entropy_02_gb300", "csrc", f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """Per-launch dram__bytes_read.sum + dram__bytes_write.sum from the committed
+    ncu capture summary, or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha256") != kernel_source_hash():
+        return None
+    return e["bytes_per_launch"]
+
+
 def run_ours(args, w):
     world, rank, local, dist = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import linear_cross_entropy_02_gb300 as flce
 
+    if args.ce_logits:
+        return run_ce_logits(args, w, world, rank, local, dist, flce)
     h_cpu, W_cpu, lab_cpu = workloads.make_inputs(w)
     h = h_cpu.to(dev)
     W = W_cpu.to(dev)
     lab = lab_cpu.to(dev)
     gW = torch.zeros(W.shape, dtype=torch.float32, device=dev) if w.mode == "fwd_bwd" else None
     kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+    bkw = dict(low_memory=args.low_memory, vocab_slab=args.vocab_slab)
 
     def step():
         if w.mode == "ce_only":
             return flce.flce_ce_only(h, W, lab, **kw)
         return flce.flce_forward_backward(h, W, lab, grad_W=gW, need_grad_h=True,
-                                          return_predicted=w.return_predicted, **kw)
+                                          return_predicted=w.return_predicted, **kw, **bkw)
 
     for _ in range(args.warmup):
         step()
@@ -256,7 +288,7 @@ def run_ours(args, w):
             loss, acc = flce.flce_ce_only(h_dev, W, lab_dev, **kw)
         else:
             o = flce.flce_forward_backward(h_dev, W, lab_dev, grad_W=gW, need_grad_h=True,
-                                           return_predicted=w.return_predicted, **kw)
+                                           return_predicted=w.return_predicted, **kw, **bkw)
             loss, acc = o["loss"], o["token_accuracy"]
         res_pin[0:1].copy_(loss.view(1), non_blocking=True)
         res_pin[1:2].copy_(acc.view(1), non_blocking=True)
@@ -280,7 +312,8 @@ def run_ours(args, w):
         # roofline of the dominant kernel, from the per-launch events of the timed region
         gemm_flops = {"fwd_gemm_stats": 2.0 * w.n_rows * w.hidden * w.vocab,
                       "grad_h_gemm": 2.0 * w.n_rows * w.hidden * w.vocab,
-                      "grad_W_gemm": 2.0 * w.n_rows * w.hidden * w.vocab}
+                      "grad_W_gemm": 2.0 * w.n_rows * w.hidden * w.vocab,
+                      "recompute_dz_gemm": 2.0 * w.n_rows * w.hidden * w.vocab}
         total_ms = sum(v[1] for v in kernels.values()) or 1.0
         dom = max(kernels.items(), key=lambda kv: kv[1][1])[0] if kernels else None
         roof = None
@@ -291,7 +324,9 @@ def run_ours(args, w):
             roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
                     "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
-                    "traffic": None, "algorithmic_flops_per_launch": per_launch_flops,
+                    "traffic": recorded_traffic(w.name + ("-lowmem" if args.low_memory else ""), dom),
+                    "traffic_unit": "bytes per launch (dram read + write, ncu)",
+                    "algorithmic_flops_per_launch": per_launch_flops,
                     "avg_launch_ms": tms / n_launch}
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -307,14 +342,117 @@ def run_ours(args, w):
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / peaks["bf16_sustained"],
             "peak_tflops": peaks["bf16_sustained"], "peak_source": peaks["source"],
             "flops_per_step": flops,
+            "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if args.low_memory and w.mode == "fwd_bwd"
+                                                       else 1.0),
+            "backward": "recompute (low memory)" if args.low_memory else "stored logits",
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h.numel() * 2 + lab.numel() * 8, "d2h_bytes_per_step": 8},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "kernels": {k: {"launches": v[0], "ms": v[1], "share": v[1] / total_ms} for k, v in kernels.items()},
-            "workspace_bytes": flce.flce_workspace_size(w.n_rows, w.hidden, w.vocab, chunk_rows=args.chunk_rows,
-                                                        need_grad_W=w.mode == "fwd_bwd"),
+            "workspace_bytes": flce.flce_workspace_size(
+                w.n_rows, w.hidden, w.vocab, chunk_rows=args.chunk_rows,
+                mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
+                need_grad_W=w.mode == "fwd_bwd", flags=flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_ce_logits(args, w, world, rank, local, dist, flce):
+    """Cross-entropy on materialised bf16 logits [N, V] (the workload's N and V)
+    with dL/dlogits: two streaming kernels, bounded by HBM bandwidth."""
+    dev = torch.device("cuda", local)
+    g = torch.Generator(device="cpu").manual_seed(w.seed * 16 + 9)
+    x_cpu = torch.empty((w.n_rows, w.vocab), dtype=torch.bfloat16)
+    step_rows = max(1, (1 << 26) // w.vocab)
+    for r0 in range(0, w.n_rows, step_rows):
+        r1 = min(w.n_rows, r0 + step_rows)
+        x_cpu[r0:r1] = (torch.randn((r1 - r0, w.vocab), generator=g) * 1.28).to(torch.bfloat16)
+    lab_cpu = workloads.make_labels(w.n_rows, w.vocab, w.seed, w.ignore_frac, w.labels, w.zipf_s)
+    x = x_cpu.to(dev)
+    lab = lab_cpu.to(dev)
+    kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+
+    def step():
+        return flce.flce_cross_entropy(x, lab, need_grad=True, return_predicted=False, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if flce.flce_get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    stream = torch.cuda.current_stream(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    launches0 = flce.flce_launch_count()
+    flce.flce_profile_begin(True)
+    with ClockSampler(local) as clk:
+        _barrier(dist)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+    kernels = flce.flce_profile_read()
+    flce.flce_profile_begin(False)
+    launches = flce.flce_launch_count() - launches0
+    ms = start.elapsed_time(stop) / args.steps
+    ms_max = _max_over_ranks(dist, ms)
+    rows_total = _sum_over_ranks(dist, float(w.n_rows))
+
+    x_pin = x_cpu.pin_memory()
+    lab_pin = lab_cpu.pin_memory()
+    res_pin = torch.empty(2, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    lab_dev = torch.empty_like(lab)
+
+    def e2e_step():
+        x_dev.copy_(x_pin, non_blocking=True)
+        lab_dev.copy_(lab_pin, non_blocking=True)
+        o = flce.flce_cross_entropy(x_dev, lab_dev, need_grad=True, return_predicted=False, **kw)
+        res_pin[0:1].copy_(o["loss"].view(1), non_blocking=True)
+        res_pin[1:2].copy_(o["token_accuracy"].view(1), non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_step()
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_max = _max_over_ranks(dist, (time.perf_counter() - t0) / args.steps)
+    if rank == 0:
+        peaks = _peaks()
+        nv = float(w.n_rows) * w.vocab
+        # algorithmic bytes: the statistics pass reads the logits once; the
+        # gradient pass reads them again and writes dL/dlogits
+        algo = {"ce_stats": nv * 2, "ce_grad": nv * 4}
+        total_ms = sum(v[1] for v in kernels.values()) or 1.0
+        dom = max(kernels.items(), key=lambda kv: kv[1][1])[0]
+        n_launch, tms = kernels[dom]
+        per_launch = algo.get(dom, 0.0) * args.steps / n_launch
+        achieved = per_launch / (tms / n_launch / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": rows_total / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(_config(w, args.chunk_rows), mode="cross_entropy on materialised bf16 logits [N, V]",
+                           l2="logits larger than L2 (no flush needed)"),
+            "tflops": None,
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "peak_source": f"hbm_gbs ({peaks['source']})",
+                         "traffic": recorded_traffic(w.name + "-ce_logits", dom),
+                         "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": tms / n_launch},
+            "cpu_baseline": None,
+            "e2e": {"value": rows_total / e2e_max, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2 + lab.numel() * 8,
+                    "d2h_bytes_per_step": 8},
+            "gpu_launches": launches, "clocks": clk.summary(),
+            "kernels": {k: {"launches": v[0], "ms": v[1], "share": v[1] / total_ms} for k, v in kernels.items()},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -332,6 +470,11 @@ def main():
     ap.add_argument("--sample-rows", type=int, default=16)
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling captures only)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures only)")
+    ap.add_argument("--low-memory", action="store_true",
+                    help="recompute backward: no stored logits, dlogits per vocab slab")
+    ap.add_argument("--vocab-slab", type=int, default=0)
+    ap.add_argument("--ce-logits", action="store_true",
+                    help="time the cross-entropy on materialised bf16 logits [N, V] instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]

@@ -64,7 +64,7 @@ extern "C" {
 #define FLCE_ERR_ARG 1          /* null pointer, bad size, negative softcap, bad reduction */
 #define FLCE_ERR_ALIGN 2        /* pointer or row stride not 16-byte aligned, H % 8 != 0 */
 #define FLCE_ERR_WORKSPACE 3    /* workspace smaller than flce_workspace_size() */
-#define FLCE_ERR_UNSUPPORTED 4  /* device is not sm_103 / sm_100 family, or size limits */
+#define FLCE_ERR_UNSUPPORTED 4  /* device is not sm_103, or a tensor map cannot be encoded */
 #define FLCE_ERR_CUDA 5         /* a CUDA runtime call or launch failed */
 /* Device-detected bits of the status word (flce_get_status). */
 #define FLCE_ERR_LABEL 16       /* a label is neither ignore_index nor in [0, V) */
@@ -74,14 +74,27 @@ extern "C" {
 #define FLCE_MODE_CE_ONLY 0
 #define FLCE_MODE_FORWARD 1
 #define FLCE_MODE_FORWARD_BACKWARD 2
+#define FLCE_MODE_CROSS_ENTROPY 3   /* flce_cross_entropy on materialised logits */
 
 #define FLCE_REDUCTION_MEAN 0
 #define FLCE_REDUCTION_SUM 1
+#define FLCE_REDUCTION_NONE 2       /* flce_cross_entropy only: per-row losses, per-row upstream grads */
+
+/* Element types of materialised logits (flce_cross_entropy). */
+#define FLCE_DTYPE_BF16 0
+#define FLCE_DTYPE_F32 1
 
 /* Flags (flce_params.flags). */
 #define FLCE_FLAG_SIMT_GEMM 1        /* debug: plain fp32-FMA GEMMs instead of tcgen05 */
 #define FLCE_FLAG_TEST_STALL 2       /* test hook: the forward GEMM's loader issues no copies,
                                         so its bounded waits run out (FLCE_ERR_TIMEOUT) */
+#define FLCE_FLAG_KMAJOR_BWD 4       /* cross-check: feed the backward GEMMs explicit transposes
+                                        (W^T, dz^T, h^T) instead of MN-major tiles */
+#define FLCE_FLAG_RECOMPUTE 8        /* low-memory backward: keep no logits; per vocab slab of
+                                        vocab_slab columns, recompute z = m h W^T on the tensor
+                                        cores and form bf16 dlogits in the GEMM epilogue's
+                                        registers, then run both backward GEMMs on the slab.
+                                        Transient O(C * vocab_slab + C * H); 8NHV flops, not 6NHV */
 
 typedef struct flce_params {
   int64_t n_rows;        /* N >= 0 */
@@ -94,9 +107,11 @@ typedef struct flce_params {
   int64_t ignore_index;  /* rows with this label do not count (default -100) */
   int32_t reduction;     /* FLCE_REDUCTION_MEAN (default) or FLCE_REDUCTION_SUM */
   float grad_scale;      /* g: upstream dL/dloss multiplying every gradient (default 1) */
-  int64_t chunk_rows;    /* rows per chunk C (0 => library default); rounded up to 128 */
+  int64_t chunk_rows;    /* rows per chunk C (0 => 8192); at most 32768; rounded up to 128 */
   int32_t flags;         /* FLCE_FLAG_* */
   int64_t timeout_ns;    /* limit of each bounded device wait (0 => 2 s) */
+  int64_t vocab_slab;    /* FLCE_FLAG_RECOMPUTE: vocab columns per slab (0 => 16384);
+                            rounded up to 256 */
 } flce_params;
 
 /* Fills the defaults: softcap 0, out_mult 1, ignore_index -100, MEAN,
@@ -146,6 +161,23 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W,
                           int64_t* predicted, void* grad_h, float* grad_W,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Cross-entropy on logits that are already materialised, [N, V] with row
+ * stride ld_logits (>= V) in bf16 or fp32 (logits_dtype): the non-fused branch
+ * the Liger-Kernel "Muse Glimmer" page tests next to the fused path (Testing
+ * Done: the non-fused softcap branch; Details / Softcap: T tanh(logits m / T)),
+ * and what DeepSeek-V3's lce_forward does when logits are kept (Summary).
+ * Same per-row definition as the fused path with z = m * logits (p->hidden is
+ * ignored). reduction: MEAN, SUM, or NONE (per-row losses; loss = their sum;
+ * the gradient of sum_i row_scale_i * l_i, row_scale NULL = all ones).
+ * Outputs (all device, nullable except loss): token_accuracy, predicted [N],
+ * row_loss [N] (0 on ignored rows), grad_logits (dL/dlogits, logits' dtype,
+ * [N, ld_logits]; may alias logits to overwrite them in place).
+ * Workspace: flce_workspace_size(p, FLCE_MODE_CROSS_ENTROPY, 0, 0). */
+int flce_cross_entropy(const flce_params* p, const void* logits, int logits_dtype, int64_t ld_logits,
+                       const int64_t* labels, float* loss, float* token_accuracy, int64_t* predicted,
+                       float* row_loss, const float* row_scale, void* grad_logits,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream` and returns (in *status) the device status word of the
  * last call that used this workspace: 0 or FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT.
  * Return value: FLCE_OK or FLCE_ERR_ARG / FLCE_ERR_CUDA. */
@@ -162,7 +194,7 @@ int64_t flce_launch_count(void);
  * flce_profile_begin(0) stops. flce_profile_read synchronises the recorded
  * events and fills, for kernel ids 0..n-1, the launch count and the summed
  * milliseconds; it returns the number of kernel ids (FLCE_NUM_KERNELS). */
-#define FLCE_NUM_KERNELS 10
+#define FLCE_NUM_KERNELS 14
 int flce_profile_begin(int enable);
 int flce_profile_read(int64_t* launches, double* total_ms, int n);
 const char* flce_kernel_name(int id);

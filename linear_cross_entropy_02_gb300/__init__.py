@@ -22,15 +22,15 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,  # noqa: F401
+from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,  # noqa: F401
                    FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
 
 __all__ = [
-    "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward", "flce_workspace_size", "flce_get_status",
+    "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward", "flce_cross_entropy", "flce_workspace_size", "flce_get_status",
     "flce_launch_count", "flce_profile_begin", "flce_profile_read", "FlceError",
 ]
 
-_REDUCTIONS = {"mean": FLCE_REDUCTION_MEAN, "sum": FLCE_REDUCTION_SUM}
+_REDUCTIONS = {"mean": FLCE_REDUCTION_MEAN, "sum": FLCE_REDUCTION_SUM, "none": _lib.FLCE_REDUCTION_NONE}
 _workspaces: dict = {}
 
 
@@ -44,7 +44,7 @@ def _stream_handle(device: torch.device):
 
 def _params(n_rows: int, hidden: int, vocab: int, ld_h: int, ld_w: int, softcap: float, out_mult: float,
             ignore_index: int, reduction: str, grad_scale: float, chunk_rows: int, flags: int,
-            timeout_ns: int) -> FlceParams:
+            timeout_ns: int, vocab_slab: int = 0) -> FlceParams:
     if reduction not in _REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
     p = FlceParams()
@@ -58,6 +58,7 @@ def _params(n_rows: int, hidden: int, vocab: int, ld_h: int, ld_w: int, softcap:
     p.chunk_rows = int(chunk_rows)
     p.flags = int(flags)
     p.timeout_ns = int(timeout_ns)
+    p.vocab_slab = int(vocab_slab)
     return p
 
 
@@ -107,7 +108,7 @@ def flce_workspace_size(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_M
 
 
 def _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags,
-             timeout_ns, mode, need_gh, need_gw):
+             timeout_ns, mode, need_gh, need_gw, vocab_slab=0):
     _check(h, W, labels)
     H = W.shape[1]
     V = W.shape[0]
@@ -116,7 +117,7 @@ def _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scal
         W = W.contiguous()
     lab = labels.reshape(-1).contiguous()
     p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
-                grad_scale, chunk_rows, flags, timeout_ns)
+                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab)
     nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_gh), int(need_gw))
     if nbytes == 0:
         raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
@@ -184,10 +185,15 @@ def flce_forward(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, 
 
 def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None, need_grad_h=True,
                           softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean", grad_scale=1.0,
-                          return_predicted=False, chunk_rows=0, flags=0, timeout_ns=0):
+                          return_predicted=False, chunk_rows=0, flags=0, timeout_ns=0, low_memory=False,
+                          vocab_slab=0):
     """Forward + backward. grad_W: fp32 [V, H] CUDA tensor ACCUMULATED in place
     (grad_W += dL/dW), or None for a frozen W. Returns dict(loss,
-    token_accuracy, predicted, grad_h, grad_W); grad_h (bf16) has h's shape."""
+    token_accuracy, predicted, grad_h, grad_W); grad_h (bf16) has h's shape.
+    low_memory=True selects the recompute backward (FLCE_FLAG_RECOMPUTE): no
+    logits kept, dlogits formed per vocab slab of vocab_slab columns."""
+    if low_memory:
+        flags |= FLCE_FLAG_RECOMPUTE
     if grad_W is not None:
         if grad_W.dtype != torch.float32 or grad_W.shape != W.shape or not grad_W.is_contiguous():
             raise ValueError("grad_W must be a contiguous fp32 tensor shaped like W")
@@ -195,7 +201,7 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
             raise ValueError("grad_W must be on W's device")
     p, h2, W, lab, ws, nbytes = _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale,
                                          chunk_rows, flags, timeout_ns, FLCE_MODE_FORWARD_BACKWARD,
-                                         need_grad_h, grad_W is not None)
+                                         need_grad_h, grad_W is not None, vocab_slab)
     dev = h.device
     loss = torch.empty((), dtype=torch.float32, device=dev)
     acc = torch.empty((), dtype=torch.float32, device=dev)
@@ -209,6 +215,55 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
     return {"loss": loss, "token_accuracy": acc,
             "predicted": None if pred is None else pred.view(lead),
             "grad_h": None if gh is None else gh.view(h.shape), "grad_W": grad_W}
+
+
+def flce_cross_entropy(logits, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                       grad_scale=1.0, row_scale: Optional[torch.Tensor] = None, need_grad=True,
+                       grad_in_place=False, return_predicted=True, chunk_rows=0):
+    """Cross-entropy on materialised logits [..., V] (bf16 or fp32 CUDA tensor).
+    Returns dict(loss, token_accuracy, predicted, row_loss, grad_logits); with
+    reduction="none" the gradient is that of sum_i row_scale_i * row_loss_i.
+    grad_in_place=True writes dL/dlogits over the logits."""
+    if not isinstance(logits, torch.Tensor) or logits.device.type != "cuda":
+        raise ValueError("logits must be a CUDA tensor (the library has no CPU path)")
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("logits must be bfloat16 or float32")
+    if labels.dtype != torch.int64 or labels.shape != logits.shape[:-1] or labels.device != logits.device:
+        raise ValueError("labels must be int64 with logits' leading shape, on its device")
+    V = logits.shape[-1]
+    x = logits.reshape(-1, V)
+    if x.stride(1) != 1:
+        x = x.contiguous()
+    if grad_in_place and x.data_ptr() != logits.data_ptr():
+        raise ValueError("grad_in_place needs logits whose rows can be viewed as [N, V] in place")
+    lab = labels.reshape(-1).contiguous()
+    N = x.shape[0]
+    rs = None
+    if row_scale is not None:
+        rs = row_scale.reshape(-1).to(dtype=torch.float32).contiguous()
+        if rs.numel() != N or rs.device != logits.device:
+            raise ValueError("row_scale must hold one value per row, on the logits' device")
+    p = _params(N, 8, V, 0, 0, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, 0, 0)
+    nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), _lib.FLCE_MODE_CROSS_ENTROPY, 0, 0)
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
+    dev = logits.device
+    ws = _workspace(dev, nbytes)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    pred = torch.empty(N, dtype=torch.int64, device=dev) if return_predicted else None
+    row_loss = torch.empty(N, dtype=torch.float32, device=dev)
+    grad = None
+    if need_grad:
+        grad = x if grad_in_place else torch.empty_like(x)
+    dt = _lib.FLCE_DTYPE_BF16 if x.dtype == torch.bfloat16 else _lib.FLCE_DTYPE_F32
+    rc = _lib.lib().flce_cross_entropy(ctypes.byref(p), _ptr(x), dt, x.stride(0), _ptr(lab), _ptr(loss), _ptr(acc),
+                                       _ptr(pred), _ptr(row_loss), _ptr(rs), _ptr(grad), _ptr(ws), nbytes,
+                                       _stream_handle(dev))
+    _raise(rc, "flce_cross_entropy")
+    lead = logits.shape[:-1]
+    return {"loss": loss, "token_accuracy": acc, "predicted": None if pred is None else pred.view(lead),
+            "row_loss": row_loss.view(lead), "grad_logits": None if grad is None else grad.view(logits.shape)}
 
 
 def flce_get_status(device=None) -> int:

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflce.so")
 
-SOURCES = ["engine.cpp", "gemm_tc.cu", "kernels_aux.cu", "no_alloc.cu"]
+SOURCES = ["engine.cpp", "gemm_tc.cu", "kernels_aux.cu", "kernels_ce.cu", "no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

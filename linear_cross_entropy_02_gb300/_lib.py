@@ -20,18 +20,25 @@ FLCE_ERR_TIMEOUT = 32
 FLCE_MODE_CE_ONLY = 0
 FLCE_MODE_FORWARD = 1
 FLCE_MODE_FORWARD_BACKWARD = 2
+FLCE_MODE_CROSS_ENTROPY = 3
 
 FLCE_REDUCTION_MEAN = 0
 FLCE_REDUCTION_SUM = 1
+FLCE_REDUCTION_NONE = 2
+
+FLCE_DTYPE_BF16 = 0
+FLCE_DTYPE_F32 = 1
 
 FLCE_FLAG_SIMT_GEMM = 1
 FLCE_FLAG_TEST_STALL = 2
+FLCE_FLAG_KMAJOR_BWD = 4
+FLCE_FLAG_RECOMPUTE = 8
 
-FLCE_NUM_KERNELS = 10
+FLCE_NUM_KERNELS = 14
 
 EXPORTED = [
     "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
-    "flce_forward_backward", "flce_get_status", "flce_status_string", "flce_launch_count",
+    "flce_forward_backward", "flce_cross_entropy", "flce_get_status", "flce_status_string", "flce_launch_count",
     "flce_profile_begin", "flce_profile_read", "flce_kernel_name",
 ]
 
@@ -51,6 +58,7 @@ class FlceParams(ctypes.Structure):
         ("chunk_rows", ctypes.c_int64),
         ("flags", ctypes.c_int32),
         ("timeout_ns", ctypes.c_int64),
+        ("vocab_slab", ctypes.c_int64),
     ]
 
 
@@ -94,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.flce_forward.restype = ctypes.c_int
         L.flce_forward_backward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.flce_forward_backward.restype = ctypes.c_int
+        L.flce_cross_entropy.argtypes = [_P, _vp, ctypes.c_int, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _sz, _vp]
+        L.flce_cross_entropy.restype = ctypes.c_int
         L.flce_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
         L.flce_get_status.restype = ctypes.c_int
         L.flce_status_string.argtypes = [ctypes.c_int]

@@ -72,7 +72,8 @@ struct LaunchScope {
 
 const char* const kKernelNames[FLCE_NUM_KERNELS] = {
     "prologue", "fwd_gemm_stats", "merge", "dlogits", "grad_h_gemm",
-    "grad_W_gemm", "transpose_W", "transpose_h", "finish", "simt_stats"};
+    "grad_W_gemm", "transpose_W", "transpose_h", "finish", "simt_stats",
+    "ce_stats", "ce_grad", "recompute_dz_gemm", "convert_grad_h"};
 
 // ------------------------------------------------------------ device info
 int g_sm_count[kMaxDevices] = {0};
@@ -123,6 +124,19 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+// fp32 [outer][inner] with row stride `ld` elements; 32 x 32 boxes (128-byte
+// rows), 128-byte swizzle: the epilogue's bulk store / reduce-add target.
+bool encode_f32_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ layout
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -131,9 +145,10 @@ struct Layout {
   int64_t n_vtiles; // vocab tiles of 256
   int64_t ldp, ldz, ldd, ldt, ldwt, ldht;
   int64_t merge_blocks;
-  bool need_z, need_dz, need_dzt, need_wt, need_ht;
+  int64_t slab;     // recompute mode: vocab columns per slab (0 otherwise)
+  bool need_z, need_dz, need_dzt, need_wt, need_ht, need_gh32;
   size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_dz, off_dzt, off_wt,
-      off_ht, total;
+      off_ht, off_gh32, total;
 };
 
 struct Norm {
@@ -141,17 +156,25 @@ struct Norm {
   int64_t ld_h, ld_w;
 };
 
-int normalise(const flce_params* in, Norm* out) {
+// need_hidden = false for the cross-entropy on materialised logits, which has
+// no hidden dimension (p->hidden, ld_h, ld_w are ignored there).
+int normalise(const flce_params* in, Norm* out, bool need_hidden = true) {
   if (!in) return FLCE_ERR_ARG;
   Norm n;
   n.p = *in;
+  if (!need_hidden) {
+    n.p.hidden = 8;
+    n.p.ld_h = n.p.ld_w = 0;
+  }
   const flce_params& p = n.p;
   if (p.n_rows < 0 || p.hidden <= 0 || p.vocab <= 0 || p.vocab >= (int64_t(1) << 31) - 512) return FLCE_ERR_ARG;
   if (p.n_rows >= (int64_t(1) << 31) - 512 || p.hidden >= (int64_t(1) << 24)) return FLCE_ERR_ARG;
   if (!(p.softcap >= 0.f) || !std::isfinite(p.softcap) || !std::isfinite(p.out_mult) ||
       !std::isfinite(p.grad_scale))
     return FLCE_ERR_ARG;
-  if (p.reduction != FLCE_REDUCTION_MEAN && p.reduction != FLCE_REDUCTION_SUM) return FLCE_ERR_ARG;
+  if (p.reduction != FLCE_REDUCTION_MEAN && p.reduction != FLCE_REDUCTION_SUM &&
+      !(p.reduction == FLCE_REDUCTION_NONE && !need_hidden))
+    return FLCE_ERR_ARG;
   if (p.chunk_rows < 0 || p.timeout_ns < 0) return FLCE_ERR_ARG;
   if (p.hidden % 8 != 0) return FLCE_ERR_ALIGN;
   n.ld_h = p.ld_h == 0 ? p.hidden : p.ld_h;
@@ -164,24 +187,39 @@ int normalise(const flce_params* in, Norm* out) {
 
 void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   const flce_params& p = n.p;
-  const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
+  const bool ce = mode == FLCE_MODE_CROSS_ENTROPY;
+  const bool simt = !ce && (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool bwd = mode == FLCE_MODE_FORWARD_BACKWARD && (gh || gw);
   int64_t c = p.chunk_rows > 0 ? p.chunk_rows : kDefaultChunkRows;
   c = std::min<int64_t>(c, std::max<int64_t>(p.n_rows, 1));
+  c = std::min<int64_t>(c, 32768);  // grid.y of the row-streaming kernels stays below 65536
   L->C = round_up(c, kBM);
-  L->n_vtiles = (p.vocab + kVTile - 1) / kVTile;
+  L->n_vtiles = ce ? (p.vocab + kCeTile - 1) / kCeTile : (p.vocab + kVTile - 1) / kVTile;
   L->ldp = L->C;
   L->ldz = L->n_vtiles * kVTile;
   L->ldd = round_up(p.vocab, 8);
   L->ldt = L->C;
   L->ldwt = round_up(p.vocab, 8);
   L->ldht = L->C;
-  L->merge_blocks = (L->C + 127) / 128;
-  L->need_z = bwd || simt;
-  L->need_dz = bwd && gh;
-  L->need_dzt = bwd && gw;
-  L->need_wt = bwd && gh;
-  L->need_ht = bwd && gw;
+  L->merge_blocks = (L->C + kMergeRows - 1) / kMergeRows;
+  // The backward GEMMs read W, dz and h_c in place as MN-major tiles; the
+  // transposed copies exist only on the debug paths (SIMT GEMMs, or the
+  // K-major cross-check flag).
+  // The recompute mode keeps no logits: a [C][slab] bf16 dlogits slab and an
+  // fp32 [C][H] grad_h accumulator instead.
+  const bool recompute = bwd && !simt && (p.flags & FLCE_FLAG_RECOMPUTE) != 0;
+  const bool kmajor = !recompute && (simt || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
+  L->slab = 0;
+  if (recompute) {
+    const int64_t want = p.vocab_slab > 0 ? p.vocab_slab : 16384;
+    L->slab = round_up(std::min<int64_t>(want, round_up(p.vocab, kVTile)), kVTile);
+  }
+  L->need_z = (bwd && !recompute) || simt;
+  L->need_dz = bwd && (gh || (gw && !kmajor));
+  L->need_dzt = bwd && gw && kmajor;
+  L->need_wt = bwd && gh && kmajor;
+  L->need_ht = bwd && gw && kmajor;
+  L->need_gh32 = recompute && gh;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -197,10 +235,11 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_tgt = take(sizeof(float) * L->C);
   L->off_lse = take(sizeof(float) * L->C);
   L->off_z = L->need_z ? take(sizeof(float) * L->C * L->ldz) : 0;
-  L->off_dz = L->need_dz ? take(sizeof(uint16_t) * L->C * L->ldd) : 0;
+  L->off_dz = L->need_dz ? take(sizeof(uint16_t) * L->C * (recompute ? L->slab : L->ldd)) : 0;
   L->off_dzt = L->need_dzt ? take(sizeof(uint16_t) * round_up(p.vocab, kBM) * L->ldt) : 0;
   L->off_wt = L->need_wt ? take(sizeof(uint16_t) * p.hidden * L->ldwt) : 0;
   L->off_ht = L->need_ht ? take(sizeof(uint16_t) * p.hidden * L->ldht) : 0;
+  L->off_gh32 = L->need_gh32 ? take(sizeof(float) * L->C * p.hidden) : 0;
   L->total = off;
 }
 
@@ -247,6 +286,8 @@ int run(const flce_params* params, const Call& c) {
   rc = device_info(&sms, &cc);
   if (rc != FLCE_OK) return rc;
   const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
+  const bool recompute = L.slab > 0;
+  const bool kmajor = !recompute && (simt || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
   if (cc != 103) return FLCE_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
   if (!simt && !load_encoder()) return FLCE_ERR_UNSUPPORTED;
 
@@ -274,7 +315,7 @@ int run(const flce_params* params, const Call& c) {
     if (!encode_bf16(&map_h, c.h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
     if (!encode_bf16(&map_w, c.W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
   }
-  if (L.need_wt && N > 0) {
+  if (L.need_wt && N > 0) {  // debug paths only
     FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_bf16(static_cast<const uint16_t*>(c.W), n.ld_w, V, H, wt, L.ldwt,
                                                      stream));
     if (!simt && !encode_bf16(&map_wt, wt, V, H, L.ldwt, kBN)) return FLCE_ERR_UNSUPPORTED;
@@ -319,12 +360,14 @@ int run(const flce_params* params, const Call& c) {
       FLCE_LAUNCH(K_SIMT_STATS, launch_stats_from_z(g, rows, store, stream));
     } else {
       const int tiles = g.m_tiles * g.n_tiles;
-      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, &map_h, &map_w, g,
-                                             std::min(tiles, sms), stream));
+      CUtensorMap map_z;
+      if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, &map_h, &map_w,
+                                             store ? &map_z : nullptr, g, std::min(tiles, sms), stream));
     }
 
     // ---- merge of the vocab-tile statistics
-    MergeParams mp;
+    MergeParams mp{};
     mp.rows = rows;
     mp.n_vtiles = static_cast<int>(L.n_vtiles);
     mp.ldp = static_cast<int>(L.ldp);
@@ -343,6 +386,106 @@ int run(const flce_params* params, const Call& c) {
     FLCE_LAUNCH(K_MERGE, launch_merge(mp, stream));
 
     if (!gh && !gw) continue;
+
+    if (recompute) {
+      // ---- low-memory backward: per vocab slab, recompute z on the tensor
+      // cores with dlogits formed in the epilogue, then both backward GEMMs.
+      float* gh32 = L.need_gh32 ? reinterpret_cast<float*>(ws + L.off_gh32) : nullptr;
+      if (gh32 && cudaMemsetAsync(gh32, 0, sizeof(float) * rows * H, stream) != cudaSuccess) return FLCE_ERR_CUDA;
+      const int slab = static_cast<int>(L.slab);
+      for (int v0 = 0; v0 < V; v0 += slab) {
+        const int vs = std::min(slab, V - v0);
+        GemmParams r;
+        std::memset(&r, 0, sizeof(r));
+        r.M = rows;
+        r.N = vs;
+        r.K = H;
+        r.m_tiles = (rows + kBM - 1) / kBM;
+        r.n_tiles = (vs + kBN - 1) / kBN;
+        r.k_iters = (H + kBK - 1) / kBK;
+        r.group_m = std::min(r.m_tiles, 16);
+        r.a_row0 = static_cast<int>(r0);
+        r.b_row0 = v0;
+        r.alpha = p.out_mult;
+        r.M_valid = rows;
+        r.N_valid = vs;
+        r.softcap = p.softcap;
+        r.inv_softcap = inv_cap;
+        r.labels = lab_c;
+        r.ignore_index = p.ignore_index;
+        r.out = dz;
+        r.ldo = slab;
+        r.lse = lse;
+        r.hdr = hdr;
+        r.grad_scale = p.grad_scale;
+        r.reduction = p.reduction;
+        r.col0 = v0;
+        r.status = &hdr->status;
+        r.timeout_ns = timeout;
+        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, &map_h, &map_w, nullptr, r,
+                                                     std::min(r.m_tiles * r.n_tiles, sms), stream));
+        if (gh) {
+          // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
+          CUtensorMap map_a, map_b;
+          if (!encode_bf16(&map_a, dz, vs, rows, slab, kBM)) return FLCE_ERR_UNSUPPORTED;
+          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.W) + static_cast<int64_t>(v0) * n.ld_w, H, vs,
+                           n.ld_w, 64))
+            return FLCE_ERR_UNSUPPORTED;
+          GemmParams b;
+          std::memset(&b, 0, sizeof(b));
+          b.M = rows;
+          b.N = H;
+          b.K = vs;
+          b.m_tiles = (rows + kBM - 1) / kBM;
+          b.n_tiles = (H + kBN - 1) / kBN;
+          b.k_iters = (vs + kBK - 1) / kBK;
+          b.group_m = std::min(b.m_tiles, 8);
+          b.alpha = p.out_mult;
+          b.M_valid = rows;
+          b.N_valid = H;
+          b.out = gh32;
+          b.ldo = H;
+          b.status = &hdr->status;
+          b.timeout_ns = timeout;
+          CUtensorMap map_o;
+          if (!encode_f32_out(&map_o, gh32, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
+          FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, &map_a, &map_b, &map_o, b,
+                                                   std::min(b.m_tiles * b.n_tiles, sms), stream));
+        }
+        if (gw) {
+          // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
+          CUtensorMap map_a, map_b;
+          if (!encode_bf16(&map_a, dz, vs, rows, slab, 64)) return FLCE_ERR_UNSUPPORTED;
+          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
+            return FLCE_ERR_UNSUPPORTED;
+          GemmParams b;
+          std::memset(&b, 0, sizeof(b));
+          b.M = vs;
+          b.N = H;
+          b.K = rows;
+          b.m_tiles = (vs + kBM - 1) / kBM;
+          b.n_tiles = (H + kBN - 1) / kBN;
+          b.k_iters = (rows + kBK - 1) / kBK;
+          b.group_m = std::min(b.m_tiles, 16);
+          b.alpha = p.out_mult;
+          b.M_valid = vs;
+          b.N_valid = H;
+          b.out = c.grad_W + static_cast<int64_t>(v0) * H;
+          b.ldo = H;
+          b.status = &hdr->status;
+          b.timeout_ns = timeout;
+          CUtensorMap map_o;
+          if (!encode_f32_out(&map_o, c.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
+          FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, &map_a, &map_b, &map_o, b,
+                                                   std::min(b.m_tiles * b.n_tiles, sms), stream));
+        }
+      }
+      if (gh) {
+        FLCE_LAUNCH(K_CONVERT, launch_f32_to_bf16(gh32, static_cast<uint16_t*>(c.grad_h) + r0 * H,
+                                                  static_cast<int64_t>(rows) * H, stream));
+      }
+      continue;
+    }
 
     // ---- dlogits
     DlogitParams dp;
@@ -374,7 +517,7 @@ int run(const flce_params* params, const Call& c) {
       b.m_tiles = (rows + kBM - 1) / kBM;
       b.n_tiles = (H + kBN - 1) / kBN;
       b.k_iters = (V + kBK - 1) / kBK;
-      b.group_m = std::min(b.m_tiles, 8);
+      b.group_m = std::min(b.m_tiles, 16);
       b.alpha = p.out_mult;
       b.M_valid = rows;
       b.N_valid = H;
@@ -385,17 +528,24 @@ int run(const flce_params* params, const Call& c) {
       if (simt) {
         FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_simt(EPI_BF16, dz, L.ldd, wt, L.ldwt, b, stream));
       } else {
-        CUtensorMap map_dz;
+        CUtensorMap map_dz, map_wb;
         if (!encode_bf16(&map_dz, dz, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
-        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, &map_dz, &map_wt, b,
+        if (kmajor) {
+          map_wb = map_wt;  // W^T [H][V]: K-major B
+        } else if (!encode_bf16(&map_wb, c.W, H, V, n.ld_w, 64)) {  // W [V][H]: MN-major B
+          return FLCE_ERR_UNSUPPORTED;
+        }
+        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, false, !kmajor, &map_dz, &map_wb, nullptr, b,
                                                  std::min(b.m_tiles * b.n_tiles, sms), stream));
       }
     }
 
     // ---- grad_W += m dz^T h_c
     if (gw) {
-      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_bf16(static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, n.ld_h,
-                                                       rows, H, ht, L.ldht, stream));
+      if (kmajor) {
+        FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_bf16(static_cast<const uint16_t*>(c.h) + r0 * n.ld_h,
+                                                         n.ld_h, rows, H, ht, L.ldht, stream));
+      }
       GemmParams b;
       std::memset(&b, 0, sizeof(b));
       b.M = V;
@@ -415,16 +565,108 @@ int run(const flce_params* params, const Call& c) {
       if (simt) {
         FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_simt(EPI_ACC_F32, dzt, L.ldt, ht, L.ldht, b, stream));
       } else {
-        CUtensorMap map_dzt, map_ht;
-        if (!encode_bf16(&map_dzt, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
-        if (!encode_bf16(&map_ht, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
-        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, &map_dzt, &map_ht, b,
+        CUtensorMap map_a, map_b;
+        if (kmajor) {
+          // dz^T [V][C] and h_c^T [H][C]: K-major A and B
+          if (!encode_bf16(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
+          if (!encode_bf16(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
+        } else {
+          // dz [C][V] and h_c [C][H] read in place: MN-major A and B (K = chunk rows)
+          if (!encode_bf16(&map_a, dz, V, rows, L.ldd, 64)) return FLCE_ERR_UNSUPPORTED;
+          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
+            return FLCE_ERR_UNSUPPORTED;
+        }
+        CUtensorMap map_o;
+        if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, !kmajor, !kmajor, &map_a, &map_b, &map_o, b,
                                                  std::min(b.m_tiles * b.n_tiles, sms), stream));
       }
     }
   }
 
   FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
+  return FLCE_OK;
+}
+
+// Cross-entropy on materialised logits: prologue, then per chunk the tile
+// statistics, the merge and (when asked) the gradient, then the scalars.
+int run_ce(const flce_params* params, const void* logits, int dtype, int64_t ldx, const int64_t* labels,
+           float* loss, float* acc, int64_t* predicted, float* row_loss, const float* row_scale, void* grad,
+           void* wsv, size_t ws_bytes, cudaStream_t stream) {
+  Norm n;
+  int rc = normalise(params, &n, false);
+  if (rc != FLCE_OK) return rc;
+  const flce_params& p = n.p;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_F32) return FLCE_ERR_ARG;
+  if (!loss || !wsv) return FLCE_ERR_ARG;
+  if (p.n_rows > 0 && (!logits || !labels)) return FLCE_ERR_ARG;
+  if (ldx < p.vocab) return FLCE_ERR_ARG;
+  if (!aligned16(wsv)) return FLCE_ERR_ALIGN;
+  Layout L;
+  make_layout(n, FLCE_MODE_CROSS_ENTROPY, false, false, &L);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  int sms = 0, cc = 0;
+  rc = device_info(&sms, &cc);
+  if (rc != FLCE_OK) return rc;
+  if (cc != 103) return FLCE_ERR_UNSUPPORTED;
+
+  uint8_t* ws = static_cast<uint8_t*>(wsv);
+  Header* hdr = reinterpret_cast<Header*>(ws + L.off_hdr);
+  const size_t esz = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  const bool vec_ok = aligned16(logits) && (grad == nullptr || aligned16(grad)) && (ldx * esz) % 16 == 0;
+
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+  for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
+    const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
+    CeParams cp{};
+    cp.rows = rows;
+    cp.vocab = static_cast<int>(p.vocab);
+    cp.n_vtiles = static_cast<int>(L.n_vtiles);
+    cp.ldp = static_cast<int>(L.ldp);
+    cp.dtype = dtype;
+    cp.vec_ok = vec_ok ? 1 : 0;
+    cp.logits = static_cast<const uint8_t*>(logits) + r0 * ldx * esz;
+    cp.ldx = ldx;
+    cp.grad = grad ? static_cast<uint8_t*>(grad) + r0 * ldx * esz : nullptr;
+    cp.ldg = ldx;
+    cp.labels = labels + r0;
+    cp.ignore_index = p.ignore_index;
+    cp.out_mult = p.out_mult;
+    cp.softcap = p.softcap;
+    cp.inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    cp.grad_scale = p.grad_scale;
+    cp.reduction = p.reduction;
+    cp.row_scale = row_scale ? row_scale + r0 : nullptr;
+    cp.part_max = reinterpret_cast<float*>(ws + L.off_pmax);
+    cp.part_sum = reinterpret_cast<float*>(ws + L.off_psum);
+    cp.part_idx = reinterpret_cast<int32_t*>(ws + L.off_pidx);
+    cp.tgt = reinterpret_cast<float*>(ws + L.off_tgt);
+    cp.lse = reinterpret_cast<float*>(ws + L.off_lse);
+    cp.hdr = hdr;
+    FLCE_LAUNCH(K_CE_STATS, launch_ce_stats(cp, stream));
+
+    MergeParams mp{};
+    mp.rows = rows;
+    mp.n_vtiles = static_cast<int>(L.n_vtiles);
+    mp.ldp = static_cast<int>(L.ldp);
+    mp.part_max = cp.part_max;
+    mp.part_sum = cp.part_sum;
+    mp.part_idx = cp.part_idx;
+    mp.tgt = cp.tgt;
+    mp.labels = labels + r0;
+    mp.ignore_index = p.ignore_index;
+    mp.lse = reinterpret_cast<float*>(ws + L.off_lse);
+    mp.predicted = predicted ? predicted + r0 : nullptr;
+    mp.row_lse = nullptr;
+    mp.row_loss = row_loss ? row_loss + r0 : nullptr;
+    mp.block_loss = reinterpret_cast<double*>(ws + L.off_bl);
+    mp.block_correct = reinterpret_cast<int64_t*>(ws + L.off_bc);
+    mp.hdr = hdr;
+    FLCE_LAUNCH(K_MERGE, launch_merge(mp, stream));
+
+    if (grad) FLCE_LAUNCH(K_CE_GRAD, launch_ce_grad(cp, stream));
+  }
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, loss, acc, stream));
   return FLCE_OK;
 }
 
@@ -444,8 +686,8 @@ void flce_default_params(flce_params* p) {
 
 size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W) {
   Norm n;
-  if (normalise(p, &n) != FLCE_OK) return 0;
-  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_FORWARD_BACKWARD) return 0;
+  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_CROSS_ENTROPY) return 0;
+  if (normalise(p, &n, mode != FLCE_MODE_CROSS_ENTROPY) != FLCE_OK) return 0;
   Layout L;
   make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
   return L.total;
@@ -472,6 +714,14 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W, co
   Call c{FLCE_MODE_FORWARD_BACKWARD, h, W, labels, loss, token_accuracy, predicted, nullptr, grad_h, grad_W,
          workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   return run(p, c);
+}
+
+int flce_cross_entropy(const flce_params* p, const void* logits, int logits_dtype, int64_t ld_logits,
+                       const int64_t* labels, float* loss, float* token_accuracy, int64_t* predicted,
+                       float* row_loss, const float* row_scale, void* grad_logits, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return run_ce(p, logits, logits_dtype, ld_logits, labels, loss, token_accuracy, predicted, row_loss, row_scale,
+                grad_logits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int flce_get_status(const void* workspace, void* stream, int32_t* status) {

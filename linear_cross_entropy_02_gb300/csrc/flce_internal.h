@@ -19,10 +19,17 @@ constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: epilogue
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kBN * kBK * 2;
-constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
+// Per epilogue warp: two 4 KB staging buffers for a 32 x 32 fp32 sub-tile that a
+// TMA bulk store (stored logits) or bulk reduce-add (fp32 gradients) sends out.
+constexpr int kStageBufBytes = 32 * 32 * 4;
+constexpr int kEpiStagingBytes = 4 * 2 * kStageBufBytes;
+constexpr int kGemmSmemBytes =
+    kStages * (kAStageBytes + kBStageBytes) + kEpiStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 // Vocab columns per forward statistics partial (= the GEMM's N tile).
 constexpr int kVTile = kBN;
+// Rows per block of the merge kernel (one merge block partial per 32 rows).
+constexpr int kMergeRows = 32;
 
 // Workspace header (offset 0 of every workspace).
 struct Header {
@@ -44,6 +51,10 @@ enum KernelId {
   K_TRANSPOSE_H = 7,
   K_FINISH = 8,
   K_SIMT_STATS = 9,
+  K_CE_STATS = 10,
+  K_CE_GRAD = 11,
+  K_RECOMPUTE_GEMM = 12,
+  K_CONVERT = 13,
 };
 
 enum EpiMode {
@@ -51,6 +62,7 @@ enum EpiMode {
   EPI_STATS_STORE = 1,  // statistics partials + capped logits s stored (fp32)
   EPI_BF16 = 2,         // out = bf16(alpha * acc)
   EPI_ACC_F32 = 3,      // out += alpha * acc (fp32)
+  EPI_DZ = 4,           // out = bf16 dlogits formed from z = alpha * acc, lse and labels
 };
 
 struct GemmParams {
@@ -75,6 +87,12 @@ struct GemmParams {
   // plain epilogues
   void* out;
   int64_t ldo;
+  // dlogits epilogue (EPI_DZ): column j of D is vocab index col0 + j
+  const float* lse;  // [rows of D]
+  const struct Header* hdr;
+  float grad_scale;
+  int reduction;
+  int col0;
   // control
   int32_t* status;
   uint64_t timeout_ns;
@@ -82,8 +100,13 @@ struct GemmParams {
 };
 
 // Tensor-core GEMM (tcgen05 + TMA + TMEM), persistent over `grid` CTAs.
-cudaError_t launch_gemm_tc(int mode, const CUtensorMap* a, const CUtensorMap* b, const GemmParams& p,
-                           int grid, cudaStream_t s);
+// a_mn / b_mn: the operand is MN-major in global memory ([K rows][MN cols]),
+// loaded as 64x64 boxes; otherwise K-major ([MN rows][K cols]).
+// c: fp32 output tensor map with 32 x 32 boxes and 128-byte swizzle, used by
+// EPI_STATS_STORE (the stored logits, bulk store) and EPI_ACC_F32 (bulk
+// reduce-add into the fp32 accumulator); ignored by the other modes.
+cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
+                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
 // Debug GEMM on the fp32 FMA pipes; writes alpha*acc to zbuf for the statistics
 // modes (then run launch_stats_from_z) and behaves like the tensor-core GEMM
 // for the plain modes.
@@ -106,6 +129,7 @@ struct MergeParams {
   float* lse;             // [rows] chunk workspace
   int64_t* predicted;     // global output offset to the chunk, or null
   float* row_lse;         // global output offset to the chunk, or null
+  float* row_loss;        // global output offset to the chunk, or null (0 on ignored rows)
   double* block_loss;     // [blocks]
   int64_t* block_correct; // [blocks]
   Header* hdr;
@@ -133,6 +157,35 @@ cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s);
 // out [cols][ldo] = in [rows][ldi]^T, bf16.
 cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int cols, uint16_t* out,
                                   int64_t ldo, cudaStream_t s);
+
+// Columns per warp task of the cross-entropy-on-logits statistics.
+constexpr int kCeTile = 2048;
+
+struct CeParams {
+  int rows, vocab, n_vtiles, ldp;
+  int dtype;          // FLCE_DTYPE_*
+  int vec_ok;         // rows are 16-byte aligned: vector loads / stores
+  const void* logits;
+  int64_t ldx;
+  void* grad;
+  int64_t ldg;
+  const int64_t* labels;
+  int64_t ignore_index;
+  float out_mult, softcap, inv_softcap, grad_scale;
+  int reduction;
+  const float* row_scale;
+  float* part_max;
+  float* part_sum;
+  int32_t* part_idx;
+  float* tgt;
+  const float* lse;
+  const Header* hdr;
+};
+cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s);
+cudaError_t launch_ce_grad(const CeParams& p, cudaStream_t s);
+
+// out [n] (bf16) = in [n] (fp32), round to nearest even.
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 
 cudaError_t launch_finish(const Header* hdr, int reduction, float* loss, float* token_accuracy,
                           cudaStream_t s);

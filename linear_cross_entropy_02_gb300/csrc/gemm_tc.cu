@@ -37,17 +37,49 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
   nb = local / gsize;
 }
 
+// Staging of one epilogue warp's 32 x 32 fp32 sub-tile for a TMA bulk store or
+// reduce-add: lane r writes its row as eight 16-byte chunks, chunk q at slot
+// q ^ (r & 7) (the 128-byte swizzle the tensor map expects; also spreads the
+// writes of a warp over all banks). Two buffers alternate; lane 0 issues the
+// bulk copy and keeps at most one older copy reading shared memory.
+struct EpiStage {
+  uint8_t* base;  // this warp's two buffers
+  int next;       // buffer to fill next
+};
+
+template <bool REDUCE>
+__device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* map, int lane, const float (&v)[32],
+                                               int32_t x, int32_t y) {
+  uint8_t* buf = es.base + es.next * kStageBufBytes;
+  if (lane == 0) bulk_wait_group_read<1>();  // the copy that used `buf` two sends ago has read it
+  __syncwarp();
+  float4* row = reinterpret_cast<float4*>(buf + lane * 128);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) row[q ^ (lane & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (REDUCE)
+      tma_reduce_add_2d(map, buf, x, y);
+    else
+      tma_store_2d(map, buf, x, y);
+    bulk_commit_group();
+  }
+  es.next ^= 1;
+}
+
 template <bool STORE>
-__device__ __forceinline__ void epilogue_stats(const GemmParams& p, uint32_t tcol, int mb, int nb,
-                                               int row) {
+__device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtensorMap* zmap, EpiStage& es,
+                                               uint32_t tcol, int mb, int nb, int quarter, int lane) {
+  const int row = quarter * 32 + lane;
   const int grow = mb * kBM + row;
   const bool row_ok = grow < p.M_valid;
   const int64_t label = row_ok ? __ldg(p.labels + grow) : p.ignore_index;
   const int n0 = nb * kBN;
   const bool has_label = label != p.ignore_index && label >= n0 && label < n0 + kBN;
+  const bool full_tile = n0 + kBN <= p.N_valid;  // no column past V: skip the mask
   RowStats st;
   row_stats_init(st, n0);
-  float* zrow = STORE ? p.zbuf + static_cast<int64_t>(grow) * p.ldz + n0 : nullptr;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
@@ -55,14 +87,19 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, uint32_t tco
     tmem_load_wait();
     float s[32];
     const int col0 = n0 + c * 32;
+    if (p.softcap > 0.f) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      s[j] = cap_logit(__uint_as_float(r[j]) * p.alpha, p.softcap, p.inv_softcap, col0 + j < p.N_valid);
-    if (STORE && row_ok) {
-      float4* dst = reinterpret_cast<float4*>(zrow + c * 32);
+      for (int j = 0; j < 32; ++j) s[j] = p.softcap * tanhf(__uint_as_float(r[j]) * p.alpha * p.inv_softcap);
+    } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+      for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]) * p.alpha;
     }
+    if (!full_tile) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j >= p.N_valid) s[j] = -INFINITY;
+    }
+    if (STORE) stage_and_send<false>(es, zmap, lane, s, col0, mb * kBM + quarter * 32);
     row_stats_update32(st, s, col0, has_label ? label : -1);
   }
   if (row_ok) {
@@ -104,43 +141,80 @@ __device__ __forceinline__ void epilogue_bf16(const GemmParams& p, uint32_t tcol
   }
 }
 
-__device__ __forceinline__ void epilogue_acc_f32(const GemmParams& p, uint32_t tcol, int mb, int nb,
-                                                 int row) {
-  const int grow = mb * kBM + row;
-  const bool row_ok = grow < p.M_valid;
+// grad_W (or the recompute path's fp32 grad_h) += alpha * acc: the sub-tile is
+// staged in shared memory and added in L2 by a TMA bulk reduce-add; rows and
+// columns outside the tensor map are clipped by the copy engine.
+__device__ __forceinline__ void epilogue_acc_f32(const GemmParams& p, const CUtensorMap* omap, EpiStage& es,
+                                                 uint32_t tcol, int mb, int nb, int quarter, int lane) {
   const int n0 = nb * kBN;
-  float* orow = static_cast<float*>(p.out) + static_cast<int64_t>(grow) * p.ldo + n0;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
     tmem_load_32cols(tcol + c * 32, r);
     tmem_load_wait();
+    float v[32];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int col = n0 + c * 32 + g * 4;
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.alpha;
+    if (n0 + c * 32 < p.N_valid) stage_and_send<true>(es, omap, lane, v, n0 + c * 32, mb * kBM + quarter * 32);
+  }
+}
+
+// Recompute pass of the low-memory backward: z = alpha * acc is capped, turned
+// into dlogits with the row's lse and label, rounded to bf16 and stored.
+__device__ __forceinline__ void epilogue_dz(const GemmParams& p, uint32_t tcol, int mb, int nb, int row,
+                                            float coef) {
+  const int grow = mb * kBM + row;
+  const bool row_ok = grow < p.M_valid;
+  const int64_t label = row_ok ? __ldg(p.labels + grow) : p.ignore_index;
+  const bool valid = row_ok && label != p.ignore_index;
+  const float ci = valid ? coef : 0.f;
+  const float lse = row_ok ? __ldg(p.lse + grow) : 0.f;
+  const int n0 = nb * kBN;
+  const int64_t ylocal = valid ? label - p.col0 : -1;
+  uint16_t* orow = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(grow) * p.ldo + n0;
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_load_32cols(tcol + c * 32, r);
+    tmem_load_wait();
+    float d[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float z = __uint_as_float(r[j]) * p.alpha;
+      const float sv = p.softcap > 0.f ? p.softcap * tanhf(z * p.inv_softcap) : z;
+      float q = __expf(sv - lse) - (static_cast<int64_t>(n0 + c * 32 + j) == ylocal ? 1.f : 0.f);
+      if (p.softcap > 0.f) {
+        const float u = sv * p.inv_softcap;
+        q *= (1.f - u * u);
+      }
+      d[j] = ci * q;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int col = n0 + c * 32 + g * 8;
       if (row_ok && col < p.N_valid) {
-        float4* dst = reinterpret_cast<float4*>(orow + c * 32 + g * 4);
-        float4 o = *dst;
-        o.x += __uint_as_float(r[g * 4 + 0]) * p.alpha;
-        o.y += __uint_as_float(r[g * 4 + 1]) * p.alpha;
-        o.z += __uint_as_float(r[g * 4 + 2]) * p.alpha;
-        o.w += __uint_as_float(r[g * 4 + 3]) * p.alpha;
-        *dst = o;
+        uint4 v;
+        v.x = pack_bf16x2(d[g * 8 + 0], d[g * 8 + 1]);
+        v.y = pack_bf16x2(d[g * 8 + 2], d[g * 8 + 3]);
+        v.z = pack_bf16x2(d[g * 8 + 4], d[g * 8 + 5]);
+        v.w = pack_bf16x2(d[g * 8 + 6], d[g * 8 + 7]);
+        *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = v;
       }
     }
   }
 }
 
-template <int MODE>
+template <int MODE, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kAStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBStageBytes);
+  uint8_t* sStage = sB + kStages * kBStageBytes;  // epilogue staging, 4 warps x 2 buffers
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kEpiStagingBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -167,6 +241,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
+    if (MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32) tma_prefetch_desc(&tma_c);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -197,8 +272,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&full[stage], kAStageBytes + kBStageBytes);
-            tma_load_2d(sA + stage * kAStageBytes, &tma_a, &full[stage], k * kBK, p.a_row0 + mb * kBM);
-            tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kBK, p.b_row0 + nb * kBN);
+            // K-major operand: one box of 64 K x rows. MN-major operand: boxes of
+            // 64 MN x 64 K, one per 64 rows of the tile, 8 KB apart.
+            if (A_MN) {
+#pragma unroll
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d(sA + stage * kAStageBytes + j * 8192, &tma_a, &full[stage], p.a_row0 + mb * kBM + j * 64,
+                            k * kBK);
+            } else {
+              tma_load_2d(sA + stage * kAStageBytes, &tma_a, &full[stage], k * kBK, p.a_row0 + mb * kBM);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < kBN / 64; ++j)
+                tma_load_2d(sB + stage * kBStageBytes + j * 8192, &tma_b, &full[stage], p.b_row0 + nb * kBN + j * 64,
+                            k * kBK);
+            } else {
+              tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kBK, p.b_row0 + nb * kBN);
+            }
             ++issued;
             if (++stage == kStages) {
               stage = 0;
@@ -232,7 +323,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool aborted = false;
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
       const uint32_t a_base = smem_u32(sA);
       const uint32_t b_base = smem_u32(sB);
       for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
@@ -249,8 +340,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t b0 = b_base + stage * kBStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32), sdesc_kmajor_sw128(b0 + kk * 32), idesc,
-                        (k | kk) != 0 ? 1u : 0u);
+            // 16 K-elements per MMA: 32 B along a K-major row, or two 8-row
+            // K groups (2048 B) of an MN-major tile.
+            const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(a0 + kk * 2048) : sdesc_kmajor_sw128(a0 + kk * 32);
+            const uint64_t bd = B_MN ? sdesc_mnmajor_sw128(b0 + kk * 2048) : sdesc_kmajor_sw128(b0 + kk * 32);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -269,9 +363,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    float coef = 0.f;  // dlogits scale c of the EPI_DZ epilogue
+    if (MODE == EPI_DZ) {
+      const int64_t nv = p.hdr->n_valid;
+      if (nv > 0) coef = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(nv) : p.grad_scale;
+    }
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    EpiStage es{sStage + (warp - 2) * 2 * kStageBufBytes, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -283,19 +383,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after_sync();
       const uint32_t tcol = t_lane + static_cast<uint32_t>(acc * kBN);
       if (MODE == EPI_STATS) {
-        epilogue_stats<false>(p, tcol, mb, nb, row);
+        epilogue_stats<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
       } else if (MODE == EPI_STATS_STORE) {
-        epilogue_stats<true>(p, tcol, mb, nb, row);
+        epilogue_stats<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
       } else if (MODE == EPI_BF16) {
         epilogue_bf16(p, tcol, mb, nb, row);
+      } else if (MODE == EPI_ACC_F32) {
+        epilogue_acc_f32(p, &tma_c, es, tcol, mb, nb, quarter, lane);
       } else {
-        epilogue_acc_f32(p, tcol, mb, nb, row);
+        epilogue_dz(p, tcol, mb, nb, row, coef);
       }
       tc_fence_before_sync();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // Outstanding bulk stores / reduce-adds must finish before the CTA exits.
+    if ((MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32) && lane == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before_sync();
@@ -306,26 +410,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const GemmParams& p, int grid,
-                               cudaStream_t s) {
+template <int MODE, bool A_MN, bool B_MN>
+static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
+                               const GemmParams& p, int grid, cudaStream_t s) {
   // Per device and cheap: set on every launch rather than caching per process.
-  cudaError_t e =
-      cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, p);
+  gemm_tc_kernel<MODE, A_MN, B_MN><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(int mode, const CUtensorMap* a, const CUtensorMap* b, const GemmParams& p, int grid,
-                           cudaStream_t s) {
-  switch (mode) {
-    case EPI_STATS: return launch_mode<EPI_STATS>(a, b, p, grid, s);
-    case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE>(a, b, p, grid, s);
-    case EPI_BF16: return launch_mode<EPI_BF16>(a, b, p, grid, s);
-    case EPI_ACC_F32: return launch_mode<EPI_ACC_F32>(a, b, p, grid, s);
-    default: return cudaErrorInvalidValue;
+cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
+                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
+  if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32) && c == nullptr) return cudaErrorInvalidValue;
+  // The combinations the engine uses: the forward GEMM (both K-major), grad_h
+  // (dz K-major, W MN-major or its transpose K-major), grad_W (dz and h_c
+  // MN-major, or their transposes K-major).
+  if (!a_mn && !b_mn) {
+    switch (mode) {
+      case EPI_STATS: return launch_mode<EPI_STATS, false, false>(a, b, c, p, grid, s);
+      case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false>(a, b, c, p, grid, s);
+      case EPI_BF16: return launch_mode<EPI_BF16, false, false>(a, b, c, p, grid, s);
+      case EPI_ACC_F32: return launch_mode<EPI_ACC_F32, false, false>(a, b, c, p, grid, s);
+      case EPI_DZ: return launch_mode<EPI_DZ, false, false>(a, b, c, p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (!a_mn && b_mn && mode == EPI_BF16) return launch_mode<EPI_BF16, false, true>(a, b, c, p, grid, s);
+  if (!a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode<EPI_ACC_F32, false, true>(a, b, c, p, grid, s);
+  if (a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode<EPI_ACC_F32, true, true>(a, b, c, p, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace flce

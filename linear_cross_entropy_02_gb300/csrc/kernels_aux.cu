@@ -74,19 +74,23 @@ cudaError_t launch_prologue(const int64_t* labels, int64_t n, int64_t vocab, int
 }
 
 // ------------------------------------------------------------------ merge
-constexpr int kMergeThreads = 128;
+// 32 rows per block (one per lane) x 8 warps: warp w folds vocab tiles w, w+8,
+// w+16, ... of its lane's row (reads of one tile are 32 consecutive rows), the
+// eight partial results are merged in warp order through shared memory, and
+// warp 0 finishes the rows. Ties keep the lowest vocab index throughout.
+constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-  __shared__ double s_loss[kMergeThreads / 32];
-  __shared__ long long s_corr[kMergeThreads / 32];
+__global__ void __launch_bounds__(kMergeRows * kMergeWarps) merge_kernel(const MergeParams p) {
+  __shared__ float s_m[kMergeWarps][kMergeRows];
+  __shared__ float s_s[kMergeWarps][kMergeRows];
+  __shared__ int s_a[kMergeWarps][kMergeRows];
   __shared__ bool s_last;
-  const int row = blockIdx.x * kMergeThreads + threadIdx.x;
-  double loss_i = 0.0;
-  long long corr_i = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = blockIdx.x * kMergeRows + lane;
+  float mx = -INFINITY, sum = 0.f;
+  int arg = 0x7fffffff;
   if (row < p.rows) {
-    float mx = -INFINITY, sum = 0.f;
-    int arg = 0;
-    for (int t = 0; t < p.n_vtiles; ++t) {
+    for (int t = warp; t < p.n_vtiles; t += kMergeWarps) {
       const int64_t o = static_cast<int64_t>(t) * p.ldp + row;
       const float pm = p.part_max[o];
       const float ps = p.part_sum[o];
@@ -98,38 +102,53 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         sum += ps * expf(pm - mx);
       }
     }
-    const float lse = mx + logf(sum);
-    p.lse[row] = lse;
-    const int64_t y = p.labels[row];
-    if (y != p.ignore_index) {
-      loss_i = static_cast<double>(lse) - static_cast<double>(p.tgt[row]);
-      corr_i = (static_cast<int64_t>(arg) == y) ? 1 : 0;
-    }
-    if (p.predicted) p.predicted[row] = arg;
-    if (p.row_lse) p.row_lse[row] = lse;
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    loss_i += __shfl_xor_sync(0xffffffffu, loss_i, o);
-    corr_i += __shfl_xor_sync(0xffffffffu, corr_i, o);
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) {
-    s_loss[w] = loss_i;
-    s_corr[w] = corr_i;
-  }
+  s_m[warp][lane] = mx;
+  s_s[warp][lane] = sum;
+  s_a[warp][lane] = arg;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double bl = 0.0;
-    long long bc = 0;
-    for (int i = 0; i < kMergeThreads / 32; ++i) {
-      bl += s_loss[i];
-      bc += s_corr[i];
+  if (warp == 0) {
+    double loss_i = 0.0;
+    long long corr_i = 0;
+    if (row < p.rows) {
+      float M = -INFINITY, S = 0.f;
+      int A = 0x7fffffff;
+      for (int w = 0; w < kMergeWarps; ++w) {
+        const float m2 = s_m[w][lane];
+        const float s2 = s_s[w][lane];
+        const int a2 = s_a[w][lane];
+        if (m2 == -INFINITY) continue;
+        if (m2 > M) {
+          S = S * expf(M - m2) + s2;
+          M = m2;
+          A = a2;
+        } else {
+          S += s2 * expf(m2 - M);
+          if (m2 == M && a2 < A) A = a2;
+        }
+      }
+      const float lse = M + logf(S);
+      p.lse[row] = lse;
+      const int64_t y = p.labels[row];
+      if (y != p.ignore_index) {
+        loss_i = static_cast<double>(lse) - static_cast<double>(p.tgt[row]);
+        corr_i = (static_cast<int64_t>(A) == y) ? 1 : 0;
+      }
+      if (p.predicted) p.predicted[row] = A;
+      if (p.row_lse) p.row_lse[row] = lse;
+      if (p.row_loss) p.row_loss[row] = static_cast<float>(loss_i);
     }
-    p.block_loss[blockIdx.x] = bl;
-    p.block_correct[blockIdx.x] = bc;
-    __threadfence();
-    const unsigned int ticket = atomicAdd(&p.hdr->ticket, 1u);
-    s_last = (ticket == gridDim.x - 1);
+    for (int o = 16; o > 0; o >>= 1) {
+      loss_i += __shfl_xor_sync(0xffffffffu, loss_i, o);
+      corr_i += __shfl_xor_sync(0xffffffffu, corr_i, o);
+    }
+    if (lane == 0) {
+      p.block_loss[blockIdx.x] = loss_i;
+      p.block_correct[blockIdx.x] = corr_i;
+      __threadfence();
+      const unsigned int ticket = atomicAdd(&p.hdr->ticket, 1u);
+      s_last = (ticket == gridDim.x - 1);
+    }
   }
   __syncthreads();
   // The last block to finish adds the block sums in block order, so the result
@@ -149,9 +168,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  const int blocks = (p.rows + kMergeThreads - 1) / kMergeThreads;
+  const int blocks = (p.rows + kMergeRows - 1) / kMergeRows;
   if (blocks == 0) return cudaSuccess;
-  merge_kernel<<<blocks, kMergeThreads, 0, s>>>(p);
+  merge_kernel<<<blocks, kMergeRows * kMergeWarps, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -253,8 +272,61 @@ __global__ void __launch_bounds__(256) dlogits_kernel(const DlogitParams p) {
   }
 }
 
+// Product path (no transposed copy): plain streaming over the rows, one
+// thread per 8 consecutive columns: 32 B of s read, 16 B of dz written.
+__global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p) {
+  const int r = blockIdx.y;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c >= p.vocab) return;
+  const int64_t n_valid = p.hdr->n_valid;
+  const int64_t y = p.labels[r];
+  float ci = 0.f;
+  if (y != p.ignore_index && n_valid > 0)
+    ci = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
+  const float lse = p.lse[r];
+  const float* srow = p.s + static_cast<int64_t>(r) * p.lds;
+  float sv[8];
+  const bool full = c + 8 <= p.vocab;
+  if (full) {
+    const float4 a = *reinterpret_cast<const float4*>(srow + c);
+    const float4 b = *reinterpret_cast<const float4*>(srow + c + 4);
+    sv[0] = a.x; sv[1] = a.y; sv[2] = a.z; sv[3] = a.w;
+    sv[4] = b.x; sv[5] = b.y; sv[6] = b.z; sv[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sv[j] = (c + j < p.vocab) ? srow[c + j] : 0.f;
+  }
+  uint16_t b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float q = ci * (__expf(sv[j] - lse) - (static_cast<int64_t>(c + j) == y ? 1.f : 0.f));
+    if (p.softcap > 0.f) {
+      const float u = sv[j] * p.inv_softcap;
+      q *= (1.f - u * u);
+    }
+    b[j] = float_to_bf16_bits(q);
+  }
+  uint16_t* drow = p.dz + static_cast<int64_t>(r) * p.ldd;
+  if (full) {
+    uint4 pk;
+    pk.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
+    pk.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
+    pk.z = static_cast<uint32_t>(b[4]) | (static_cast<uint32_t>(b[5]) << 16);
+    pk.w = static_cast<uint32_t>(b[6]) | (static_cast<uint32_t>(b[7]) << 16);
+    *reinterpret_cast<uint4*>(drow + c) = pk;
+  } else {
+    for (int j = 0; j < 8; ++j)
+      if (c + j < p.vocab) drow[c + j] = b[j];
+  }
+}
+
 cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s) {
   if (p.rows <= 0 || p.vocab <= 0) return cudaSuccess;
+  if (p.dzt == nullptr && p.dz != nullptr) {
+    dim3 grid((p.vocab + 2047) / 2048, p.rows);
+    dlogits_rows_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   dim3 grid((p.vocab + kDzTile - 1) / kDzTile, (p.rows + kDzTile - 1) / kDzTile);
   dlogits_kernel<<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
@@ -296,6 +368,28 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   dim3 grid((cols + 63) / 64, (rows + 63) / 64);
   transpose_bf16_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ convert
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ out,
+                                                          int64_t n) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i + 4 <= n) {
+    const float4 v = *reinterpret_cast<const float4*>(in + i);
+    uint2 pk;
+    pk.x = static_cast<uint32_t>(float_to_bf16_bits(v.x)) | (static_cast<uint32_t>(float_to_bf16_bits(v.y)) << 16);
+    pk.y = static_cast<uint32_t>(float_to_bf16_bits(v.z)) | (static_cast<uint32_t>(float_to_bf16_bits(v.w)) << 16);
+    *reinterpret_cast<uint2*>(out + i) = pk;
+  } else {
+    for (int64_t j = i; j < n; ++j) out[j] = float_to_bf16_bits(in[j]);
+  }
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t threads = (n + 3) / 4;
+  f32_to_bf16_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(in, out, n);
   return cudaGetLastError();
 }
 

@@ -1,2 +1,3 @@
 """CPU fp64 oracle (test infrastructure only; see flce_oracle)."""
-from .flce_oracle import capped_logits, flce_oracle, oracle_grad_W_rows, oracle_rows  # noqa: F401
+from .flce_oracle import (capped_logits, flce_oracle, oracle_ce_logits, oracle_grad_W_rows,  # noqa: F401
+                          oracle_rows)

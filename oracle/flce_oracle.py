@@ -50,6 +50,7 @@ __all__ = [
     "flce_oracle",
     "oracle_rows",
     "oracle_grad_W_rows",
+    "oracle_ce_logits",
 ]
 
 
@@ -249,3 +250,55 @@ def oracle_grad_W_rows(h, W, labels, vocab_ids, lse, n_valid: int, *, softcap: f
             q = q * (1.0 - (s / softcap) ** 2)
         out += q.T @ hm
     return out
+
+
+def oracle_ce_logits(logits, labels, *, softcap: float = 0.0, out_mult: float = 1.0,
+                     ignore_index: int = -100, reduction: str = "mean", grad_scale: float = 1.0,
+                     row_scale=None, need_grad: bool = True, block_rows: int = 256) -> dict:
+    """Cross-entropy on logits that are already materialised: the non-fused
+    branch the Muse Glimmer page tests next to the fused path (Testing Done:
+    "the non-fused softcap branch"; Details: HF caps T tanh(logits m / T)), and
+    the path DeepSeek-V3's lce_forward takes when logits are kept (Summary).
+
+    Same row definition as flce_oracle with z = m * logits:
+        s = T tanh(z / T) (T > 0) or z;  l_i = lse_i - s_{i, y_i}
+    reduction "mean" / "sum" as there; "none" returns the row losses only
+    (loss = their sum) and takes its upstream gradient per row from row_scale
+    (default all ones): q_ij = row_scale_i (softmax - onehot) on valid rows.
+    grad_logits = dL/dlogits = m * dz, dz as in flce_oracle.
+    """
+    x = _f64(logits)
+    lab = _i64(labels)
+    N, V = x.shape
+    valid = lab != ignore_index
+    if np.any((lab[valid] < 0) | (lab[valid] >= V)):
+        raise ValueError("label outside [0, V) that is not ignore_index")
+    n_valid = int(valid.sum())
+    rs = np.ones(N) if row_scale is None else _f64(row_scale)
+    lse = np.zeros(N)
+    pred = np.zeros(N, dtype=np.int64)
+    gap = np.zeros(N)
+    row_loss = np.zeros(N)
+    grad = np.zeros((N, V)) if need_grad else None
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        z = out_mult * x[r0:r1]
+        s = softcap * np.tanh(z / softcap) if softcap > 0.0 else z
+        lb = np.where(valid[r0:r1], lab[r0:r1], 0)
+        vb = valid[r0:r1]
+        lse[r0:r1], pred[r0:r1], gap[r0:r1], row_loss[r0:r1] = _row_stats(s, lb, vb)
+        if need_grad:
+            if reduction == "none":
+                dz = _dz(s, lse[r0:r1], lb, vb, 1.0, softcap) * rs[r0:r1, None]
+            else:
+                dz = _dz(s, lse[r0:r1], lb, vb, _coef(n_valid, reduction, grad_scale), softcap)
+            grad[r0:r1] = out_mult * dz
+    total = float(row_loss[valid].sum())
+    correct = int(np.sum(valid & (pred == lab)))
+    if n_valid == 0:
+        loss, acc = 0.0, 0.0
+    else:
+        loss = total / n_valid if reduction == "mean" else total
+        acc = correct / n_valid
+    return {"loss": loss, "token_accuracy": acc, "n_valid": n_valid, "correct": correct,
+            "predicted": pred, "lse": lse, "row_loss": row_loss, "top2_gap": gap, "grad_logits": grad}

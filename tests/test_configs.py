@@ -93,10 +93,17 @@ def test_full_size_sampled_rows(flce, name):
         scale = np.abs(ref["grad_h"]).max()
         assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * scale
 
-    # property: without softcap the columns of dL/dW sum to zero over the vocabulary
+    # property: without softcap the columns of dL/dW sum to zero over the vocabulary,
+    # up to the bf16 rounding of dz (at most 2^-9 of each term; the label term
+    # -1/n_valid rounds the same way on every row, so the error does not average
+    # out): |sum_j gW_jk| <= 2^-8 |m| / n_valid * sum_{valid i} |h_ik|
     if gW is not None and w.softcap == 0.0:
-        col = gW.double().sum(dim=0).abs().max().item()
-        assert col <= 1e-2 * gW.abs().max().item(), col
+        col = gW.double().sum(dim=0).abs()
+        habs = hd.reshape(-1, w.hidden)[valid].double().abs().sum(0)
+        bound = 2.0 ** -8 * abs(w.out_mult) / n_valid * habs
+        assert torch.all(col <= bound), (col.max().item(), bound.min().item())
+        # a lost or doubled chunk would leave sums of the order of sum_i h_ik / n_valid
+        print(f"{name}: max column sum {col.max().item():.3e}, bound {bound.min().item():.3e}")
 
 
 @pytest.mark.parametrize("name", ["llama", "muse", "dsv3"])

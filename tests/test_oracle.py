@@ -353,3 +353,44 @@ def test_workload_recipe_is_deterministic_and_shaped():
     # Zipf(1.1): id 0 is the most frequent, about 1/H_{1000,1.1} of the draws
     hz = sum((k + 1) ** -1.1 for k in range(1000))
     assert abs(float((zv == 0).float().mean()) - 1 / hz) < 0.02
+
+
+# --- cross-entropy on materialised logits -------------------------------------------
+def test_ce_logits_matches_torch_and_autograd():
+    from oracle import oracle_ce_logits
+    rng = np.random.default_rng(20)
+    N, V = 37, 53
+    x = rng.standard_normal((N, V)) * 3
+    lab = rng.integers(0, V, N)
+    lab[[2, 9]] = -100
+    for T, m in [(0.0, 1.0), (2.5, 0.5)]:
+        xt = torch.tensor(x, requires_grad=True)
+        s = T * torch.tanh(xt * m / T) if T > 0 else xt * m
+        loss = torch.nn.functional.cross_entropy(s, torch.tensor(lab), ignore_index=-100)
+        loss.backward()
+        out = oracle_ce_logits(x, lab, softcap=T, out_mult=m)
+        assert out["loss"] == pytest.approx(loss.item(), rel=1e-13)
+        np.testing.assert_allclose(out["grad_logits"], xt.grad.numpy(), rtol=1e-12, atol=1e-15)
+        # reduction none: per-row losses of torch, and the gradient of sum_i r_i l_i
+        xt2 = torch.tensor(x, requires_grad=True)
+        s2 = T * torch.tanh(xt2 * m / T) if T > 0 else xt2 * m
+        rl = torch.nn.functional.cross_entropy(s2, torch.tensor(lab), ignore_index=-100, reduction="none")
+        r = torch.tensor(rng.standard_normal(N))
+        (rl * r).sum().backward()
+        o2 = oracle_ce_logits(x, lab, softcap=T, out_mult=m, reduction="none", row_scale=r.numpy())
+        np.testing.assert_allclose(o2["row_loss"], rl.detach().numpy(), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(o2["grad_logits"], xt2.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_ce_logits_equals_fused_with_identity_weight():
+    from oracle import oracle_ce_logits
+    rng = np.random.default_rng(21)
+    N, V = 24, 31
+    x = rng.standard_normal((N, V))
+    lab = rng.integers(0, V, N)
+    lab[0] = -100
+    a = oracle_ce_logits(x, lab, softcap=4.0, out_mult=0.5)
+    b = flce_oracle(x, np.eye(V), lab, softcap=4.0, out_mult=0.5)   # h = logits, W = I
+    assert a["loss"] == pytest.approx(b["loss"], rel=1e-14)
+    np.testing.assert_allclose(a["grad_logits"], b["grad_h"], atol=1e-16)
+    np.testing.assert_array_equal(a["predicted"], b["predicted"])
