@@ -112,6 +112,9 @@ typedef struct flce_params {
   int64_t timeout_ns;    /* limit of each bounded device wait (0 => 2 s) */
   int64_t vocab_slab;    /* FLCE_FLAG_RECOMPUTE: vocab columns per slab (0 => 16384);
                             rounded up to 256 */
+  int32_t dtype;         /* element type of h, W and grad_h: FLCE_DTYPE_BF16 (default) or
+                            FLCE_DTYPE_F32 (fp32 operands on the tf32 tensor cores; fp32
+                            grad_h; not with FLCE_FLAG_RECOMPUTE or FLCE_FLAG_SIMT_GEMM) */
 } flce_params;
 
 /* Fills the defaults: softcap 0, out_mult 1, ignore_index -100, MEAN,

@@ -44,7 +44,7 @@ def _stream_handle(device: torch.device):
 
 def _params(n_rows: int, hidden: int, vocab: int, ld_h: int, ld_w: int, softcap: float, out_mult: float,
             ignore_index: int, reduction: str, grad_scale: float, chunk_rows: int, flags: int,
-            timeout_ns: int, vocab_slab: int = 0) -> FlceParams:
+            timeout_ns: int, vocab_slab: int = 0, dtype: int = 0) -> FlceParams:
     if reduction not in _REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
     p = FlceParams()
@@ -59,6 +59,7 @@ def _params(n_rows: int, hidden: int, vocab: int, ld_h: int, ld_w: int, softcap:
     p.flags = int(flags)
     p.timeout_ns = int(timeout_ns)
     p.vocab_slab = int(vocab_slab)
+    p.dtype = int(dtype)
     return p
 
 
@@ -69,12 +70,16 @@ def _rows2d(h: torch.Tensor, H: int) -> torch.Tensor:
     return h2
 
 
+def _dtype_code(t: torch.Tensor) -> int:
+    return _lib.FLCE_DTYPE_F32 if t.dtype == torch.float32 else _lib.FLCE_DTYPE_BF16
+
+
 def _check(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor):
     for name, t in (("h", h), ("W", W), ("labels", labels)):
         if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
             raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
-    if h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
-        raise ValueError("h and W must be bfloat16")
+    if h.dtype not in (torch.bfloat16, torch.float32) or W.dtype != h.dtype:
+        raise ValueError("h and W must both be bfloat16, or both float32 (tf32 tensor-core path)")
     if labels.dtype != torch.int64:
         raise ValueError("labels must be int64")
     if W.dim() != 2 or h.shape[-1] != W.shape[1]:
@@ -117,7 +122,7 @@ def _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scal
         W = W.contiguous()
     lab = labels.reshape(-1).contiguous()
     p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
-                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab)
+                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _dtype_code(h2))
     nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_gh), int(need_gw))
     if nbytes == 0:
         raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
@@ -152,7 +157,7 @@ def flce_ce_only_noalloc(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_inde
         W = W.contiguous()
     lab = labels.reshape(-1).contiguous()
     p = _params(h2.shape[0], H, W.shape[0], h2.stride(0), W.stride(0), softcap, out_mult, ignore_index,
-                reduction, 1.0, chunk_rows, flags, timeout_ns)
+                reduction, 1.0, chunk_rows, flags, timeout_ns, 0, _dtype_code(h2))
     dev = h.device
     loss = torch.empty((), dtype=torch.float32, device=dev)
     acc = torch.empty((), dtype=torch.float32, device=dev)
@@ -206,7 +211,7 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
     loss = torch.empty((), dtype=torch.float32, device=dev)
     acc = torch.empty((), dtype=torch.float32, device=dev)
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
-    gh = torch.empty((h2.shape[0], W.shape[1]), dtype=torch.bfloat16, device=dev) if need_grad_h else None
+    gh = torch.empty((h2.shape[0], W.shape[1]), dtype=h2.dtype, device=dev) if need_grad_h else None
     rc = _lib.lib().flce_forward_backward(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                           _ptr(pred), _ptr(gh), _ptr(grad_W), _ptr(ws), nbytes,
                                           _stream_handle(dev))

@@ -59,6 +59,7 @@ class FlceParams(ctypes.Structure):
         ("flags", ctypes.c_int32),
         ("timeout_ns", ctypes.c_int64),
         ("vocab_slab", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
     ]
 
 

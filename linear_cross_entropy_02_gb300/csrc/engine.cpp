@@ -124,6 +124,20 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+// fp32 operand [outer][inner] with row stride `ld` elements, read as tf32:
+// box = 32 x box_rows (one 128-byte swizzle row per operand row).
+bool encode_f32_in(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                   uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // fp32 [outer][inner] with row stride `ld` elements; 32 x 32 boxes (128-byte
 // rows), 128-byte swizzle: the epilogue's bulk store / reduce-add target.
 bool encode_f32_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld) {
@@ -176,6 +190,7 @@ int normalise(const flce_params* in, Norm* out, bool need_hidden = true) {
       !(p.reduction == FLCE_REDUCTION_NONE && !need_hidden))
     return FLCE_ERR_ARG;
   if (p.chunk_rows < 0 || p.timeout_ns < 0) return FLCE_ERR_ARG;
+  if (p.dtype != FLCE_DTYPE_BF16 && p.dtype != FLCE_DTYPE_F32) return FLCE_ERR_ARG;
   if (p.hidden % 8 != 0) return FLCE_ERR_ALIGN;
   n.ld_h = p.ld_h == 0 ? p.hidden : p.ld_h;
   n.ld_w = p.ld_w == 0 ? p.hidden : p.ld_w;
@@ -207,8 +222,12 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   // K-major cross-check flag).
   // The recompute mode keeps no logits: a [C][slab] bf16 dlogits slab and an
   // fp32 [C][H] grad_h accumulator instead.
-  const bool recompute = bwd && !simt && (p.flags & FLCE_FLAG_RECOMPUTE) != 0;
-  const bool kmajor = !recompute && (simt || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
+  // fp32 operands (tf32 GEMMs) take the all-K-major backward with fp32 dz and
+  // fp32 transposed copies; the recompute mode is bf16 only.
+  const bool f32 = p.dtype == FLCE_DTYPE_F32;
+  const bool recompute = bwd && !simt && !f32 && (p.flags & FLCE_FLAG_RECOMPUTE) != 0;
+  const bool kmajor = !recompute && (simt || f32 || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
+  const size_t es = f32 ? 4 : 2;  // element size of dz, dz^T, W^T, h_c^T
   L->slab = 0;
   if (recompute) {
     const int64_t want = p.vocab_slab > 0 ? p.vocab_slab : 16384;
@@ -235,10 +254,10 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_tgt = take(sizeof(float) * L->C);
   L->off_lse = take(sizeof(float) * L->C);
   L->off_z = L->need_z ? take(sizeof(float) * L->C * L->ldz) : 0;
-  L->off_dz = L->need_dz ? take(sizeof(uint16_t) * L->C * (recompute ? L->slab : L->ldd)) : 0;
-  L->off_dzt = L->need_dzt ? take(sizeof(uint16_t) * round_up(p.vocab, kBM) * L->ldt) : 0;
-  L->off_wt = L->need_wt ? take(sizeof(uint16_t) * p.hidden * L->ldwt) : 0;
-  L->off_ht = L->need_ht ? take(sizeof(uint16_t) * p.hidden * L->ldht) : 0;
+  L->off_dz = L->need_dz ? take(es * L->C * (recompute ? L->slab : L->ldd)) : 0;
+  L->off_dzt = L->need_dzt ? take(es * round_up(p.vocab, kBM) * L->ldt) : 0;
+  L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
+  L->off_ht = L->need_ht ? take(es * p.hidden * L->ldht) : 0;
   L->off_gh32 = L->need_gh32 ? take(sizeof(float) * L->C * p.hidden) : 0;
   L->total = off;
 }
@@ -267,10 +286,13 @@ struct Call {
   cudaStream_t stream;
 };
 
+int run_f32(const Norm& n, const Call& c);
+
 int run(const flce_params* params, const Call& c) {
   Norm n;
   int rc = normalise(params, &n);
   if (rc != FLCE_OK) return rc;
+  if (n.p.dtype == FLCE_DTYPE_F32) return run_f32(n, c);
   const flce_params& p = n.p;
   const bool gh = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_h != nullptr;
   const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
@@ -488,7 +510,7 @@ int run(const flce_params* params, const Call& c) {
     }
 
     // ---- dlogits
-    DlogitParams dp;
+    DlogitParams dp{};
     dp.rows = rows;
     dp.vocab = V;
     dp.s = zbuf;
@@ -584,6 +606,180 @@ int run(const flce_params* params, const Call& c) {
     }
   }
 
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
+  return FLCE_OK;
+}
+
+// fp32 operands (the pages' fp32 parity and convergence runs): tcgen05
+// kind::tf32 GEMMs on K-major operands, fp32 dlogits with an fp32 transposed
+// copy, fp32 transposes of W and h_c, grad_h written in fp32 by bulk stores.
+int run_f32(const Norm& n, const Call& c) {
+  const flce_params& p = n.p;
+  const bool gh = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_h != nullptr;
+  const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
+  if (!c.loss || !c.ws || !c.W) return FLCE_ERR_ARG;
+  if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
+  if (!aligned16(c.ws) || (c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
+  if ((gh && !aligned16(c.grad_h)) || (gw && !aligned16(c.grad_W))) return FLCE_ERR_ALIGN;
+  if (p.flags & (FLCE_FLAG_SIMT_GEMM | FLCE_FLAG_RECOMPUTE)) return FLCE_ERR_UNSUPPORTED;
+  Layout L;
+  make_layout(n, c.mode, gh, gw, &L);
+  if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  int sms = 0, cc = 0;
+  int rc = device_info(&sms, &cc);
+  if (rc != FLCE_OK) return rc;
+  if (cc != 103) return FLCE_ERR_UNSUPPORTED;
+  if (!load_encoder()) return FLCE_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = c.stream;
+  uint8_t* ws = static_cast<uint8_t*>(c.ws);
+  Header* hdr = reinterpret_cast<Header*>(ws + L.off_hdr);
+  float* pmax = reinterpret_cast<float*>(ws + L.off_pmax);
+  float* psum = reinterpret_cast<float*>(ws + L.off_psum);
+  int32_t* pidx = reinterpret_cast<int32_t*>(ws + L.off_pidx);
+  float* tgt = reinterpret_cast<float*>(ws + L.off_tgt);
+  float* lse = reinterpret_cast<float*>(ws + L.off_lse);
+  float* zbuf = L.need_z ? reinterpret_cast<float*>(ws + L.off_z) : nullptr;
+  float* dz = L.need_dz ? reinterpret_cast<float*>(ws + L.off_dz) : nullptr;
+  float* dzt = L.need_dzt ? reinterpret_cast<float*>(ws + L.off_dzt) : nullptr;
+  float* wt = L.need_wt ? reinterpret_cast<float*>(ws + L.off_wt) : nullptr;
+  float* ht = L.need_ht ? reinterpret_cast<float*>(ws + L.off_ht) : nullptr;
+  const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
+  const int N = static_cast<int>(p.n_rows), H = static_cast<int>(p.hidden), V = static_cast<int>(p.vocab);
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+  const float* h = static_cast<const float*>(c.h);
+  const float* W = static_cast<const float*>(c.W);
+  constexpr int kSlice = kBK / 2;  // fp32 elements per 128-byte K slice
+
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(c.labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+  CUtensorMap map_h, map_w, map_wt;
+  if (N > 0) {
+    if (!encode_f32_in(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+    if (!encode_f32_in(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+  }
+  if (L.need_wt && N > 0) {
+    FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_f32(W, n.ld_w, V, H, wt, L.ldwt, stream));
+    if (!encode_f32_in(&map_wt, wt, V, H, L.ldwt, kBN)) return FLCE_ERR_UNSUPPORTED;
+  }
+  for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
+    const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
+    const int64_t* lab_c = c.labels + r0;
+    GemmParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.M = rows;
+    g.N = V;
+    g.K = H;
+    g.m_tiles = (rows + kBM - 1) / kBM;
+    g.n_tiles = static_cast<int>(L.n_vtiles);
+    g.k_iters = (H + kSlice - 1) / kSlice;
+    g.group_m = std::min(g.m_tiles, 16);
+    g.a_row0 = static_cast<int>(r0);
+    g.alpha = p.out_mult;
+    g.M_valid = rows;
+    g.N_valid = V;
+    g.softcap = p.softcap;
+    g.inv_softcap = inv_cap;
+    g.labels = lab_c;
+    g.ignore_index = p.ignore_index;
+    g.part_max = pmax;
+    g.part_sum = psum;
+    g.part_idx = pidx;
+    g.tgt = tgt;
+    g.ldp = static_cast<int>(L.ldp);
+    g.zbuf = zbuf;
+    g.ldz = L.ldz;
+    g.status = &hdr->status;
+    g.timeout_ns = timeout;
+    g.debug_flags = p.flags;
+    const bool store = L.need_z;
+    CUtensorMap map_z;
+    if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
+    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, &map_h, &map_w,
+                                                store ? &map_z : nullptr, g,
+                                                std::min(g.m_tiles * g.n_tiles, sms), stream));
+    MergeParams mp{};
+    mp.rows = rows;
+    mp.n_vtiles = static_cast<int>(L.n_vtiles);
+    mp.ldp = static_cast<int>(L.ldp);
+    mp.part_max = pmax;
+    mp.part_sum = psum;
+    mp.part_idx = pidx;
+    mp.tgt = tgt;
+    mp.labels = lab_c;
+    mp.ignore_index = p.ignore_index;
+    mp.lse = lse;
+    mp.predicted = c.predicted ? c.predicted + r0 : nullptr;
+    mp.row_lse = c.row_lse ? c.row_lse + r0 : nullptr;
+    mp.block_loss = reinterpret_cast<double*>(ws + L.off_bl);
+    mp.block_correct = reinterpret_cast<int64_t*>(ws + L.off_bc);
+    mp.hdr = hdr;
+    FLCE_LAUNCH(K_MERGE, launch_merge(mp, stream));
+    if (!gh && !gw) continue;
+
+    DlogitParams dp{};
+    dp.rows = rows;
+    dp.vocab = V;
+    dp.s = zbuf;
+    dp.lds = L.ldz;
+    dp.lse = lse;
+    dp.labels = lab_c;
+    dp.ignore_index = p.ignore_index;
+    dp.softcap = p.softcap;
+    dp.inv_softcap = inv_cap;
+    dp.grad_scale = p.grad_scale;
+    dp.reduction = p.reduction;
+    dp.hdr = hdr;
+    dp.dz32 = gh ? dz : nullptr;
+    dp.ldd = L.ldd;
+    dp.dzt32 = gw ? dzt : nullptr;
+    dp.ldt = L.ldt;
+    FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
+
+    if (gh) {  // grad_h_c = m dz W: A = dz [C][V], B = W^T [H][V], fp32 output
+      GemmParams b;
+      std::memset(&b, 0, sizeof(b));
+      b.M = rows;
+      b.N = H;
+      b.K = V;
+      b.m_tiles = (rows + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (V + kSlice - 1) / kSlice;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = rows;
+      b.N_valid = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      CUtensorMap map_a, map_o;
+      if (!encode_f32_in(&map_a, dz, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_f32_out(&map_o, static_cast<float*>(c.grad_h) + r0 * H, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
+      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc_tf32(EPI_F32, &map_a, &map_wt, &map_o, b,
+                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
+    }
+    if (gw) {  // grad_W += m dz^T h_c: A = dz^T [V][C], B = h_c^T [H][C]
+      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_f32(h + r0 * n.ld_h, n.ld_h, rows, H, ht, L.ldht, stream));
+      GemmParams b;
+      std::memset(&b, 0, sizeof(b));
+      b.M = V;
+      b.N = H;
+      b.K = rows;
+      b.m_tiles = (V + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (rows + kSlice - 1) / kSlice;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = V;
+      b.N_valid = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      CUtensorMap map_a, map_b, map_o;
+      if (!encode_f32_in(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_f32_in(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
+      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc_tf32(EPI_ACC_F32, &map_a, &map_b, &map_o, b,
+                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
+    }
+  }
   FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
   return FLCE_OK;
 }

@@ -63,6 +63,7 @@ enum EpiMode {
   EPI_BF16 = 2,         // out = bf16(alpha * acc)
   EPI_ACC_F32 = 3,      // out += alpha * acc (fp32)
   EPI_DZ = 4,           // out = bf16 dlogits formed from z = alpha * acc, lse and labels
+  EPI_F32 = 5,          // out = alpha * acc (fp32, bulk store)
 };
 
 struct GemmParams {
@@ -107,6 +108,10 @@ struct GemmParams {
 // reduce-add into the fp32 accumulator); ignored by the other modes.
 cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
+// The same GEMM on fp32 operands (tcgen05 kind::tf32), both K-major; modes
+// EPI_STATS, EPI_STATS_STORE, EPI_F32, EPI_ACC_F32.
+cudaError_t launch_gemm_tc_tf32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
+                                const GemmParams& p, int grid, cudaStream_t s);
 // Debug GEMM on the fp32 FMA pipes; writes alpha*acc to zbuf for the statistics
 // modes (then run launch_stats_from_z) and behaves like the tensor-core GEMM
 // for the plain modes.
@@ -151,12 +156,16 @@ struct DlogitParams {
   int64_t ldd;
   uint16_t* dzt;    // bf16 [vocab][ldt] or null
   int64_t ldt;
+  float* dz32;      // fp32-operand path: dz [rows][ldd] and dz^T [vocab][ldt] in fp32
+  float* dzt32;
 };
 cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s);
 
-// out [cols][ldo] = in [rows][ldi]^T, bf16.
+// out [cols][ldo] = in [rows][ldi]^T, bf16 / fp32.
 cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int cols, uint16_t* out,
                                   int64_t ldo, cudaStream_t s);
+cudaError_t launch_transpose_f32(const float* in, int64_t ldi, int rows, int cols, float* out, int64_t ldo,
+                                 cudaStream_t s);
 
 // Columns per warp task of the cross-entropy-on-logits statistics.
 constexpr int kCeTile = 2048;

@@ -144,7 +144,8 @@ __device__ __forceinline__ void epilogue_bf16(const GemmParams& p, uint32_t tcol
 // grad_W (or the recompute path's fp32 grad_h) += alpha * acc: the sub-tile is
 // staged in shared memory and added in L2 by a TMA bulk reduce-add; rows and
 // columns outside the tensor map are clipped by the copy engine.
-__device__ __forceinline__ void epilogue_acc_f32(const GemmParams& p, const CUtensorMap* omap, EpiStage& es,
+template <bool REDUCE>
+__device__ __forceinline__ void epilogue_out_f32(const GemmParams& p, const CUtensorMap* omap, EpiStage& es,
                                                  uint32_t tcol, int mb, int nb, int quarter, int lane) {
   const int n0 = nb * kBN;
 #pragma unroll 1
@@ -155,7 +156,7 @@ __device__ __forceinline__ void epilogue_acc_f32(const GemmParams& p, const CUte
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.alpha;
-    if (n0 + c * 32 < p.N_valid) stage_and_send<true>(es, omap, lane, v, n0 + c * 32, mb * kBM + quarter * 32);
+    if (n0 + c * 32 < p.N_valid) stage_and_send<REDUCE>(es, omap, lane, v, n0 + c * 32, mb * kBM + quarter * 32);
   }
 }
 
@@ -204,7 +205,9 @@ __device__ __forceinline__ void epilogue_dz(const GemmParams& p, uint32_t tcol, 
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN>
+// TF32: operands are fp32 (read by the tensor cores as tf32); a K slice is then
+// 32 elements, still one 128-byte swizzle row, and one MMA covers K = 8.
+template <int MODE, bool A_MN, bool B_MN, bool TF32>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                    const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
@@ -222,6 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
+  static_assert(!(TF32 && (A_MN || B_MN)), "tf32 operands are K-major only");
+  constexpr int kSliceK = TF32 ? kBK / 2 : kBK;  // elements per 128-byte K slice
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
-    if (MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32) tma_prefetch_desc(&tma_c);
+    if (MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32 || MODE == EPI_F32) tma_prefetch_desc(&tma_c);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -278,17 +283,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_2d(sA + stage * kAStageBytes + j * 8192, &tma_a, &full[stage], p.a_row0 + mb * kBM + j * 64,
-                            k * kBK);
+                            k * kSliceK);
             } else {
-              tma_load_2d(sA + stage * kAStageBytes, &tma_a, &full[stage], k * kBK, p.a_row0 + mb * kBM);
+              tma_load_2d(sA + stage * kAStageBytes, &tma_a, &full[stage], k * kSliceK, p.a_row0 + mb * kBM);
             }
             if (B_MN) {
 #pragma unroll
               for (int j = 0; j < kBN / 64; ++j)
                 tma_load_2d(sB + stage * kBStageBytes + j * 8192, &tma_b, &full[stage], p.b_row0 + nb * kBN + j * 64,
-                            k * kBK);
+                            k * kSliceK);
             } else {
-              tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kBK, p.b_row0 + nb * kBN);
+              tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kSliceK, p.b_row0 + nb * kBN);
             }
             ++issued;
             if (++stage == kStages) {
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool aborted = false;
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+      constexpr uint32_t idesc = TF32 ? idesc_tf32_f32(kBM, kBN) : idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
       const uint32_t a_base = smem_u32(sA);
       const uint32_t b_base = smem_u32(sB);
       for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
@@ -339,12 +344,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a0 = a_base + stage * kAStageBytes;
           const uint32_t b0 = b_base + stage * kBStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // 16 K-elements per MMA: 32 B along a K-major row, or two 8-row
-            // K groups (2048 B) of an MN-major tile.
+          for (int kk = 0; kk < 4; ++kk) {
+            // One MMA per 32 B of K (16 bf16 or 8 tf32 elements): 32 B along a
+            // K-major row, or two 8-row K groups (2048 B) of an MN-major tile.
             const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(a0 + kk * 2048) : sdesc_kmajor_sw128(a0 + kk * 32);
             const uint64_t bd = B_MN ? sdesc_mnmajor_sw128(b0 + kk * 2048) : sdesc_kmajor_sw128(b0 + kk * 32);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+            if (TF32)
+              tc_mma_tf32(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -389,7 +397,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if (MODE == EPI_BF16) {
         epilogue_bf16(p, tcol, mb, nb, row);
       } else if (MODE == EPI_ACC_F32) {
-        epilogue_acc_f32(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        epilogue_out_f32<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+      } else if (MODE == EPI_F32) {
+        epilogue_out_f32<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
       } else {
         epilogue_dz(p, tcol, mb, nb, row, coef);
       }
@@ -399,7 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
     // Outstanding bulk stores / reduce-adds must finish before the CTA exits.
-    if ((MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32) && lane == 0) bulk_wait_group<0>();
+    if ((MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32 || MODE == EPI_F32) && lane == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before_sync();
@@ -410,20 +420,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN>
+template <int MODE, bool A_MN, bool B_MN, bool TF32 = false>
 static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                                const GemmParams& p, int grid, cudaStream_t s) {
   // Per device and cheap: set on every launch rather than caching per process.
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<MODE, A_MN, B_MN><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
+  gemm_tc_kernel<MODE, A_MN, B_MN, TF32><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
-  if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32) && c == nullptr) return cudaErrorInvalidValue;
+  if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
+    return cudaErrorInvalidValue;
   // The combinations the engine uses: the forward GEMM (both K-major), grad_h
   // (dz K-major, W MN-major or its transpose K-major), grad_W (dz and h_c
   // MN-major, or their transposes K-major).
@@ -441,6 +452,19 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a,
   if (!a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode<EPI_ACC_F32, false, true>(a, b, c, p, grid, s);
   if (a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode<EPI_ACC_F32, true, true>(a, b, c, p, grid, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc_tf32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
+                                const GemmParams& p, int grid, cudaStream_t s) {
+  if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
+    return cudaErrorInvalidValue;
+  switch (mode) {
+    case EPI_STATS: return launch_mode<EPI_STATS, false, false, true>(a, b, c, p, grid, s);
+    case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false, true>(a, b, c, p, grid, s);
+    case EPI_F32: return launch_mode<EPI_F32, false, false, true>(a, b, c, p, grid, s);
+    case EPI_ACC_F32: return launch_mode<EPI_ACC_F32, false, false, true>(a, b, c, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace flce

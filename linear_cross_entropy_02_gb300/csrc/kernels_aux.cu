@@ -320,8 +320,60 @@ __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p)
   }
 }
 
+// fp32-operand path: dz and dz^T in fp32 (64x64 tiles, transposed through
+// shared memory as in the bf16 kernel above).
+__global__ void __launch_bounds__(256) dlogits_f32_kernel(const DlogitParams p) {
+  __shared__ float tile[kDzTile][kDzTile + 1];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = blockIdx.y * kDzTile, c0 = blockIdx.x * kDzTile;
+  const int64_t n_valid = p.hdr->n_valid;
+  const float coef = n_valid == 0 ? 0.f
+                                  : (p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid)
+                                                                        : p.grad_scale);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lr = ty + 16 * k;
+    const int r = r0 + lr;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + tx * 4 + j;
+      float q = 0.f;
+      if (r < p.rows && c < p.vocab) {
+        const int64_t y = p.labels[r];
+        const float ci = y != p.ignore_index ? coef : 0.f;
+        const float sv = p.s[static_cast<int64_t>(r) * p.lds + c];
+        q = ci * (__expf(sv - p.lse[r]) - (c == y ? 1.f : 0.f));
+        if (p.softcap > 0.f) {
+          const float u = sv * p.inv_softcap;
+          q *= (1.f - u * u);
+        }
+        if (p.dz32) p.dz32[static_cast<int64_t>(r) * p.ldd + c] = q;
+      }
+      tile[lr][tx * 4 + j] = q;
+    }
+  }
+  if (!p.dzt32) return;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lc = ty + 16 * k;
+    const int c = c0 + lc;
+    if (c >= p.vocab) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = r0 + tx * 4 + j;
+      if (r < p.rows) p.dzt32[static_cast<int64_t>(c) * p.ldt + r] = tile[tx * 4 + j][lc];
+    }
+  }
+}
+
 cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s) {
   if (p.rows <= 0 || p.vocab <= 0) return cudaSuccess;
+  if (p.dz32 != nullptr || p.dzt32 != nullptr) {
+    dim3 grid((p.vocab + kDzTile - 1) / kDzTile, (p.rows + kDzTile - 1) / kDzTile);
+    dlogits_f32_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   if (p.dzt == nullptr && p.dz != nullptr) {
     dim3 grid((p.vocab + 2047) / 2048, p.rows);
     dlogits_rows_kernel<<<grid, 256, 0, s>>>(p);
@@ -368,6 +420,43 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   dim3 grid((cols + 63) / 64, (rows + 63) / 64);
   transpose_bf16_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ in, int64_t ldi, int rows,
+                                                            int cols, float* __restrict__ out, int64_t ldo) {
+  __shared__ float tile[64][65];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lr = ty + 16 * k;
+    const int r = r0 + lr;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + tx * 4 + j;
+      tile[lr][tx * 4 + j] = (r < rows && c < cols) ? in[static_cast<int64_t>(r) * ldi + c] : 0.f;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lc = ty + 16 * k;
+    const int c = c0 + lc;
+    if (c >= cols) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = r0 + tx * 4 + j;
+      if (r < rows) out[static_cast<int64_t>(c) * ldo + r] = tile[tx * 4 + j][lc];
+    }
+  }
+}
+
+cudaError_t launch_transpose_f32(const float* in, int64_t ldi, int rows, int cols, float* out, int64_t ldo,
+                                 cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid((cols + 63) / 64, (rows + 63) / 64);
+  transpose_f32_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo);
   return cudaGetLastError();
 }
 

@@ -2,10 +2,10 @@
 // branch next to the fused path (Liger-Kernel "Muse Glimmer" page, Testing Done:
 // the non-fused softcap branch; DeepSeek-V3 page, Summary: logits kept outside
 // training-with-labels). Both kernels stream the logits once each, coalesced:
-//   ce_stats   one warp per (row, 2048-column tile): lane l holds columns
-//              8l .. 8l+7 of each 256-column step; running max / sum of
-//              exponentials / argmax per lane, merged across the warp with
-//              shuffles; the lane holding the label writes its capped logit.
+//   ce_stats   one block per (row, 2048-column tile), 8 columns per thread:
+//              max / sum of exponentials / first argmax per thread, merged
+//              with shuffles and across warps in a fixed order; the thread
+//              holding the label writes its capped logit.
 //   ce_grad    one thread per 8 consecutive columns: recomputes s = cap(m x),
 //              writes dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
 // The per-tile statistics go through the same merge kernel as the fused path.
@@ -81,62 +81,46 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, int& ix, float m
 
 }  // namespace
 
+// One 256-thread block per (row, 2048-column tile): thread t holds columns
+// 8t .. 8t+7 of the tile (one 16- or 32-byte load, coalesced across the block,
+// the same pattern as the gradient kernel); per-thread max / sum / first argmax,
+// merged across each warp with shuffles and across the 8 warps in warp order.
 template <typename T>
 __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n_tiles = p.n_vtiles;
-  const int row = warp / n_tiles;
-  const int tile = warp - row * n_tiles;
-  if (row >= p.rows) return;
+  __shared__ float s_m[8];
+  __shared__ float s_s[8];
+  __shared__ int s_i[8];
+  const int row = blockIdx.y;
+  const int tile = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const T* x = static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ldx;
   const int64_t label = p.labels[row];
   const int c_begin = tile * kCeTile;
   const int c_end = min(c_begin + kCeTile, p.vocab);
+  const int c0 = c_begin + threadIdx.x * 8;
+  float v[8];
+  if (c0 + 8 <= c_end && p.vec_ok) {
+    Vec8<T>::load(x + c0, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
+  }
   float m = -INFINITY, s = 0.f;
-  int ix = c_begin;
-  // All of this lane's loads of the tile (up to kCeTile / 256 = 8 vectors) are
-  // issued before any is used, so a warp keeps 8 x 512 B in flight.
-  constexpr int kSteps = kCeTile / 256;
-  float vv[kSteps][8];
+  int ix = c0;
 #pragma unroll
-  for (int i = 0; i < kSteps; ++i) {
-    const int c0 = c_begin + lane * 8 + i * 256;
-    if (c0 + 8 <= c_end && p.vec_ok) {
-      Vec8<T>::load(x + c0, vv[i]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) vv[i][j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
+  for (int j = 0; j < 8; ++j) {
+    const bool in = c0 + j < c_end;
+    const float sv = in ? cap(v[j] * p.out_mult, p.softcap, p.inv_softcap) : -INFINITY;
+    v[j] = sv;
+    if (in && static_cast<int64_t>(c0 + j) == label) p.tgt[row] = sv;
+    if (sv > m) {
+      m = sv;
+      ix = c0 + j;
     }
   }
+  if (m != -INFINITY) {
 #pragma unroll
-  for (int i = 0; i < kSteps; ++i) {
-    const int c0 = c_begin + lane * 8 + i * 256;
-    float (&v)[8] = vv[i];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = c0 + j < c_end;
-      const float sv = in ? cap(v[j] * p.out_mult, p.softcap, p.inv_softcap) : -INFINITY;
-      v[j] = sv;
-      if (in && static_cast<int64_t>(c0 + j) == label) p.tgt[row] = sv;
-    }
-    float cm = v[0];
-    int ci = 0;
-#pragma unroll
-    for (int j = 1; j < 8; ++j)
-      if (v[j] > cm) {
-        cm = v[j];
-        ci = j;
-      }
-    if (cm > m) {
-      s = (m == -INFINITY) ? 0.f : s * __expf(m - cm);
-      m = cm;
-      ix = c0 + ci;
-    }
-    if (m != -INFINITY) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s += __expf(v[j] - m);
-    }
+    for (int j = 0; j < 8; ++j) s += __expf(v[j] - m);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -146,10 +130,19 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
     merge_stats(m, s, ix, m2, s2, ix2);
   }
   if (lane == 0) {
+    s_m[warp] = m;
+    s_s[warp] = s;
+    s_i[warp] = ix;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = s_m[0], S = s_s[0];
+    int I = s_i[0];
+    for (int w = 1; w < 8; ++w) merge_stats(M, S, I, s_m[w], s_s[w], s_i[w]);
     const int64_t o = static_cast<int64_t>(tile) * p.ldp + row;
-    p.part_max[o] = m;
-    p.part_sum[o] = s;
-    p.part_idx[o] = ix;
+    p.part_max[o] = M;
+    p.part_sum[o] = S;
+    p.part_idx[o] = I;
   }
 }
 
@@ -204,12 +197,11 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
 
 cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
-  const int64_t warps = static_cast<int64_t>(p.rows) * p.n_vtiles;
-  const int64_t blocks = (warps * 32 + 255) / 256;
+  dim3 grid(p.n_vtiles, p.rows);
   if (p.dtype == FLCE_DTYPE_BF16)
-    ce_stats_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    ce_stats_kernel<uint16_t><<<grid, 256, 0, s>>>(p);
   else
-    ce_stats_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    ce_stats_kernel<float><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,87 @@
+"""GPU parity of the fp32-operand variant (h, W and grad_h in fp32; tcgen05
+kind::tf32 GEMMs) against the fp64 oracle on the exact fp32 inputs. The pages
+run their parity and convergence suites in fp32 as well as bf16 (Liger-Kernel
+Muse Glimmer page, Testing Done; DeepSeek-V3 page, Testing Done table). Same
+tolerances as the bf16 path."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import flce_oracle
+from test_parity import check_against_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def flce():
+    import __graft_entry__
+    __graft_entry__.build()
+    import linear_cross_entropy_02_gb300 as m
+    return m
+
+
+def _inputs_f32(N, H, V, seed, ign=0.1, w_std=0.05):
+    g = torch.Generator().manual_seed(seed)
+    h = torch.randn((N, H), generator=g)
+    W = torch.randn((V, H), generator=g) * w_std
+    y = workloads.make_labels(N, V, seed, ign)
+    return h, W, y
+
+
+@pytest.mark.parametrize("case", [
+    dict(N=256, H=512, V=4096),
+    dict(N=300, H=192, V=1000, chunk_rows=128),
+    dict(N=129, H=64, V=4100),
+    dict(N=513, H=136, V=777, chunk_rows=256, softcap=30.0, out_mult=0.5),
+    dict(N=256, H=256, V=2048, softcap=2.0, out_mult=0.5, reduction="sum", grad_scale=0.75),
+])
+def test_fp32_parity(flce, case):
+    c = dict(case)
+    N, H, V = c.pop("N"), c.pop("H"), c.pop("V")
+    h, W, y = _inputs_f32(N, H, V, seed=N + H + V)
+    G0 = (np.random.default_rng(2).standard_normal((V, H)) * 1e-3).astype(np.float32).astype(np.float64)
+    gW = torch.from_numpy(G0).float().to(DEV)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True, **c)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    assert out["grad_h"].dtype == torch.float32
+    ref = flce_oracle(h, W, y, grad_W0=G0, softcap=c.get("softcap", 0.0), out_mult=c.get("out_mult", 1.0),
+                      reduction=c.get("reduction", "mean"), grad_scale=c.get("grad_scale", 1.0))
+    rep = check_against_oracle(out, ref, y, grad_W0=G0, what=f"fp32 {case}")
+    print(case, rep)
+
+
+def test_fp32_forward_and_ce_only(flce):
+    N, H, V = 400, 256, 3333
+    h, W, y = _inputs_f32(N, H, V, seed=7)
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    f = flce.flce_forward(hd, Wd, yd, return_lse=True, softcap=5.0)
+    loss, acc = flce.flce_ce_only(hd, Wd, yd, softcap=5.0)
+    torch.cuda.synchronize()
+    ref = flce_oracle(h, W, y, softcap=5.0, need_grad_h=False, need_grad_W=False)
+    assert float(loss) == float(f["loss"])
+    assert abs(float(loss) - ref["loss"]) <= 2e-3 * ref["loss"]
+    assert np.abs(f["lse"].cpu().double().numpy() - ref["lse"]).max() <= 1e-3 * np.abs(ref["lse"]).max()
+    check_against_oracle({"loss": loss, "token_accuracy": acc, "predicted": f["predicted"]}, ref, y, what="fwd")
+
+
+def test_fp32_frozen_weight_and_llama_width(flce):
+    """A Llama-width head (H = 4096) in fp32 with a frozen W, two chunks."""
+    N, H, V = 1024, 4096, 32000
+    h, W, y = _inputs_f32(N, H, V, seed=8, w_std=0.02)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=None, return_predicted=True,
+                                     chunk_rows=512)
+    torch.cuda.synchronize()
+    ref = flce_oracle(h, W, y, need_grad_W=False)
+    check_against_oracle(out, ref, y, what="fp32 llama width")
+
+
+def test_fp32_rejects_unsupported_modes(flce):
+    h, W, y = _inputs_f32(64, 64, 300, seed=9)
+    with pytest.raises(flce.FlceError):
+        flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), low_memory=True)
+    with pytest.raises(ValueError):
+        flce.flce_forward_backward(h.to(DEV), W.to(DEV).bfloat16(), y.to(DEV))
