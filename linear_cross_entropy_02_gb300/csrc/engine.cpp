@@ -356,6 +356,10 @@ int run(const flce_params* params, const Call& c) {
     g.m_tiles = (rows + kBM - 1) / kBM;
     g.n_tiles = static_cast<int>(L.n_vtiles);
     g.k_iters = (H + kBK - 1) / kBK;
+    // Groups of 16 row tiles: the group's h_c rows stay in L2 while W streams
+    // through once per group. On the DSV3 head, larger groups, and L2
+    // evict-last / evict-first policies on either operand, all measured slower:
+    // the kept lines crowd the next GEMM's operands out of L2.
     g.group_m = std::min(g.m_tiles, 16);
     g.a_row0 = static_cast<int>(r0);
     g.b_row0 = 0;
@@ -576,6 +580,8 @@ int run(const flce_params* params, const Call& c) {
       b.m_tiles = (V + kBM - 1) / kBM;
       b.n_tiles = (H + kBN - 1) / kBN;
       b.k_iters = (rows + kBK - 1) / kBK;
+      // Groups of 16 vocab tiles: on the DSV3 head this beat an N-fastest walk
+      // with h_c kept in L2 and evict-first dz loads.
       b.group_m = std::min(b.m_tiles, 16);
       b.alpha = p.out_mult;
       b.M_valid = V;

@@ -168,7 +168,7 @@ cudaError_t launch_transpose_f32(const float* in, int64_t ldi, int rows, int col
                                  cudaStream_t s);
 
 // Columns per warp task of the cross-entropy-on-logits statistics.
-constexpr int kCeTile = 2048;
+constexpr int kCeTile = 8192;
 
 struct CeParams {
   int rows, vocab, n_vtiles, ldp;

@@ -2,10 +2,10 @@
 // branch next to the fused path (Liger-Kernel "Muse Glimmer" page, Testing Done:
 // the non-fused softcap branch; DeepSeek-V3 page, Summary: logits kept outside
 // training-with-labels). Both kernels stream the logits once each, coalesced:
-//   ce_stats   one block per (row, 2048-column tile), 8 columns per thread:
-//              max / sum of exponentials / first argmax per thread, merged
-//              with shuffles and across warps in a fixed order; the thread
-//              holding the label writes its capped logit.
+//   ce_stats   one warp per (row, 8192-column tile), four 8-column loads in
+//              flight per lane: max / sum of exponentials / first argmax per
+//              lane, merged across the warp with shuffles; the lane holding the
+//              label writes its capped logit.
 //   ce_grad    one thread per 8 consecutive columns: recomputes s = cap(m x),
 //              writes dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
 // The per-tile statistics go through the same merge kernel as the fused path.
@@ -81,46 +81,64 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, int& ix, float m
 
 }  // namespace
 
-// One 256-thread block per (row, 2048-column tile): thread t holds columns
-// 8t .. 8t+7 of the tile (one 16- or 32-byte load, coalesced across the block,
-// the same pattern as the gradient kernel); per-thread max / sum / first argmax,
-// merged across each warp with shuffles and across the 8 warps in warp order.
+// One warp per (row, 8192-column tile), eight warps per block, no block-level
+// synchronisation. Per step the lane loads four 8-column pieces 256 columns
+// apart (four loads in flight, each covering 512 B per warp), so a step spans
+// 1024 columns and eight steps the tile; max / sum of exponentials / first
+// argmax per lane, merged across the warp with shuffles.
 template <typename T>
 __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
-  __shared__ float s_m[8];
-  __shared__ float s_s[8];
-  __shared__ int s_i[8];
-  const int row = blockIdx.y;
-  const int tile = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t task = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = static_cast<int>(task / p.n_vtiles);
+  const int tile = static_cast<int>(task - static_cast<int64_t>(row) * p.n_vtiles);
+  if (row >= p.rows) return;
   const T* x = static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ldx;
   const int64_t label = p.labels[row];
   const int c_begin = tile * kCeTile;
   const int c_end = min(c_begin + kCeTile, p.vocab);
-  const int c0 = c_begin + threadIdx.x * 8;
-  float v[8];
-  if (c0 + 8 <= c_end && p.vec_ok) {
-    Vec8<T>::load(x + c0, v);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
-  }
   float m = -INFINITY, s = 0.f;
-  int ix = c0;
+  int ix = c_begin;
+  for (int base = c_begin; base < c_end; base += 1024) {
+    float v[4][8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const bool in = c0 + j < c_end;
-    const float sv = in ? cap(v[j] * p.out_mult, p.softcap, p.inv_softcap) : -INFINITY;
-    v[j] = sv;
-    if (in && static_cast<int64_t>(c0 + j) == label) p.tgt[row] = sv;
-    if (sv > m) {
-      m = sv;
-      ix = c0 + j;
+    for (int q = 0; q < 4; ++q) {
+      const int c0 = base + q * 256 + lane * 8;
+      if (c0 + 8 <= c_end && p.vec_ok) {
+        Vec8<T>::load(x + c0, v[q]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[q][j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
+      }
     }
-  }
-  if (m != -INFINITY) {
+    float cm = -INFINITY;
+    int ci = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s += __expf(v[j] - m);
+    for (int q = 0; q < 4; ++q) {
+      const int c0 = base + q * 256 + lane * 8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool in = c0 + j < c_end;
+        const float sv = in ? cap(v[q][j] * p.out_mult, p.softcap, p.inv_softcap) : -INFINITY;
+        v[q][j] = sv;
+        if (in && static_cast<int64_t>(c0 + j) == label) p.tgt[row] = sv;
+        if (sv > cm) {  // columns go up with (q, j): the first maximum is kept
+          cm = sv;
+          ci = c0 + j;
+        }
+      }
+    }
+    if (cm > m) {
+      s = (m == -INFINITY) ? 0.f : s * __expf(m - cm);
+      m = cm;
+      ix = ci;
+    }
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += __expf(v[q][j] - m);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -130,19 +148,10 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
     merge_stats(m, s, ix, m2, s2, ix2);
   }
   if (lane == 0) {
-    s_m[warp] = m;
-    s_s[warp] = s;
-    s_i[warp] = ix;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = s_m[0], S = s_s[0];
-    int I = s_i[0];
-    for (int w = 1; w < 8; ++w) merge_stats(M, S, I, s_m[w], s_s[w], s_i[w]);
     const int64_t o = static_cast<int64_t>(tile) * p.ldp + row;
-    p.part_max[o] = M;
-    p.part_sum[o] = S;
-    p.part_idx[o] = I;
+    p.part_max[o] = m;
+    p.part_sum[o] = s;
+    p.part_idx[o] = ix;
   }
 }
 
@@ -197,11 +206,12 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
 
 cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
-  dim3 grid(p.n_vtiles, p.rows);
+  const int64_t warps = static_cast<int64_t>(p.rows) * p.n_vtiles;
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
   if (p.dtype == FLCE_DTYPE_BF16)
-    ce_stats_kernel<uint16_t><<<grid, 256, 0, s>>>(p);
+    ce_stats_kernel<uint16_t><<<blocks, 256, 0, s>>>(p);
   else
-    ce_stats_kernel<float><<<grid, 256, 0, s>>>(p);
+    ce_stats_kernel<float><<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ def test_workspace_independent_of_n_beyond_a_chunk(L):
     assert L.flce_workspace_size(ctypes.byref(pk), 2, 1, 1) > both + 129280 * 7168 * 2
     # cross-entropy on materialised logits keeps only per-tile statistics
     pc = _params(L, N=131072, H=0, V=151936)
-    assert 0 < L.flce_workspace_size(ctypes.byref(pc), 3, 0, 0) < 20e6
+    assert 0 < L.flce_workspace_size(ctypes.byref(pc), 3, 0, 0) < 100e6
 
 
 @pytest.mark.parametrize("field,value", [("hidden", 0), ("vocab", 0), ("n_rows", -1), ("softcap", -1.0),

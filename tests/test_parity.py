@@ -291,3 +291,38 @@ def test_zipf_labels_and_row_sums(flce):
     valid = y != -100
     bound = 2.0 ** -8 / int(valid.sum()) * h[valid].double().abs().sum(0).to(DEV)
     assert torch.all(col <= bound)
+
+
+@pytest.mark.parametrize("flags", [0, 8])
+@pytest.mark.parametrize("case", [
+    dict(N=5, H=64, V=100),                                   # one partial row tile, V < one vocab tile
+    dict(N=130, H=128, V=257, ignore_index=-1),               # custom ignore index, one column past a tile
+    dict(N=200, H=64, V=1000, out_mult=-0.5, softcap=3.0),    # negative multiplier: the argmax flips
+])
+def test_small_and_unusual_heads(flce, flags, case):
+    c = dict(case)
+    N, H, V = c.pop("N"), c.pop("H"), c.pop("V")
+    ign = c.pop("ignore_index", -100)
+    h, W, y = _inputs(N, H, V, seed=N * 7 + V, W_scale=0.1)
+    y = torch.where(y == -100, torch.full_like(y, ign), y)
+    gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, ignore_index=ign,
+                                     return_predicted=True, flags=flags, vocab_slab=256 if flags else 0, **c)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = flce_oracle(h, W, y, ignore_index=ign, softcap=c.get("softcap", 0.0), out_mult=c.get("out_mult", 1.0))
+    lab = torch.where(y == ign, torch.full_like(y, -100), y)       # the checker's ignored-row marker
+    check_against_oracle(out, ref, lab, what=f"{case} flags={flags}")
+
+
+def test_strided_hidden_rows(flce):
+    """h with a row stride larger than H (a view into a wider buffer) is read in place."""
+    N, H, V = 300, 128, 2000
+    big, W, y = _inputs(N, 192, V, seed=13)
+    h = big[:, :H]
+    W = W[:, :H].contiguous()
+    assert h.stride(0) == 192
+    gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
+    out = flce.flce_forward_backward(big.to(DEV)[:, :H], W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True)
+    torch.cuda.synchronize()
+    check_against_oracle(out, flce_oracle(h, W, y), y, what="strided h")
