@@ -91,7 +91,10 @@ def _check(h: torch.Tensor, W: torch.Tensor, labels: torch.Tensor):
 
 
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    """The cached workspace of (device, current stream): calls on one stream
+    reuse it in stream order; calls on different streams never share one."""
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    key = (dev, torch.cuda.current_stream(dev).cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
         _workspaces.pop(key, None)
@@ -273,9 +276,10 @@ def flce_cross_entropy(logits, labels, *, softcap=0.0, out_mult=1.0, ignore_inde
 
 def flce_get_status(device=None) -> int:
     """Synchronises the current stream and returns the device status word of
-    the last call on this device's cached workspace (0 = no device error)."""
+    the last call on the cached workspace of this device and stream (0 = no
+    device error)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    ws = _workspaces.get(dev.index)
+    ws = _workspaces.get((dev.index, torch.cuda.current_stream(dev).cuda_stream))
     if ws is None:
         return 0
     st = ctypes.c_int32(0)

@@ -423,10 +423,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int MODE, bool A_MN, bool B_MN, bool TF32 = false>
 static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                                const GemmParams& p, int grid, cudaStream_t s) {
-  // Per device and cheap: set on every launch rather than caching per process.
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  // The shared-memory opt-in is a per-device function attribute: set it on the
+  // first launch on each device (outside any stream capture that follows).
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
   gemm_tc_kernel<MODE, A_MN, B_MN, TF32><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
   return cudaGetLastError();
 }

@@ -81,64 +81,97 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, int& ix, float m
 
 }  // namespace
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Per-lane statistics of one step: four 8-column pieces 256 columns apart.
+// FULL: every column is inside the tile; CAP: softcap on. The label is found
+// once per warp task, not per element (its lane writes it separately).
+template <typename T, bool FULL, bool CAP>
+__device__ __forceinline__ void ce_step(const CeParams& p, const T* x, int base, int c_end, int lane, float& m,
+                                        float& s, int& ix) {
+  float v[4][8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c0 = base + q * 256 + lane * 8;
+    if (FULL && p.vec_ok) {
+      Vec8<T>::load(x + c0, v[q]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[q][j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
+    }
+  }
+  float cm = -INFINITY;
+  int ci = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float sv = v[q][j] * p.out_mult;
+      if (CAP) sv = p.softcap * tanhf(sv * p.inv_softcap);
+      if (!FULL && base + q * 256 + lane * 8 + j >= c_end) sv = -INFINITY;
+      v[q][j] = sv;
+      if (sv > cm) {  // columns go up with (q, j): the first maximum is kept
+        cm = sv;
+        ci = q * 256 + j;
+      }
+    }
+  }
+  if (cm > m) {
+    s = (m == -INFINITY) ? 0.f : s * ex2f_approx((m - cm) * kLog2e);
+    m = cm;
+    ix = base + lane * 8 + ci;
+  }
+  if (m != -INFINITY) {
+    const float ml = m * kLog2e;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += ex2f_approx(fmaf(v[q][j], kLog2e, -ml));
+  }
+}
+
 // One warp per (row, 8192-column tile), eight warps per block, no block-level
-// synchronisation. Per step the lane loads four 8-column pieces 256 columns
-// apart (four loads in flight, each covering 512 B per warp), so a step spans
-// 1024 columns and eight steps the tile; max / sum of exponentials / first
-// argmax per lane, merged across the warp with shuffles.
+// synchronisation: eight steps of 1024 columns, each with four 16- or 32-byte
+// loads per lane in flight, max / sum of exponentials / first argmax per lane,
+// then a shuffle merge across the warp.
 template <typename T>
 __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
-  const int64_t task = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int task = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  const int row = static_cast<int>(task / p.n_vtiles);
-  const int tile = static_cast<int>(task - static_cast<int64_t>(row) * p.n_vtiles);
+  const int row = task / p.n_vtiles;
+  const int tile = task - row * p.n_vtiles;
   if (row >= p.rows) return;
   const T* x = static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ldx;
-  const int64_t label = p.labels[row];
   const int c_begin = tile * kCeTile;
   const int c_end = min(c_begin + kCeTile, p.vocab);
   float m = -INFINITY, s = 0.f;
   int ix = c_begin;
   for (int base = c_begin; base < c_end; base += 1024) {
-    float v[4][8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c0 = base + q * 256 + lane * 8;
-      if (c0 + 8 <= c_end && p.vec_ok) {
-        Vec8<T>::load(x + c0, v[q]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[q][j] = (c0 + j < c_end) ? Vec8<T>::load1(x + c0 + j) : 0.f;
-      }
+    const bool full = base + 1024 <= c_end;
+    if (p.softcap > 0.f) {
+      if (full)
+        ce_step<T, true, true>(p, x, base, c_end, lane, m, s, ix);
+      else
+        ce_step<T, false, true>(p, x, base, c_end, lane, m, s, ix);
+    } else {
+      if (full)
+        ce_step<T, true, false>(p, x, base, c_end, lane, m, s, ix);
+      else
+        ce_step<T, false, false>(p, x, base, c_end, lane, m, s, ix);
     }
-    float cm = -INFINITY;
-    int ci = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c0 = base + q * 256 + lane * 8;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool in = c0 + j < c_end;
-        const float sv = in ? cap(v[q][j] * p.out_mult, p.softcap, p.inv_softcap) : -INFINITY;
-        v[q][j] = sv;
-        if (in && static_cast<int64_t>(c0 + j) == label) p.tgt[row] = sv;
-        if (sv > cm) {  // columns go up with (q, j): the first maximum is kept
-          cm = sv;
-          ci = c0 + j;
-        }
-      }
-    }
-    if (cm > m) {
-      s = (m == -INFINITY) ? 0.f : s * __expf(m - cm);
-      m = cm;
-      ix = ci;
-    }
-    if (m != -INFINITY) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s += __expf(v[q][j] - m);
-    }
+  }
+  // The label's capped logit, written by the lane that read that column (the
+  // same arithmetic on a re-read of the one element).
+  const int64_t label = p.labels[row];
+  if (label >= c_begin && label < c_end) {
+    const int d = static_cast<int>(label - c_begin);
+    if (((d >> 3) & 31) == lane) p.tgt[row] = cap(Vec8<T>::load1(x + label) * p.out_mult, p.softcap, p.inv_softcap);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -155,6 +188,39 @@ __global__ void __launch_bounds__(256) ce_stats_kernel(const CeParams p) {
   }
 }
 
+template <typename T, bool CAP>
+__device__ __forceinline__ void ce_grad8(const CeParams& p, const T* x, T* g, int c0, bool full, float lse_l2e,
+                                         float cm, int label_local) {
+  float v[8];
+  if (full) {
+    Vec8<T>::load(x + c0, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < p.vocab) ? Vec8<T>::load1(x + c0 + j) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float sv = v[j] * p.out_mult;
+    float cap_d = 1.f;
+    if (CAP) {
+      sv = p.softcap * tanhf(sv * p.inv_softcap);
+      const float u = sv * p.inv_softcap;
+      cap_d = 1.f - u * u;
+    }
+    const float q = ex2f_approx(fmaf(sv, kLog2e, -lse_l2e)) - (j == label_local ? 1.f : 0.f);
+    v[j] = CAP ? cm * q * cap_d : cm * q;
+  }
+  if (full) {
+    Vec8<T>::store(g + c0, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (c0 + j < p.vocab) Vec8<T>::store1(g + c0 + j, v[j]);
+  }
+}
+
+// One thread per 8 consecutive columns: recomputes s = cap(m x) and writes
+// dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
 template <typename T>
 __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
   const int row = blockIdx.y;
@@ -173,35 +239,17 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
   } else {
     c = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
   }
-  const float lse = p.lse[row];
+  const float lse_l2e = p.lse[row] * kLog2e;
   const float cm = c * p.out_mult;
+  const int64_t dl = valid ? label - c0 : -1;
+  const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
   const T* x = static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ldx;
   T* g = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.ldg;
-  float v[8];
   const bool full = c0 + 8 <= p.vocab && p.vec_ok;
-  if (full) {
-    Vec8<T>::load(x + c0, v);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < p.vocab) ? Vec8<T>::load1(x + c0 + j) : 0.f;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float sv = cap(v[j] * p.out_mult, p.softcap, p.inv_softcap);
-    float q = __expf(sv - lse) - (static_cast<int64_t>(c0 + j) == label ? 1.f : 0.f);
-    if (p.softcap > 0.f) {
-      const float u = sv * p.inv_softcap;
-      q *= (1.f - u * u);
-    }
-    v[j] = cm * q;
-  }
-  if (full) {
-    Vec8<T>::store(g + c0, v);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (c0 + j < p.vocab) Vec8<T>::store1(g + c0 + j, v[j]);
-  }
+  if (p.softcap > 0.f)
+    ce_grad8<T, true>(p, x, g, c0, full, lse_l2e, cm, label_local);
+  else
+    ce_grad8<T, false>(p, x, g, c0, full, lse_l2e, cm, label_local);
 }
 
 cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s) {
