@@ -35,6 +35,9 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "FLCE fwd+bwd tokens/s and TFLOP/s (6·N·H·V) as % of GB300 bf16 tensor peak"
+# Nominal dense tf32 / bf16 tensor rate of GB300 (1.1 / 2.25 PFLOP/s): the tf32
+# path's peak is the measured bf16 peak scaled by it.
+TF32_OVER_BF16 = 1.1 / 2.25
 UNIT = "tokens/s"
 
 
@@ -231,6 +234,8 @@ def run_ours(args, w):
     if args.ce_logits:
         return run_ce_logits(args, w, world, rank, local, dist, flce)
     h_cpu, W_cpu, lab_cpu = workloads.make_inputs(w)
+    if args.fp32:  # the same bf16-valued inputs carried in fp32: the tf32 tensor-core path
+        h_cpu, W_cpu = h_cpu.float(), W_cpu.float()
     h = h_cpu.to(dev)
     W = W_cpu.to(dev)
     lab = lab_cpu.to(dev)
@@ -307,6 +312,7 @@ def run_ours(args, w):
     peaks = _peaks()
     flops = w.flops
     tflops = flops / (ms / 1e3) / 1e12
+    step_peak = peaks["bf16_sustained"] * (TF32_OVER_BF16 if args.fp32 else 1.0)
     line = None
     if rank == 0:
         # roofline of the dominant kernel, from the per-launch events of the timed region
@@ -321,9 +327,11 @@ def run_ours(args, w):
             n_launch, tms = kernels[dom]
             per_launch_flops = gemm_flops[dom] * args.steps / n_launch
             achieved = per_launch_flops / (tms / n_launch / 1e3) / 1e12
-            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
-                    "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
+            peak = peaks["bf16_sustained"] * (TF32_OVER_BF16 if args.fp32 else 1.0)
+            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": (f"bf16_tflops_sustained ({peaks['source']}) x 1.1/2.25 nominal tf32/bf16"
+                                    if args.fp32 else f"bf16_tflops_sustained ({peaks['source']})"),
                     "traffic": recorded_traffic(w.name + ("-lowmem" if args.low_memory else ""), dom),
                     "traffic_unit": "bytes per launch (dram read + write, ncu)",
                     "algorithmic_flops_per_launch": per_launch_flops,
@@ -338,16 +346,17 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w, args.chunk_rows),
-            "tflops": tflops, "pct_of_peak": 100.0 * tflops / peaks["bf16_sustained"],
-            "peak_tflops": peaks["bf16_sustained"], "peak_source": peaks["source"],
+            "vs_baseline": None, "dtype": "f32 (tf32 tensor cores)" if args.fp32 else "bf16", "data": "synthetic",
+            "config": _config(w, args.chunk_rows),
+            "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
+            "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,
             "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if args.low_memory and w.mode == "fwd_bwd"
                                                        else 1.0),
             "backward": "recompute (low memory)" if args.low_memory else "stored logits",
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT,
-                    "h2d_bytes_per_step": h.numel() * 2 + lab.numel() * 8, "d2h_bytes_per_step": 8},
+                    "h2d_bytes_per_step": h.numel() * h.element_size() + lab.numel() * 8, "d2h_bytes_per_step": 8},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "kernels": {k: {"launches": v[0], "ms": v[1], "share": v[1] / total_ms} for k, v in kernels.items()},
@@ -473,6 +482,7 @@ def main():
     ap.add_argument("--low-memory", action="store_true",
                     help="recompute backward: no stored logits, dlogits per vocab slab")
     ap.add_argument("--vocab-slab", type=int, default=0)
+    ap.add_argument("--fp32", action="store_true", help="fp32 h and W: the tf32 tensor-core path")
     ap.add_argument("--ce-logits", action="store_true",
                     help="time the cross-entropy on materialised bf16 logits [N, V] instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "flce_device.cuh"
 #include "flce_epilogue.cuh"
 #include "flce_internal.h"
 
@@ -272,19 +273,14 @@ __global__ void __launch_bounds__(256) dlogits_kernel(const DlogitParams p) {
   }
 }
 
-// Product path (no transposed copy): plain streaming over the rows, one
-// thread per 8 consecutive columns: 32 B of s read, 16 B of dz written.
-__global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p) {
-  const int r = blockIdx.y;
-  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (c >= p.vocab) return;
-  const int64_t n_valid = p.hdr->n_valid;
-  const int64_t y = p.labels[r];
-  float ci = 0.f;
-  if (y != p.ignore_index && n_valid > 0)
-    ci = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
-  const float lse = p.lse[r];
-  const float* srow = p.s + static_cast<int64_t>(r) * p.lds;
+// Product path (no transposed copy): plain streaming over the rows. A block
+// covers 8192 columns of one row; thread t handles four 8-column pieces
+// 2048 i + 8 t (each piece: 32 B of s read, 16 B of dz written, contiguous
+// across the block), so the per-row setup is paid once per 32 columns.
+// exp(s - lse) is 2^(s log2 e - lse log2 e) on the special-function unit.
+template <bool CAP>
+__device__ __forceinline__ void dlogits_piece(const DlogitParams& p, const float* srow, uint16_t* drow, int c,
+                                              float ci, float lse_l2e, int label_local) {
   float sv[8];
   const bool full = c + 8 <= p.vocab;
   if (full) {
@@ -296,27 +292,49 @@ __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p)
 #pragma unroll
     for (int j = 0; j < 8; ++j) sv[j] = (c + j < p.vocab) ? srow[c + j] : 0.f;
   }
-  uint16_t b[8];
+  uint32_t w[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float q = ci * (__expf(sv[j] - lse) - (static_cast<int64_t>(c + j) == y ? 1.f : 0.f));
-    if (p.softcap > 0.f) {
-      const float u = sv[j] * p.inv_softcap;
-      q *= (1.f - u * u);
+  for (int j = 0; j < 8; j += 2) {
+    float q0 = ex2_approx(fmaf(sv[j], 1.4426950408889634f, -lse_l2e)) - (j == label_local ? 1.f : 0.f);
+    float q1 = ex2_approx(fmaf(sv[j + 1], 1.4426950408889634f, -lse_l2e)) - (j + 1 == label_local ? 1.f : 0.f);
+    if (CAP) {
+      const float u0 = sv[j] * p.inv_softcap, u1 = sv[j + 1] * p.inv_softcap;
+      q0 *= (1.f - u0 * u0);
+      q1 *= (1.f - u1 * u1);
     }
-    b[j] = float_to_bf16_bits(q);
+    w[j / 2] = static_cast<uint32_t>(float_to_bf16_bits(ci * q0)) |
+               (static_cast<uint32_t>(float_to_bf16_bits(ci * q1)) << 16);
   }
-  uint16_t* drow = p.dz + static_cast<int64_t>(r) * p.ldd;
   if (full) {
-    uint4 pk;
-    pk.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
-    pk.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
-    pk.z = static_cast<uint32_t>(b[4]) | (static_cast<uint32_t>(b[5]) << 16);
-    pk.w = static_cast<uint32_t>(b[6]) | (static_cast<uint32_t>(b[7]) << 16);
-    *reinterpret_cast<uint4*>(drow + c) = pk;
+    *reinterpret_cast<uint4*>(drow + c) = make_uint4(w[0], w[1], w[2], w[3]);
   } else {
     for (int j = 0; j < 8; ++j)
-      if (c + j < p.vocab) drow[c + j] = b[j];
+      if (c + j < p.vocab) drow[c + j] = static_cast<uint16_t>(w[j / 2] >> (16 * (j & 1)));
+  }
+}
+
+__global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p) {
+  const int r = blockIdx.y;
+  const int c_base = blockIdx.x * 8192 + threadIdx.x * 8;
+  if (c_base >= p.vocab) return;
+  const int64_t n_valid = p.hdr->n_valid;
+  const int64_t y = p.labels[r];
+  float ci = 0.f;
+  if (y != p.ignore_index && n_valid > 0)
+    ci = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
+  const float lse_l2e = p.lse[r] * 1.4426950408889634f;
+  const float* srow = p.s + static_cast<int64_t>(r) * p.lds;
+  uint16_t* drow = p.dz + static_cast<int64_t>(r) * p.ldd;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c_base + i * 2048;
+    if (c >= p.vocab) break;
+    const int64_t dl = y - c;
+    const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
+    if (p.softcap > 0.f)
+      dlogits_piece<true>(p, srow, drow, c, ci, lse_l2e, label_local);
+    else
+      dlogits_piece<false>(p, srow, drow, c, ci, lse_l2e, label_local);
   }
 }
 
@@ -375,7 +393,7 @@ cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s) {
     return cudaGetLastError();
   }
   if (p.dzt == nullptr && p.dz != nullptr) {
-    dim3 grid((p.vocab + 2047) / 2048, p.rows);
+    dim3 grid((p.vocab + 8191) / 8192, p.rows);
     dlogits_rows_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
   }

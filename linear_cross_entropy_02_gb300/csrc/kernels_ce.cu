@@ -6,8 +6,9 @@
 //              flight per lane: max / sum of exponentials / first argmax per
 //              lane, merged across the warp with shuffles; the lane holding the
 //              label writes its capped logit.
-//   ce_grad    one thread per 8 consecutive columns: recomputes s = cap(m x),
-//              writes dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
+//   ce_grad    one block per 8192 columns of a row, four 8-column pieces per
+//              thread: recomputes s = cap(m x), writes
+//              dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
 // The per-tile statistics go through the same merge kernel as the fused path.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -219,13 +220,14 @@ __device__ __forceinline__ void ce_grad8(const CeParams& p, const T* x, T* g, in
   }
 }
 
-// One thread per 8 consecutive columns: recomputes s = cap(m x) and writes
+// A block covers 8192 columns of one row; thread t handles four 8-column
+// pieces 2048 i + 8 t: recomputes s = cap(m x) and writes
 // dL/dx = m c_i (exp(s - lse_i) - [j = y_i]) (1 - (s/T)^2).
 template <typename T>
 __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
   const int row = blockIdx.y;
-  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (row >= p.rows || c0 >= p.vocab) return;
+  const int c_base = blockIdx.x * 8192 + threadIdx.x * 8;
+  if (row >= p.rows || c_base >= p.vocab) return;
   const int64_t label = p.labels[row];
   const bool valid = label != p.ignore_index;
   const int64_t n_valid = p.hdr->n_valid;
@@ -241,15 +243,20 @@ __global__ void __launch_bounds__(256) ce_grad_kernel(const CeParams p) {
   }
   const float lse_l2e = p.lse[row] * kLog2e;
   const float cm = c * p.out_mult;
-  const int64_t dl = valid ? label - c0 : -1;
-  const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
   const T* x = static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ldx;
   T* g = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.ldg;
-  const bool full = c0 + 8 <= p.vocab && p.vec_ok;
-  if (p.softcap > 0.f)
-    ce_grad8<T, true>(p, x, g, c0, full, lse_l2e, cm, label_local);
-  else
-    ce_grad8<T, false>(p, x, g, c0, full, lse_l2e, cm, label_local);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c0 = c_base + i * 2048;
+    if (c0 >= p.vocab) break;
+    const int64_t dl = valid ? label - c0 : -1;
+    const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
+    const bool full = c0 + 8 <= p.vocab && p.vec_ok;
+    if (p.softcap > 0.f)
+      ce_grad8<T, true>(p, x, g, c0, full, lse_l2e, cm, label_local);
+    else
+      ce_grad8<T, false>(p, x, g, c0, full, lse_l2e, cm, label_local);
+  }
 }
 
 cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s) {
@@ -265,7 +272,7 @@ cudaError_t launch_ce_stats(const CeParams& p, cudaStream_t s) {
 
 cudaError_t launch_ce_grad(const CeParams& p, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
-  dim3 grid((p.vocab + 2047) / 2048, p.rows);
+  dim3 grid((p.vocab + 8191) / 8192, p.rows);
   if (p.dtype == FLCE_DTYPE_BF16)
     ce_grad_kernel<uint16_t><<<grid, 256, 0, s>>>(p);
   else
