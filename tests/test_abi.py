@@ -138,3 +138,17 @@ def test_binding_rejects_cpu_tensors():
     y = torch.zeros(4, dtype=torch.int64)
     with pytest.raises(ValueError, match="CUDA"):
         flce.flce_ce_only(h, W, y)
+
+
+def test_params_struct_matches_header():
+    """ctypes' FlceParams has the fields of the header's flce_params, in order and
+    with the same C types, so the two agree on the struct's layout."""
+    from linear_cross_entropy_02_gb300._lib import FlceParams
+    with open(os.path.join(ROOT, "include", "flce.h")) as f:
+        src = f.read()
+    body = src[src.index("typedef struct flce_params {"):src.index("} flce_params;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    decl = re.findall(r"^\s*(int64_t|int32_t|float)\s+(\w+);", body, flags=re.M)
+    ctype = {"int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "float": ctypes.c_float}
+    assert [(n, ctype[t]) for t, n in decl] == list(FlceParams._fields_)
+    assert ctypes.sizeof(FlceParams) == 104
