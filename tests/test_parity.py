@@ -326,3 +326,24 @@ def test_strided_hidden_rows(flce):
     out = flce.flce_forward_backward(big.to(DEV)[:, :H], W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True)
     torch.cuda.synchronize()
     check_against_oracle(out, flce_oracle(h, W, y), y, what="strided h")
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_exact_tie_across_vocab_tiles_keeps_lowest_index(flce, flags):
+    """Two identical rows of W in different 256-column vocab tiles (and chunks of
+    the statistics) that dominate every row's logits: the capped logits tie
+    bit for bit, and the argmax must be the lower index (the reading of the
+    tie-break), both within the forward GEMM's tile walk and in the merge."""
+    N, H, V = 96, 128, 1500
+    j1, j2 = 300, 1210
+    h = workloads.make_hidden(N, H, 40).abs()          # positive rows
+    W = workloads.make_weight(V, H, 40)
+    W[j1] = 0.5
+    W[j2] = 0.5
+    y = workloads.make_labels(N, V, 40, 0.1)
+    y[:10] = j2                                         # labelled with the tied twin: counted as wrong
+    out = run_fwd_bwd(flce, h, W, y, flags=flags)
+    pred = out["predicted"].cpu()
+    assert torch.all(pred == j1)
+    valid = (y != -100)
+    assert round(float(out["token_accuracy"]) * int(valid.sum())) == int(((y == j1) & valid).sum())
