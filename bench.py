@@ -259,23 +259,23 @@ def run_ours(args, w):
         raise RuntimeError(f"device status {flce.flce_get_status()} after warm-up")
 
     stream = torch.cuda.current_stream(dev)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     launches0 = flce.flce_launch_count()
     flce.flce_profile_begin(True)
     with ClockSampler(local) as clk:
         _barrier(dist)
         torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(args.steps):
+        marks[0].record(stream)
+        for k in range(args.steps):
             step()
-        stop.record(stream)
+            marks[k + 1].record(stream)
         torch.cuda.synchronize()
         _barrier(dist)
     kernels = flce.flce_profile_read()
     flce.flce_profile_begin(False)
     launches = flce.flce_launch_count() - launches0
-    ms = start.elapsed_time(stop) / args.steps
+    ms = marks[0].elapsed_time(marks[-1]) / args.steps
+    per_step = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
     if flce.flce_get_status() != 0:
         raise RuntimeError(f"device status {flce.flce_get_status()} after timed steps")
     ms_max = _max_over_ranks(dist, ms)
@@ -345,10 +345,14 @@ def run_ours(args, w):
             n, t = cpu_oracle_rate(w, weight_f64(W_cpu), h_cpu[:R], lab_cpu[:R], warmup=True)
             cpu = {"value": n / t[0], "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                    "sample": f"first {R} rows of the workload, full fp64 forward+backward over all "
-                             f"{w.vocab} logits (numpy), after one untimed warm-up call", "seconds": t[0]}
+                             f"{w.vocab} logits (numpy), after one untimed warm-up call", "seconds": t[0],
+                   "extrapolated_full_step_s": t[0] * w.n_rows / n,
+                   "extrapolation": "measured seconds per sampled row x the workload's rows (the oracle's "
+                                    "cost is linear in rows); extrapolated, not measured"}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step_median": statistics.median(per_step), "ms_per_step_min": min(per_step),
             "vs_baseline": None, "dtype": "f32 (tf32 tensor cores)" if args.fp32 else "bf16", "data": "synthetic",
             "config": _config(w, args.chunk_rows),
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
@@ -397,23 +401,23 @@ def run_ce_logits(args, w, world, rank, local, dist, flce):
     if flce.flce_get_status() != 0:
         raise RuntimeError("device status after warm-up")
     stream = torch.cuda.current_stream(dev)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     launches0 = flce.flce_launch_count()
     flce.flce_profile_begin(True)
     with ClockSampler(local) as clk:
         _barrier(dist)
         torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(args.steps):
+        marks[0].record(stream)
+        for k in range(args.steps):
             step()
-        stop.record(stream)
+            marks[k + 1].record(stream)
         torch.cuda.synchronize()
         _barrier(dist)
     kernels = flce.flce_profile_read()
     flce.flce_profile_begin(False)
     launches = flce.flce_launch_count() - launches0
-    ms = start.elapsed_time(stop) / args.steps
+    ms = marks[0].elapsed_time(marks[-1]) / args.steps
+    per_step = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
     ms_max = _max_over_ranks(dist, ms)
     rows_total = _sum_over_ranks(dist, float(w.n_rows))
 
@@ -450,7 +454,8 @@ def run_ce_logits(args, w, world, rank, local, dist, flce):
         achieved = per_launch / (tms / n_launch / 1e3) / 1e9
         line = {
             "metric": METRIC, "value": rows_total / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "ms_per_step_median": statistics.median(per_step),
+            "ms_per_step_min": min(per_step), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(_config(w, args.chunk_rows), mode="cross_entropy on materialised bf16 logits [N, V]",
                            l2="logits larger than L2 (no flush needed)"),

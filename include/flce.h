@@ -181,6 +181,21 @@ int flce_cross_entropy(const flce_params* p, const void* logits, int logits_dtyp
                        float* row_loss, const float* row_scale, void* grad_logits,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Multiplies a gradient by a device scalar and converts it: y_k = scale * x_k
+ * for k < n, rounded to y_dtype (bf16 with round to nearest even). This is the
+ * upstream factor of an autograd backward (the chain rule through the loss):
+ * the fused entry points take grad_scale as a host float, but a caller that
+ * computes the gradients during the forward, as the pages' fused
+ * linear-cross-entropy functions do, learns the factor only afterwards, as a
+ * device scalar. x, y: device arrays of n elements of x_dtype / y_dtype
+ * (FLCE_DTYPE_*), in any alignment (16-byte aligned ones take the vector
+ * path); y may be x itself (in place) when the dtypes match, and must not
+ * overlap it otherwise. scale: device float, or NULL for 1.
+ * Returns FLCE_ERR_ARG for n < 0, an unknown dtype, a NULL array with n > 0
+ * or an overlap that is not exact in-place; FLCE_ERR_UNSUPPORTED off sm_103. */
+int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_t n, const float* scale,
+                        void* stream);
+
 /* Synchronises `stream` and returns (in *status) the device status word of the
  * last call that used this workspace: 0 or FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT.
  * Return value: FLCE_OK or FLCE_ERR_ARG / FLCE_ERR_CUDA. */
@@ -197,7 +212,7 @@ int64_t flce_launch_count(void);
  * flce_profile_begin(0) stops. flce_profile_read synchronises the recorded
  * events and fills, for kernel ids 0..n-1, the launch count and the summed
  * milliseconds; it returns the number of kernel ids (FLCE_NUM_KERNELS). */
-#define FLCE_NUM_KERNELS 14
+#define FLCE_NUM_KERNELS 15
 int flce_profile_begin(int enable);
 int flce_profile_read(int64_t* launches, double* total_ms, int n);
 const char* flce_kernel_name(int id);

@@ -26,8 +26,9 @@ from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEM
                    FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
 
 __all__ = [
-    "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward", "flce_cross_entropy", "flce_workspace_size", "flce_get_status",
-    "flce_launch_count", "flce_profile_begin", "flce_profile_read", "FlceError",
+    "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward", "flce_cross_entropy",
+    "flce_scale_gradient", "flce_workspace_size", "flce_get_status", "flce_launch_count", "flce_profile_begin",
+    "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
 ]
 
 _REDUCTIONS = {"mean": FLCE_REDUCTION_MEAN, "sum": FLCE_REDUCTION_SUM, "none": _lib.FLCE_REDUCTION_NONE}
@@ -272,6 +273,100 @@ def flce_cross_entropy(logits, labels, *, softcap=0.0, out_mult=1.0, ignore_inde
     lead = logits.shape[:-1]
     return {"loss": loss, "token_accuracy": acc, "predicted": None if pred is None else pred.view(lead),
             "row_loss": row_loss.view(lead), "grad_logits": None if grad is None else grad.view(logits.shape)}
+
+
+def flce_scale_gradient(x: torch.Tensor, scale: Optional[torch.Tensor] = None, *, out_dtype=None,
+                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out = scale * x in out_dtype (bf16 results rounded to nearest even),
+    computed by the library's kernel. x: contiguous bf16 or fp32 CUDA tensor;
+    scale: fp32 CUDA tensor of one element, or None for 1; out=x scales in
+    place (same dtype only)."""
+    if not isinstance(x, torch.Tensor) or x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor (the library has no CPU path)")
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    for t in (x.dtype, out_dtype):
+        if t not in (torch.bfloat16, torch.float32):
+            raise ValueError("x and out must be bfloat16 or float32")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if scale is not None:
+        if (not isinstance(scale, torch.Tensor) or scale.device != x.device or scale.dtype != torch.float32
+                or scale.numel() != 1):
+            raise ValueError("scale must be a one-element fp32 tensor on x's device")
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    elif out.dtype != out_dtype or out.shape != x.shape or not out.is_contiguous() or out.device != x.device:
+        raise ValueError("out must be a contiguous tensor of x's shape and device in out_dtype")
+    rc = _lib.lib().flce_scale_gradient(_ptr(x), _dtype_code(x), _ptr(out), _dtype_code(out), x.numel(),
+                                        _ptr(scale), _stream_handle(x.device))
+    _raise(rc, "flce_scale_gradient")
+    return out
+
+
+class _LinearCrossEntropy(torch.autograd.Function):
+    """Autograd node of the fused head. The forward runs the fused
+    forward+backward with grad_scale 1 and keeps grad_h and grad_W, the way the
+    pages' fused linear-cross-entropy functions do (DeepSeek-V3 page, Summary:
+    the fused loss inside the model's forward, logits never kept); the backward
+    only multiplies them by the upstream gradient of the loss."""
+
+    @staticmethod
+    def forward(ctx, h, W, labels, softcap, out_mult, ignore_index, reduction, chunk_rows, low_memory):
+        need_gh, need_gW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        ctx.w_dtype = W.dtype
+        if not (need_gh or need_gW):
+            loss, acc = flce_ce_only(h, W, labels, softcap=softcap, out_mult=out_mult, ignore_index=ignore_index,
+                                     reduction=reduction, chunk_rows=chunk_rows)
+            ctx.save_for_backward(None, None)
+        else:
+            gW = torch.zeros(W.shape, dtype=torch.float32, device=W.device) if need_gW else None
+            out = flce_forward_backward(h, W, labels, grad_W=gW, need_grad_h=need_gh, softcap=softcap,
+                                        out_mult=out_mult, ignore_index=ignore_index, reduction=reduction,
+                                        chunk_rows=chunk_rows, low_memory=low_memory)
+            loss, acc = out["loss"], out["token_accuracy"]
+            ctx.save_for_backward(out["grad_h"], gW)
+        ctx.mark_non_differentiable(acc)
+        return loss, acc
+
+    @staticmethod
+    def backward(ctx, grad_loss, grad_acc):
+        gh, gW = ctx.saved_tensors
+        g = grad_loss.reshape(1)
+        if gh is not None:
+            flce_scale_gradient(gh, g, out=gh)
+        if gW is not None:
+            gW = flce_scale_gradient(gW, g, out=gW if ctx.w_dtype == torch.float32 else None,
+                                     out_dtype=ctx.w_dtype)
+        return gh, gW, None, None, None, None, None, None, None
+
+
+def linear_cross_entropy(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                         chunk_rows=0, low_memory=False):
+    """Differentiable fused head loss: returns (loss, token_accuracy). Gradients
+    flow to h and to W where they require grad; a W that does not (a frozen
+    projection, SpecForge DSpine PR, Changes) costs no grad_W work. W's
+    gradient is accumulated in fp32 inside the call and handed to autograd in
+    W's dtype."""
+    if reduction not in ("mean", "sum"):
+        raise ValueError("reduction must be 'mean' or 'sum' (per-row losses: flce_cross_entropy)")
+    return _LinearCrossEntropy.apply(h, W, labels, float(softcap), float(out_mult), int(ignore_index), reduction,
+                                     int(chunk_rows), bool(low_memory))
+
+
+class FusedLinearCrossEntropyLoss(torch.nn.Module):
+    """Module form of linear_cross_entropy: loss(h, W, labels) -> loss, or
+    (loss, token_accuracy) with return_token_accuracy=True."""
+
+    def __init__(self, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean", chunk_rows=0,
+                 low_memory=False, return_token_accuracy=False):
+        super().__init__()
+        self.kw = dict(softcap=softcap, out_mult=out_mult, ignore_index=ignore_index, reduction=reduction,
+                       chunk_rows=chunk_rows, low_memory=low_memory)
+        self.return_token_accuracy = return_token_accuracy
+
+    def forward(self, h, W, labels):
+        loss, acc = linear_cross_entropy(h, W, labels, **self.kw)
+        return (loss, acc) if self.return_token_accuracy else loss
 
 
 def flce_get_status(device=None) -> int:

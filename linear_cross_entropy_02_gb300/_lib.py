@@ -34,11 +34,11 @@ FLCE_FLAG_TEST_STALL = 2
 FLCE_FLAG_KMAJOR_BWD = 4
 FLCE_FLAG_RECOMPUTE = 8
 
-FLCE_NUM_KERNELS = 14
+FLCE_NUM_KERNELS = 15
 
 EXPORTED = [
     "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
-    "flce_forward_backward", "flce_cross_entropy", "flce_get_status", "flce_status_string", "flce_launch_count",
+    "flce_forward_backward", "flce_cross_entropy", "flce_scale_gradient", "flce_get_status", "flce_status_string", "flce_launch_count",
     "flce_profile_begin", "flce_profile_read", "flce_kernel_name",
 ]
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.flce_cross_entropy.argtypes = [_P, _vp, ctypes.c_int, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _sz, _vp]
         L.flce_cross_entropy.restype = ctypes.c_int
+        L.flce_scale_gradient.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int64, _vp, _vp]
+        L.flce_scale_gradient.restype = ctypes.c_int
         L.flce_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
         L.flce_get_status.restype = ctypes.c_int
         L.flce_status_string.argtypes = [ctypes.c_int]

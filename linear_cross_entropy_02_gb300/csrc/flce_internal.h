@@ -55,6 +55,7 @@ enum KernelId {
   K_CE_GRAD = 11,
   K_RECOMPUTE_GEMM = 12,
   K_CONVERT = 13,
+  K_SCALE = 14,
 };
 
 enum EpiMode {
@@ -94,6 +95,10 @@ struct GemmParams {
   float grad_scale;
   int reduction;
   int col0;
+  // 1: the epilogue's bulk stores / reduce-adds (EPI_STATS_STORE, EPI_F32,
+  // EPI_ACC_F32) carry an L2 evict-first policy; the engine sets it for the
+  // stored logits only (on the fp32 accumulators it measured no faster)
+  int store_hint;
   // control
   int32_t* status;
   uint64_t timeout_ns;
@@ -195,6 +200,11 @@ cudaError_t launch_ce_grad(const CeParams& p, cudaStream_t s);
 
 // out [n] (bf16) = in [n] (fp32), round to nearest even.
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+
+// y [n] = scale * x [n], converted (bf16 results rounded to nearest even);
+// scale is a device float or nullptr for 1. x == y only when the types match.
+cudaError_t launch_scale_convert(const void* x, bool x_f32, void* y, bool y_f32, int64_t n, const float* scale,
+                                 int sms, cudaStream_t s);
 
 cudaError_t launch_finish(const Header* hdr, int reduction, float* loss, float* token_accuracy,
                           cudaStream_t s);

@@ -43,8 +43,10 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
 // writes of a warp over all banks). Two buffers alternate; lane 0 issues the
 // bulk copy and keeps at most one older copy reading shared memory.
 struct EpiStage {
-  uint8_t* base;  // this warp's two buffers
-  int next;       // buffer to fill next
+  uint8_t* base;    // this warp's two buffers
+  int next;         // buffer to fill next
+  uint64_t policy;  // L2 policy of the global writes (when hint)
+  bool hint;
 };
 
 template <bool REDUCE>
@@ -59,10 +61,17 @@ __device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* 
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (REDUCE)
-      tma_reduce_add_2d(map, buf, x, y);
-    else
-      tma_store_2d(map, buf, x, y);
+    if (es.hint) {
+      if (REDUCE)
+        tma_reduce_add_2d_hint(map, buf, x, y, es.policy);
+      else
+        tma_store_2d_hint(map, buf, x, y, es.policy);
+    } else {
+      if (REDUCE)
+        tma_reduce_add_2d(map, buf, x, y);
+      else
+        tma_store_2d(map, buf, x, y);
+    }
     bulk_commit_group();
   }
   es.next ^= 1;
@@ -379,7 +388,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    EpiStage es{sStage + (warp - 2) * 2 * kStageBufBytes, 0};
+    EpiStage es{sStage + (warp - 2) * 2 * kStageBufBytes, 0, 0, p.store_hint != 0};
+    if (es.hint) es.policy = l2_policy_evict_first();
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {

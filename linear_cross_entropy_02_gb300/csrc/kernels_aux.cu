@@ -500,6 +500,86 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaSt
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ scale
+// y = scale * x converted to y's type: a streaming pass, 8 elements per thread
+// and step (two or one 16-byte accesses), grid-stride over a persistent grid.
+__device__ __forceinline__ void load8(const float* p, float v[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const uint16_t* p, float v[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void store8(float* p, const float v[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(uint16_t* p, const float v[8]) {
+  uint4 a;
+  a.x = static_cast<uint32_t>(float_to_bf16_bits(v[0])) | (static_cast<uint32_t>(float_to_bf16_bits(v[1])) << 16);
+  a.y = static_cast<uint32_t>(float_to_bf16_bits(v[2])) | (static_cast<uint32_t>(float_to_bf16_bits(v[3])) << 16);
+  a.z = static_cast<uint32_t>(float_to_bf16_bits(v[4])) | (static_cast<uint32_t>(float_to_bf16_bits(v[5])) << 16);
+  a.w = static_cast<uint32_t>(float_to_bf16_bits(v[6])) | (static_cast<uint32_t>(float_to_bf16_bits(v[7])) << 16);
+  *reinterpret_cast<uint4*>(p) = a;
+}
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const uint16_t* p) { return bf16_bits_to_float(*p); }
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store1(uint16_t* p, float v) { *p = float_to_bf16_bits(v); }
+
+// VEC: both pointers 16-byte aligned, so every 8-element group is one or two
+// aligned vector accesses; otherwise element by element.
+template <typename TI, typename TO, bool VEC>
+__global__ void __launch_bounds__(256) scale_convert_kernel(const TI* x, TO* y, int64_t n, const float* scale) {
+  const float c = scale ? *scale : 1.0f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (VEC) {
+    const int64_t groups = n / 8;
+    const TI* xp = x + tid * 8;
+    TO* yp = y + tid * 8;
+    for (int64_t g = tid; g < groups; g += stride, xp += stride * 8, yp += stride * 8) {
+      float v[8];
+      load8(xp, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] *= c;
+      store8(yp, v);
+    }
+    for (int64_t i = groups * 8 + tid; i < n; i += stride) store1(y + i, c * load1(x + i));
+  } else {
+    for (int64_t i = tid; i < n; i += stride) store1(y + i, c * load1(x + i));
+  }
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_scale_typed(const void* x, void* y, int64_t n, const float* scale, int sms, cudaStream_t s) {
+  const int64_t groups = (n + 7) / 8;
+  const int64_t want = (groups + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < 4LL * sms ? want : 4LL * sms);
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
+  if (vec)
+    scale_convert_kernel<TI, TO, true><<<blocks, 256, 0, s>>>(static_cast<const TI*>(x), static_cast<TO*>(y), n, scale);
+  else
+    scale_convert_kernel<TI, TO, false><<<blocks, 256, 0, s>>>(static_cast<const TI*>(x), static_cast<TO*>(y), n, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_convert(const void* x, bool x_f32, void* y, bool y_f32, int64_t n, const float* scale,
+                                 int sms, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (x_f32 && y_f32) return launch_scale_typed<float, float>(x, y, n, scale, sms, s);
+  if (x_f32) return launch_scale_typed<float, uint16_t>(x, y, n, scale, sms, s);
+  if (y_f32) return launch_scale_typed<uint16_t, float>(x, y, n, scale, sms, s);
+  return launch_scale_typed<uint16_t, uint16_t>(x, y, n, scale, sms, s);
+}
+
 // ------------------------------------------------------------------ finish
 __global__ void finish_kernel(const Header* hdr, int reduction, float* loss, float* token_accuracy) {
   const int64_t nv = hdr->n_valid;

@@ -125,9 +125,30 @@ def test_status_strings(L):
 
 
 def test_kernel_names(L):
-    names = [L.flce_kernel_name(i).decode() for i in range(12)]
+    from linear_cross_entropy_02_gb300 import _lib as B
+    names = [L.flce_kernel_name(i).decode() for i in range(B.FLCE_NUM_KERNELS)]
     assert names[1] == "fwd_gemm_stats" and names[4] == "grad_h_gemm" and names[5] == "grad_W_gemm"
+    assert names[-1] == "scale_gradient" and len(set(names)) == len(names) and "unknown" not in names
+    assert L.flce_kernel_name(B.FLCE_NUM_KERNELS) == b"unknown"
     assert L.flce_kernel_name(99) == b"unknown"
+
+
+def test_scale_gradient_host_errors(L):
+    """Argument errors come back before any device call (the pointers are never
+    dereferenced), and n = 0 is a no-op."""
+    from linear_cross_entropy_02_gb300 import _lib as B
+    bf, f32 = B.FLCE_DTYPE_BF16, B.FLCE_DTYPE_F32
+    x = ctypes.c_void_p(1 << 20)
+    assert L.flce_scale_gradient(x, bf, ctypes.c_void_p(1 << 21), bf, -1, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(x, 7, ctypes.c_void_p(1 << 21), bf, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(x, bf, ctypes.c_void_p(1 << 21), -1, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(None, bf, ctypes.c_void_p(1 << 21), bf, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(x, f32, None, f32, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(None, bf, None, bf, 0, None, None) == B.FLCE_OK
+    # partial overlaps, and an exact alias that changes the element size
+    assert L.flce_scale_gradient(x, f32, ctypes.c_void_p((1 << 20) + 16), f32, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(ctypes.c_void_p((1 << 20) + 30), bf, x, bf, 16, None, None) == B.FLCE_ERR_ARG
+    assert L.flce_scale_gradient(x, f32, x, bf, 16, None, None) == B.FLCE_ERR_ARG
 
 
 def test_binding_rejects_cpu_tensors():
