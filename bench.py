@@ -243,7 +243,8 @@ def run_ours(args, w):
     W = W_cpu.to(dev)
     lab = lab_cpu.to(dev)
     gW = torch.zeros(W.shape, dtype=torch.float32, device=dev) if w.mode == "fwd_bwd" else None
-    kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+    kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows,
+              flags=flce.FLCE_FLAG_TILE128 if args.tile128 else 0)
     bkw = dict(low_memory=args.low_memory, vocab_slab=args.vocab_slab)
 
     def step():
@@ -361,6 +362,8 @@ def run_ours(args, w):
             "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if args.low_memory and w.mode == "fwd_bwd"
                                                        else 1.0),
             "backward": "recompute (low memory)" if args.low_memory else "stored logits",
+            "gemm_cta_tile": ("128x256, two accumulators" if (args.tile128 or args.fp32)
+                              else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"),
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h.numel() * h.element_size() + lab.numel() * 8, "d2h_bytes_per_step": 8},
@@ -491,6 +494,8 @@ def main():
                     help="recompute backward: no stored logits, dlogits per vocab slab")
     ap.add_argument("--vocab-slab", type=int, default=0)
     ap.add_argument("--fp32", action="store_true", help="fp32 h and W: the tf32 tensor-core path")
+    ap.add_argument("--tile128", action="store_true",
+                    help="128-row GEMM tiles with two accumulators (FLCE_FLAG_TILE128), for comparison")
     ap.add_argument("--ce-logits", action="store_true",
                     help="time the cross-entropy on materialised bf16 logits [N, V] instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")

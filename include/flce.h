@@ -95,6 +95,13 @@ extern "C" {
                                         cores and form bf16 dlogits in the GEMM epilogue's
                                         registers, then run both backward GEMMs on the slab.
                                         Transient O(C * vocab_slab + C * H); 8NHV flops, not 6NHV */
+#define FLCE_FLAG_TILE128 16         /* every bf16 tensor-core GEMM on 128 x 256 CTA tiles
+                                        with two TMEM accumulators. By default each GEMM takes
+                                        256 x 256 tiles (two M = 128 MMAs per K step sharing one
+                                        B slice) unless its tile count is too small for them to
+                                        fill the SMs evenly */
+#define FLCE_FLAG_TILE256 32         /* cross-check: 256 x 256 CTA tiles for every bf16 GEMM
+                                        that has them, whatever the tile count */
 
 typedef struct flce_params {
   int64_t n_rows;        /* N >= 0 */

@@ -33,6 +33,8 @@ FLCE_FLAG_SIMT_GEMM = 1
 FLCE_FLAG_TEST_STALL = 2
 FLCE_FLAG_KMAJOR_BWD = 4
 FLCE_FLAG_RECOMPUTE = 8
+FLCE_FLAG_TILE128 = 16
+FLCE_FLAG_TILE256 = 32
 
 FLCE_NUM_KERNELS = 15
 

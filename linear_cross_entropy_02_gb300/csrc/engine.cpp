@@ -310,6 +310,20 @@ int run(const flce_params* params, const Call& c) {
   const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool recompute = L.slab > 0;
   const bool kmajor = !recompute && (simt || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
+  // 256-row CTA tiles carry a third less operand traffic into each SM per
+  // flop than 128-row tiles, which the tensor cores otherwise wait on: a
+  // 256-row tile costs about 1.82 128-row tiles (measured on the DSV3 head).
+  // With few tiles the coarser grid can lose more to the last partial wave
+  // than that saves, so each GEMM takes the shape with the shorter estimated
+  // makespan, unless a flag fixes it.
+  auto wide_for = [&](const GemmParams& g) {
+    if (p.flags & FLCE_FLAG_TILE128) return false;
+    if (p.flags & FLCE_FLAG_TILE256) return true;
+    const int64_t narrow = (static_cast<int64_t>(g.m_tiles) * g.n_tiles + sms - 1) / sms;
+    const int64_t units = static_cast<int64_t>((g.m_tiles + 1) / 2) * g.n_tiles;
+    const int64_t wide_waves = (units + sms - 1) / sms;
+    return 182 * wide_waves < 100 * narrow;
+  };
   if (cc != 103) return FLCE_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
   if (!simt && !load_encoder()) return FLCE_ERR_UNSUPPORTED;
 
@@ -391,7 +405,7 @@ int run(const flce_params* params, const Call& c) {
       const int tiles = g.m_tiles * g.n_tiles;
       CUtensorMap map_z;
       if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, &map_h, &map_w,
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, wide_for(g), &map_h, &map_w,
                                              store ? &map_z : nullptr, g, std::min(tiles, sms), stream));
     }
 
@@ -451,7 +465,7 @@ int run(const flce_params* params, const Call& c) {
         r.col0 = v0;
         r.status = &hdr->status;
         r.timeout_ns = timeout;
-        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, &map_h, &map_w, nullptr, r,
+        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), &map_h, &map_w, nullptr, r,
                                                      std::min(r.m_tiles * r.n_tiles, sms), stream));
         if (gh) {
           // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
@@ -478,7 +492,7 @@ int run(const flce_params* params, const Call& c) {
           b.timeout_ns = timeout;
           CUtensorMap map_o;
           if (!encode_f32_out(&map_o, gh32, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-          FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, &map_a, &map_b, &map_o, b,
+          FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
         }
         if (gw) {
@@ -505,7 +519,7 @@ int run(const flce_params* params, const Call& c) {
           b.timeout_ns = timeout;
           CUtensorMap map_o;
           if (!encode_f32_out(&map_o, c.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
-          FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, &map_a, &map_b, &map_o, b,
+          FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
         }
       }
@@ -564,7 +578,7 @@ int run(const flce_params* params, const Call& c) {
         } else if (!encode_bf16(&map_wb, c.W, H, V, n.ld_w, 64)) {  // W [V][H]: MN-major B
           return FLCE_ERR_UNSUPPORTED;
         }
-        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, false, !kmajor, &map_dz, &map_wb, nullptr, b,
+        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, false, !kmajor, wide_for(b), &map_dz, &map_wb, nullptr, b,
                                                  std::min(b.m_tiles * b.n_tiles, sms), stream));
       }
     }
@@ -609,7 +623,7 @@ int run(const flce_params* params, const Call& c) {
         }
         CUtensorMap map_o;
         if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, !kmajor, !kmajor, &map_a, &map_b, &map_o, b,
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, !kmajor, !kmajor, wide_for(b), &map_a, &map_b, &map_o, b,
                                                  std::min(b.m_tiles * b.n_tiles, sms), stream));
       }
     }

@@ -17,6 +17,9 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: epilogue
+// Threads of the tensor-core GEMM: 128-row tiles (tmh = 1) have four epilogue
+// warps, 256-row tiles (tmh = 2) eight.
+constexpr int gemm_threads(int tmh) { return tmh == 2 ? 320 : kGemmThreads; }
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kBN * kBK * 2;
 // Per epilogue warp: two 4 KB staging buffers for a 32 x 32 fp32 sub-tile that a
@@ -111,7 +114,11 @@ struct GemmParams {
 // c: fp32 output tensor map with 32 x 32 boxes and 128-byte swizzle, used by
 // EPI_STATS_STORE (the stored logits, bulk store) and EPI_ACC_F32 (bulk
 // reduce-add into the fp32 accumulator); ignored by the other modes.
-cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
+// wide: 256 x 256 CTA tiles (two M = 128 MMAs per K step sharing the B slice,
+// one 512-column accumulator) instead of 128 x 256 tiles with two accumulators;
+// the all-K-major backward combinations always use 128-row tiles. grid is the
+// largest number of CTAs to launch (at most one per tile).
+cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUtensorMap* a, const CUtensorMap* b,
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
 // The same GEMM on fp32 operands (tcgen05 kind::tf32), both K-major; modes
 // EPI_STATS, EPI_STATS_STORE, EPI_F32, EPI_ACC_F32.

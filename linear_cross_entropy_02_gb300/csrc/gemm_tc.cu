@@ -27,24 +27,28 @@ namespace flce {
 // Grouped rasterisation: tiles walk group_m row-tiles at a time, row-tile
 // fastest, so the CTAs resident at once share a few B slices and a few A
 // slices in L2.
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
-  const int per_group = p.group_m * p.n_tiles;
+// Tile t of the walk: groups of `group` M-units, M fastest within a group. An
+// M-unit is TMH consecutive 128-row tiles (one CTA tile of TMH * 128 rows).
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int units_m, int group, int t, int& mu, int& nb) {
+  const int per_group = group * p.n_tiles;
   const int g = t / per_group;
-  const int first_m = g * p.group_m;
-  const int gsize = min(p.m_tiles - first_m, p.group_m);
+  const int first_m = g * group;
+  const int gsize = min(units_m - first_m, group);
   const int local = t - g * per_group;
-  mb = first_m + local % gsize;
+  mu = first_m + local % gsize;
   nb = local / gsize;
 }
 
 // Staging of one epilogue warp's 32 x 32 fp32 sub-tile for a TMA bulk store or
 // reduce-add: lane r writes its row as eight 16-byte chunks, chunk q at slot
 // q ^ (r & 7) (the 128-byte swizzle the tensor map expects; also spreads the
-// writes of a warp over all banks). Two buffers alternate; lane 0 issues the
-// bulk copy and keeps at most one older copy reading shared memory.
+// writes of a warp over all banks). With two buffers they alternate and lane 0
+// keeps at most one older copy reading shared memory; with one, lane 0 waits
+// for the previous copy's reads before the buffer is rewritten.
 struct EpiStage {
-  uint8_t* base;    // this warp's two buffers
+  uint8_t* base;    // this warp's buffers
   int next;         // buffer to fill next
+  int nbuf;         // 1 or 2
   uint64_t policy;  // L2 policy of the global writes (when hint)
   bool hint;
 };
@@ -53,7 +57,12 @@ template <bool REDUCE>
 __device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* map, int lane, const float (&v)[32],
                                                int32_t x, int32_t y) {
   uint8_t* buf = es.base + es.next * kStageBufBytes;
-  if (lane == 0) bulk_wait_group_read<1>();  // the copy that used `buf` two sends ago has read it
+  if (lane == 0) {  // the copy that last used `buf` has read it
+    if (es.nbuf == 2)
+      bulk_wait_group_read<1>();
+    else
+      bulk_wait_group_read<0>();
+  }
   __syncwarp();
   float4* row = reinterpret_cast<float4*>(buf + lane * 128);
 #pragma unroll
@@ -74,7 +83,7 @@ __device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* 
     }
     bulk_commit_group();
   }
-  es.next ^= 1;
+  if (es.nbuf == 2) es.next ^= 1;
 }
 
 template <bool STORE>
@@ -216,19 +225,32 @@ __device__ __forceinline__ void epilogue_dz(const GemmParams& p, uint32_t tcol, 
 
 // TF32: operands are fp32 (read by the tensor cores as tf32); a K slice is then
 // 32 elements, still one 128-byte swizzle row, and one MMA covers K = 8.
-template <int MODE, bool A_MN, bool B_MN, bool TF32>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// TMH = 1: 128 x 256 CTA tiles, a 4-stage ring and two 256-column TMEM
+// accumulators (the epilogue of one tile overlaps the MMAs of the next).
+// TMH = 2: 256 x 256 CTA tiles as two M = 128 MMAs sharing each B slice, a
+// 3-stage ring of the same size and one 512-column accumulator: a third less
+// operand traffic into the SM per flop. The accumulator is drained by eight
+// epilogue warps, two per TMEM lane quarter (warps 2-5 rows 0-127, warps 6-9
+// rows 128-255, one staging buffer each), so the tensor cores wait for half
+// as long between tiles as four warps would make them.
+template <int MODE, bool A_MN, bool B_MN, bool TF32, int TMH>
+__global__ void __launch_bounds__(gemm_threads(TMH), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                    const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
+  constexpr int S = TMH == 2 ? 3 : kStages;
+  constexpr int ABytes = kAStageBytes * TMH;
+  constexpr int NBUF = TMH == 2 ? 1 : 2;
+  static_assert(S * (ABytes + kBStageBytes) <= kStages * (kAStageBytes + kBStageBytes), "ring exceeds the budget");
+  static_assert(TMH == 1 || !TF32, "256-row tiles are bf16 only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kAStageBytes;
-  uint8_t* sStage = sB + kStages * kBStageBytes;  // epilogue staging, 4 warps x 2 buffers
+  uint8_t* sB = smem + S * ABytes;
+  uint8_t* sStage = smem + kStages * (kAStageBytes + kBStageBytes);  // epilogue staging, 4 warps x 2 buffers
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kEpiStagingBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -240,13 +262,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], TMH == 2 ? 256 : 128);  // every epilogue thread arrives
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -267,7 +289,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const int total = p.m_tiles * p.n_tiles;
+  const int units_m = (p.m_tiles + TMH - 1) / TMH;
+  const int group = p.group_m / TMH > 0 ? p.group_m / TMH : 1;
+  const int total = units_m * p.n_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -278,23 +302,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool aborted = false;
       if (!(p.debug_flags & FLCE_FLAG_TEST_STALL)) {
         for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
-          int mb, nb;
-          tile_coords(p, t, mb, nb);
+          int mu, nb;
+          tile_coords(p, units_m, group, t, mu, nb);
+          const int row0 = p.a_row0 + mu * kBM * TMH;
           for (int k = 0; k < p.k_iters; ++k) {
             if (!wait_bounded(&empty[stage], phase ^ 1u, wc)) {
               aborted = true;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], kAStageBytes + kBStageBytes);
-            // K-major operand: one box of 64 K x rows. MN-major operand: boxes of
-            // 64 MN x 64 K, one per 64 rows of the tile, 8 KB apart.
+            mbar_arrive_expect_tx(&full[stage], ABytes + kBStageBytes);
+            // K-major operand: boxes of 64 K x 128 (A) or 256 (B) rows.
+            // MN-major operand: boxes of 64 MN x 64 K, one per 64 rows of the
+            // tile, 8 KB apart.
             if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < kBM / 64; ++j)
-                tma_load_2d(sA + stage * kAStageBytes + j * 8192, &tma_a, &full[stage], p.a_row0 + mb * kBM + j * 64,
-                            k * kSliceK);
+              for (int j = 0; j < kBM * TMH / 64; ++j)
+                tma_load_2d(sA + stage * ABytes + j * 8192, &tma_a, &full[stage], row0 + j * 64, k * kSliceK);
             } else {
-              tma_load_2d(sA + stage * kAStageBytes, &tma_a, &full[stage], k * kSliceK, p.a_row0 + mb * kBM);
+#pragma unroll
+              for (int hh = 0; hh < TMH; ++hh)
+                tma_load_2d(sA + stage * ABytes + hh * kAStageBytes, &tma_a, &full[stage], k * kSliceK,
+                            row0 + hh * kBM);
             }
             if (B_MN) {
 #pragma unroll
@@ -305,7 +333,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kSliceK, p.b_row0 + nb * kBN);
             }
             ++issued;
-            if (++stage == kStages) {
+            if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
@@ -313,14 +341,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (aborted) {
-        // The most recent min(issued, kStages) loads may still be in flight:
+        // The most recent min(issued, S) loads may still be in flight:
         // wait for each to land before this CTA's shared memory goes away.
-        const int n = issued < kStages ? issued : kStages;
+        const int n = issued < S ? issued : S;
         int s = stage;
         uint32_t ph = phase;
         for (int i = 0; i < n; ++i) {
           if (s == 0) {
-            s = kStages - 1;
+            s = S - 1;
             ph ^= 1u;
           } else {
             --s;
@@ -350,29 +378,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = a_base + stage * kAStageBytes;
+          const uint32_t a0 = a_base + stage * ABytes;
           const uint32_t b0 = b_base + stage * kBStageBytes;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // One MMA per 32 B of K (16 bf16 or 8 tf32 elements): 32 B along a
             // K-major row, or two 8-row K groups (2048 B) of an MN-major tile.
-            const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(a0 + kk * 2048) : sdesc_kmajor_sw128(a0 + kk * 32);
+            // With TMH = 2 the second M half of A starts 16 KB further on (128
+            // K-major rows, or two 64-wide MN blocks) and accumulates into
+            // TMEM columns 256-511.
             const uint64_t bd = B_MN ? sdesc_mnmajor_sw128(b0 + kk * 2048) : sdesc_kmajor_sw128(b0 + kk * 32);
-            if (TF32)
-              tc_mma_tf32(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
-            else
-              tc_mma_bf16(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int hh = 0; hh < TMH; ++hh) {
+              const uint32_t ah = a0 + hh * kAStageBytes;
+              const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(ah + kk * 2048) : sdesc_kmajor_sw128(ah + kk * 32);
+              if (TF32)
+                tc_mma_tf32(d_tmem + hh * kBN, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+              else
+                tc_mma_bf16(d_tmem + hh * kBN, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (aborted) break;
         tc_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (NBUF == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
       }
       // All issued tensor-core work must finish before TMEM is released.
       tc_commit(mma_done);
@@ -388,35 +427,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    EpiStage es{sStage + (warp - 2) * 2 * kStageBufBytes, 0, 0, p.store_hint != 0};
+    // TMH = 1: four warps, two 4 KB buffers each, all of the tile's rows.
+    // TMH = 2: eight warps, one buffer each; warp 2 + 4 * half + q drains the
+    // 128-row half `half` of the 256-row tile.
+    const int half = TMH == 2 ? (warp - 2) / 4 : 0;
+    EpiStage es{sStage + (warp - 2) * (TMH == 2 ? 1 : 2) * kStageBufBytes, 0, TMH == 2 ? 1 : 2, 0,
+                p.store_hint != 0};
     if (es.hint) es.policy = l2_policy_evict_first();
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+      int mu, nb;
+      tile_coords(p, units_m, group, t, mu, nb);
       bool ok = wait_bounded(&tfull[acc], acc_phase, wc);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t tcol = t_lane + static_cast<uint32_t>(acc * kBN);
-      if (MODE == EPI_STATS) {
-        epilogue_stats<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
-      } else if (MODE == EPI_STATS_STORE) {
-        epilogue_stats<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
-      } else if (MODE == EPI_BF16) {
-        epilogue_bf16(p, tcol, mb, nb, row);
-      } else if (MODE == EPI_ACC_F32) {
-        epilogue_out_f32<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
-      } else if (MODE == EPI_F32) {
-        epilogue_out_f32<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
-      } else {
-        epilogue_dz(p, tcol, mb, nb, row, coef);
+#pragma unroll 1
+      for (int hh = half; hh < half + 1; ++hh) {
+        // 128-row tile mb of the output, held in TMEM columns tcol..tcol+255
+        const int mb = mu * TMH + hh;
+        if (mb >= p.m_tiles) break;
+        const uint32_t tcol = t_lane + static_cast<uint32_t>((acc + hh) * kBN);
+        if (MODE == EPI_STATS) {
+          epilogue_stats<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_STATS_STORE) {
+          epilogue_stats<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_BF16) {
+          epilogue_bf16(p, tcol, mb, nb, row);
+        } else if (MODE == EPI_ACC_F32) {
+          epilogue_out_f32<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_F32) {
+          epilogue_out_f32<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else {
+          epilogue_dz(p, tcol, mb, nb, row, coef);
+        }
       }
       tc_fence_before_sync();
       mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (NBUF == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
+      }
     }
     // Outstanding bulk stores / reduce-adds must finish before the CTA exits.
     if ((MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32 || MODE == EPI_F32) && lane == 0) bulk_wait_group<0>();
@@ -430,7 +484,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN, bool TF32 = false>
+template <int MODE, bool A_MN, bool B_MN, bool TF32 = false, int TMH = 1>
 static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                                const GemmParams& p, int grid, cudaStream_t s) {
   // The shared-memory opt-in is a per-device function attribute: set it on the
@@ -441,22 +495,42 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kGemmSmemBytes);
+    e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  gemm_tc_kernel<MODE, A_MN, B_MN, TF32><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
+  const int units = ((p.m_tiles + TMH - 1) / TMH) * p.n_tiles;
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
+  gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH><<<grid, gemm_threads(TMH), kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a,
+                                                                                           p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, const CUtensorMap* a, const CUtensorMap* b,
+cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUtensorMap* a, const CUtensorMap* b,
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
   if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
     return cudaErrorInvalidValue;
   // The combinations the engine uses: the forward GEMM (both K-major), grad_h
   // (dz K-major, W MN-major or its transpose K-major), grad_W (dz and h_c
   // MN-major, or their transposes K-major).
+  // wide: 256-row CTA tiles (TMH = 2) for every combination above except the
+  // all-K-major backward cross-checks, which keep 128-row tiles.
+  if (wide) {
+    if (!a_mn && !b_mn) {
+      switch (mode) {
+        case EPI_STATS: return launch_mode<EPI_STATS, false, false, false, 2>(a, b, c, p, grid, s);
+        case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false, false, 2>(a, b, c, p, grid, s);
+        case EPI_DZ: return launch_mode<EPI_DZ, false, false, false, 2>(a, b, c, p, grid, s);
+        default: break;
+      }
+    }
+    if (!a_mn && b_mn && mode == EPI_BF16) return launch_mode<EPI_BF16, false, true, false, 2>(a, b, c, p, grid, s);
+    if (!a_mn && b_mn && mode == EPI_ACC_F32)
+      return launch_mode<EPI_ACC_F32, false, true, false, 2>(a, b, c, p, grid, s);
+    if (a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode<EPI_ACC_F32, true, true, false, 2>(a, b, c, p, grid, s);
+  }
   if (!a_mn && !b_mn) {
     switch (mode) {
       case EPI_STATS: return launch_mode<EPI_STATS, false, false>(a, b, c, p, grid, s);

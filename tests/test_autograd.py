@@ -136,6 +136,27 @@ def test_autograd_frozen_weight_and_module(flce):
     assert float(l2) == float(loss)
 
 
+def test_autograd_on_256_row_tiles(flce):
+    """The same autograd gradients through the 256-row GEMM tiles (forced: at
+    this size each GEMM would otherwise pick 128-row tiles)."""
+    N, H, V = 300, 192, 1000
+    h, W, y = _inputs(N, H, V, seed=21)
+    hd = h.to(DEV).requires_grad_(True)
+    Wd = W.to(DEV).requires_grad_(True)
+    loss, acc = flce.linear_cross_entropy(hd, Wd, y.to(DEV), softcap=30.0, out_mult=0.5, chunk_rows=128)
+    loss.backward()
+    ref_loss, ref_acc = float(loss), float(acc)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=torch.zeros(V, H, device=DEV),
+                                     softcap=30.0, out_mult=0.5, chunk_rows=128, flags=flce.FLCE_FLAG_TILE256)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = flce_oracle(h, W, y, softcap=30.0, out_mult=0.5)
+    check_against_oracle(out, ref, y, what="tile256")
+    check_against_oracle({"loss": loss.detach(), "token_accuracy": acc, "grad_h": hd.grad}, ref, y,
+                         what="autograd default tiles")
+    assert abs(float(out["loss"]) - ref_loss) <= 1e-6 * abs(ref_loss) and float(out["token_accuracy"]) == ref_acc
+
+
 def test_autograd_rejects_per_row_reduction(flce):
     h, W, y = _inputs(16, 64, 100, seed=3)
     with pytest.raises(ValueError):

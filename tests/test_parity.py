@@ -103,12 +103,16 @@ def run_fwd_bwd(flce, h, W, y, *, softcap=0.0, out_mult=1.0, grad_W0=None, reduc
     return out
 
 
-# 0: tcgen05 GEMMs, backward operands read in place as MN-major tiles (the product path)
+# 0: tcgen05 GEMMs on 256 x 256 CTA tiles, backward operands read in place as
+#    MN-major tiles (the product path)
 # 1: debug fp32-FMA GEMMs (FLCE_FLAG_SIMT_GEMM)
 # 4: tcgen05 GEMMs fed explicit transposes, all operands K-major (FLCE_FLAG_KMAJOR_BWD)
 # 8: low-memory recompute backward (FLCE_FLAG_RECOMPUTE), vocab slabs of 512 columns so
 #    the shapes below span several slabs and a ragged last slab
-PATHS = [0, 1, 4, 8]
+# 16: 128 x 256 CTA tiles with two accumulators everywhere (FLCE_FLAG_TILE128)
+# 32: 256 x 256 CTA tiles everywhere (FLCE_FLAG_TILE256; by default small GEMMs
+#     such as these take 128-row tiles); 24 and 40: each with the recompute backward
+PATHS = [0, 1, 4, 8, 16, 24, 32, 40]
 
 
 @pytest.mark.parametrize("flags", PATHS)
@@ -181,7 +185,7 @@ def test_planted_accuracy(flce):
     check_against_oracle(out, ref, y2, what="planted")
 
 
-@pytest.mark.parametrize("flags", [0, 8])
+@pytest.mark.parametrize("flags", [0, 8, 16, 32])
 def test_frozen_weight_and_no_grad_h(flce, flags):
     N, H, V = 256, 128, 2000
     h, W, y = _inputs(N, H, V, seed=6)
@@ -293,7 +297,7 @@ def test_zipf_labels_and_row_sums(flce):
     assert torch.all(col <= bound)
 
 
-@pytest.mark.parametrize("flags", [0, 8])
+@pytest.mark.parametrize("flags", [0, 8, 16, 32])
 @pytest.mark.parametrize("case", [
     dict(N=5, H=64, V=100),                                   # one partial row tile, V < one vocab tile
     dict(N=130, H=128, V=257, ignore_index=-1),               # custom ignore index, one column past a tile
@@ -307,7 +311,7 @@ def test_small_and_unusual_heads(flce, flags, case):
     y = torch.where(y == -100, torch.full_like(y, ign), y)
     gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
     out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, ignore_index=ign,
-                                     return_predicted=True, flags=flags, vocab_slab=256 if flags else 0, **c)
+                                     return_predicted=True, flags=flags, vocab_slab=256 if flags & 8 else 0, **c)
     torch.cuda.synchronize()
     assert flce.flce_get_status() == 0
     ref = flce_oracle(h, W, y, ignore_index=ign, softcap=c.get("softcap", 0.0), out_mult=c.get("out_mult", 1.0))
