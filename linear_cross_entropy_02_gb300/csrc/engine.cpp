@@ -264,6 +264,21 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
 
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// 256-row CTA tiles carry a third less operand traffic into each SM per flop
+// than 128-row tiles, which the tensor cores otherwise wait on: a 256-row tile
+// costs about 1.82 128-row tiles (measured on the DSV3 head). With few tiles
+// the coarser grid can lose more to the last partial wave than that saves, so
+// each GEMM takes the shape with the shorter makespan of the persistent grid,
+// unless a flag fixes it.
+bool pick_wide(int flags, const GemmParams& g, int sms) {
+  if (flags & FLCE_FLAG_TILE128) return false;
+  if (flags & FLCE_FLAG_TILE256) return true;
+  const int64_t narrow = (static_cast<int64_t>(g.m_tiles) * g.n_tiles + sms - 1) / sms;
+  const int64_t units = static_cast<int64_t>((g.m_tiles + 1) / 2) * g.n_tiles;
+  const int64_t wide_waves = (units + sms - 1) / sms;
+  return 182 * wide_waves < 100 * narrow;
+}
+
 #define FLCE_LAUNCH(kid, expr)                         \
   do {                                                 \
     LaunchScope _scope((kid), stream);                 \
@@ -310,20 +325,7 @@ int run(const flce_params* params, const Call& c) {
   const bool simt = (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool recompute = L.slab > 0;
   const bool kmajor = !recompute && (simt || (p.flags & FLCE_FLAG_KMAJOR_BWD) != 0);
-  // 256-row CTA tiles carry a third less operand traffic into each SM per
-  // flop than 128-row tiles, which the tensor cores otherwise wait on: a
-  // 256-row tile costs about 1.82 128-row tiles (measured on the DSV3 head).
-  // With few tiles the coarser grid can lose more to the last partial wave
-  // than that saves, so each GEMM takes the shape with the shorter estimated
-  // makespan, unless a flag fixes it.
-  auto wide_for = [&](const GemmParams& g) {
-    if (p.flags & FLCE_FLAG_TILE128) return false;
-    if (p.flags & FLCE_FLAG_TILE256) return true;
-    const int64_t narrow = (static_cast<int64_t>(g.m_tiles) * g.n_tiles + sms - 1) / sms;
-    const int64_t units = static_cast<int64_t>((g.m_tiles + 1) / 2) * g.n_tiles;
-    const int64_t wide_waves = (units + sms - 1) / sms;
-    return 182 * wide_waves < 100 * narrow;
-  };
+  auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, sms); };
   if (cc != 103) return FLCE_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
   if (!simt && !load_encoder()) return FLCE_ERR_UNSUPPORTED;
 
@@ -718,7 +720,7 @@ int run_f32(const Norm& n, const Call& c) {
     g.store_hint = store ? 1 : 0;
     CUtensorMap map_z;
     if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, &map_h, &map_w,
+    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, pick_wide(p.flags, g, sms), &map_h, &map_w,
                                                 store ? &map_z : nullptr, g,
                                                 std::min(g.m_tiles * g.n_tiles, sms), stream));
     MergeParams mp{};
@@ -777,7 +779,7 @@ int run_f32(const Norm& n, const Call& c) {
       CUtensorMap map_a, map_o;
       if (!encode_f32_in(&map_a, dz, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_out(&map_o, static_cast<float*>(c.grad_h) + r0 * H, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc_tf32(EPI_F32, &map_a, &map_wt, &map_o, b,
+      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc_tf32(EPI_F32, pick_wide(p.flags, b, sms), &map_a, &map_wt, &map_o, b,
                                                     std::min(b.m_tiles * b.n_tiles, sms), stream));
     }
     if (gw) {  // grad_W += m dz^T h_c: A = dz^T [V][C], B = h_c^T [H][C]
@@ -800,7 +802,7 @@ int run_f32(const Norm& n, const Call& c) {
       if (!encode_f32_in(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_in(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc_tf32(EPI_ACC_F32, &map_a, &map_b, &map_o, b,
+      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc_tf32(EPI_ACC_F32, pick_wide(p.flags, b, sms), &map_a, &map_b, &map_o, b,
                                                     std::min(b.m_tiles * b.n_tiles, sms), stream));
     }
   }

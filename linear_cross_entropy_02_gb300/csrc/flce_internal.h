@@ -122,8 +122,8 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
 // The same GEMM on fp32 operands (tcgen05 kind::tf32), both K-major; modes
 // EPI_STATS, EPI_STATS_STORE, EPI_F32, EPI_ACC_F32.
-cudaError_t launch_gemm_tc_tf32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
-                                const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm_tc_tf32(int mode, bool wide, const CUtensorMap* a, const CUtensorMap* b,
+                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
 // Debug GEMM on the fp32 FMA pipes; writes alpha*acc to zbuf for the statistics
 // modes (then run launch_stats_from_z) and behaves like the tensor-core GEMM
 // for the plain modes.

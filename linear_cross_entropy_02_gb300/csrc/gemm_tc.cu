@@ -241,7 +241,6 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
   constexpr int ABytes = kAStageBytes * TMH;
   constexpr int NBUF = TMH == 2 ? 1 : 2;
   static_assert(S * (ABytes + kBStageBytes) <= kStages * (kAStageBytes + kBStageBytes), "ring exceeds the budget");
-  static_assert(TMH == 1 || !TF32, "256-row tiles are bf16 only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -547,10 +546,19 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm_tc_tf32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
-                                const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm_tc_tf32(int mode, bool wide, const CUtensorMap* a, const CUtensorMap* b,
+                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
   if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
     return cudaErrorInvalidValue;
+  if (wide) {
+    switch (mode) {
+      case EPI_STATS: return launch_mode<EPI_STATS, false, false, true, 2>(a, b, c, p, grid, s);
+      case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false, true, 2>(a, b, c, p, grid, s);
+      case EPI_F32: return launch_mode<EPI_F32, false, false, true, 2>(a, b, c, p, grid, s);
+      case EPI_ACC_F32: return launch_mode<EPI_ACC_F32, false, false, true, 2>(a, b, c, p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (mode) {
     case EPI_STATS: return launch_mode<EPI_STATS, false, false, true>(a, b, c, p, grid, s);
     case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false, true>(a, b, c, p, grid, s);

@@ -31,6 +31,8 @@ def _inputs_f32(N, H, V, seed, ign=0.1, w_std=0.05):
     return h, W, y
 
 
+# 0: per-GEMM tile choice (128-row tiles at these sizes); 32: 256-row tiles forced
+@pytest.mark.parametrize("flags", [0, 32])
 @pytest.mark.parametrize("case", [
     dict(N=256, H=512, V=4096),
     dict(N=300, H=192, V=1000, chunk_rows=128),
@@ -38,20 +40,21 @@ def _inputs_f32(N, H, V, seed, ign=0.1, w_std=0.05):
     dict(N=513, H=136, V=777, chunk_rows=256, softcap=30.0, out_mult=0.5),
     dict(N=256, H=256, V=2048, softcap=2.0, out_mult=0.5, reduction="sum", grad_scale=0.75),
 ])
-def test_fp32_parity(flce, case):
+def test_fp32_parity(flce, case, flags):
     c = dict(case)
     N, H, V = c.pop("N"), c.pop("H"), c.pop("V")
     h, W, y = _inputs_f32(N, H, V, seed=N + H + V)
     G0 = (np.random.default_rng(2).standard_normal((V, H)) * 1e-3).astype(np.float32).astype(np.float64)
     gW = torch.from_numpy(G0).float().to(DEV)
-    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True, **c)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True,
+                                     flags=flags, **c)
     torch.cuda.synchronize()
     assert flce.flce_get_status() == 0
     assert out["grad_h"].dtype == torch.float32
     ref = flce_oracle(h, W, y, grad_W0=G0, softcap=c.get("softcap", 0.0), out_mult=c.get("out_mult", 1.0),
                       reduction=c.get("reduction", "mean"), grad_scale=c.get("grad_scale", 1.0))
-    rep = check_against_oracle(out, ref, y, grad_W0=G0, what=f"fp32 {case}")
-    print(case, rep)
+    rep = check_against_oracle(out, ref, y, grad_W0=G0, what=f"fp32 {case} flags={flags}")
+    print(case, flags, rep)
 
 
 def test_fp32_forward_and_ce_only(flce):
