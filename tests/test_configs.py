@@ -126,3 +126,32 @@ def test_grad_W_sampled_vocab_rows_full_head(flce, name):
     ref = oracle_grad_W_rows(h, W, y, ids, full["lse"], full["n_valid"], **kw)
     got = gW[torch.from_numpy(ids).to(DEV)].double().cpu().numpy()
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+def test_largest_chunk_matches_default_chunking(flce):
+    """The largest chunk (32768 rows) on the DSV3 head: its logits buffer holds
+    32768 x 129280 = 4.2e9 elements, past 32-bit indexing, and one chunk replaces
+    four. Per-row results do not depend on the chunking, so lse, the predicted
+    tokens and grad_h must equal the default (8192-row) run's bit for bit; the
+    loss differs only by the grouping of its fp64 chunk sums, and grad_W by the
+    order of its fp32 chunk additions."""
+    w = workloads.WORKLOADS["dsv3"]
+    h, W, y = workloads.make_inputs(w)
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    runs = []
+    for chunk in (0, 32768):
+        gW = torch.zeros(W.shape, dtype=torch.float32, device=DEV)
+        o = flce.flce_forward_backward(hd, Wd, yd, grad_W=gW, return_predicted=True, chunk_rows=chunk)
+        f = flce.flce_forward(hd, Wd, yd, return_lse=True, chunk_rows=chunk)
+        torch.cuda.synchronize()
+        assert flce.flce_get_status() == 0
+        runs.append((o, f, gW))
+        flce._workspaces.clear()
+        torch.cuda.empty_cache()
+    (o1, f1, g1), (o2, f2, g2) = runs
+    assert torch.equal(o1["predicted"], o2["predicted"]) and torch.equal(f1["lse"], f2["lse"])
+    assert torch.equal(o1["grad_h"], o2["grad_h"])
+    assert float(o1["token_accuracy"]) == float(o2["token_accuracy"])
+    assert abs(float(o1["loss"]) - float(o2["loss"])) <= 1e-6 * abs(float(o1["loss"]))
+    d = (g1 - g2).abs().max().item()
+    assert d <= 1e-5 * g1.abs().max().item(), d
