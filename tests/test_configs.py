@@ -134,7 +134,10 @@ def test_largest_chunk_matches_default_chunking(flce):
     four. Per-row results do not depend on the chunking, so lse, the predicted
     tokens and grad_h must equal the default (8192-row) run's bit for bit; the
     loss differs only by the grouping of its fp64 chunk sums, and grad_W by the
-    order of its fp32 chunk additions."""
+    order of its fp32 chunk additions. Those sums cancel heavily on the Zipf head
+    ids (partial sums far larger than the result), so the bound on grad_W is
+    1e-4 of its largest entry (measured 2.5e-5): a lost or doubled chunk would
+    be off by the order of the entries themselves."""
     w = workloads.WORKLOADS["dsv3"]
     h, W, y = workloads.make_inputs(w)
     hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
@@ -154,4 +157,4 @@ def test_largest_chunk_matches_default_chunking(flce):
     assert float(o1["token_accuracy"]) == float(o2["token_accuracy"])
     assert abs(float(o1["loss"]) - float(o2["loss"])) <= 1e-6 * abs(float(o1["loss"]))
     d = (g1 - g2).abs().max().item()
-    assert d <= 1e-5 * g1.abs().max().item(), d
+    assert d <= 1e-4 * g1.abs().max().item(), d
