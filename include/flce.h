@@ -75,6 +75,7 @@ extern "C" {
 #define FLCE_MODE_FORWARD 1
 #define FLCE_MODE_FORWARD_BACKWARD 2
 #define FLCE_MODE_CROSS_ENTROPY 3   /* flce_cross_entropy on materialised logits */
+#define FLCE_MODE_FORWARD_BACKWARD_HOST 4  /* flce_forward_backward_from_host */
 
 #define FLCE_REDUCTION_MEAN 0
 #define FLCE_REDUCTION_SUM 1
@@ -170,6 +171,27 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W,
                           const int64_t* labels, float* loss, float* token_accuracy,
                           int64_t* predicted, void* grad_h, float* grad_W,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward + backward with the inputs in HOST memory: h_host (bf16, rows of
+ * ld_h elements) and labels_host (int64 [N]) are host pointers; page-locked
+ * memory lets the copies overlap the kernels, pageable memory works but the
+ * copies then serialise. The labels are copied first (the prologue counts them
+ * all); h then goes over one chunk at a time on `copy_stream` into two staging
+ * buffers in the workspace, the copy of chunk k + 1 running under the kernels
+ * of chunk k on `stream`, ordered by events that the call creates and
+ * releases. loss_host and token_accuracy_host (nullable) are HOST floats,
+ * written by copies on `stream` at the end: read them after synchronising
+ * `stream`. W, predicted, grad_h and grad_W are device pointers as in
+ * flce_forward_backward. copy_stream may equal stream (the copies then do not
+ * overlap). bf16 only; FLCE_ERR_UNSUPPORTED with FLCE_FLAG_SIMT_GEMM or
+ * FLCE_FLAG_KMAJOR_BWD. Workspace: flce_workspace_size(p,
+ * FLCE_MODE_FORWARD_BACKWARD_HOST, ...), which adds two chunks of h and N
+ * labels to the FORWARD_BACKWARD size. The host buffers must stay valid and
+ * unchanged until `stream` has finished the call's work. */
+int flce_forward_backward_from_host(const flce_params* p, const void* h_host, const void* W,
+                                   const int64_t* labels_host, float* loss_host, float* token_accuracy_host,
+                                   int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* copy_stream);
 
 /* Cross-entropy on logits that are already materialised, [N, V] with row
  * stride ld_logits (>= V) in bf16 or fp32 (logits_dtype): the non-fused branch

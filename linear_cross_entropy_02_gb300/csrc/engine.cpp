@@ -163,6 +163,10 @@ struct Layout {
   bool need_z, need_dz, need_dzt, need_wt, need_ht, need_gh32;
   size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_dz, off_dzt, off_wt,
       off_ht, off_gh32, total;
+  // host inputs (flce_forward_backward_from_host): two chunk buffers of h, all
+  // labels, and the two result scalars before they are copied to the host
+  bool host_in;
+  size_t off_hstage, hstage_bytes, off_labels, off_out;
 };
 
 struct Norm {
@@ -202,6 +206,8 @@ int normalise(const flce_params* in, Norm* out, bool need_hidden = true) {
 
 void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   const flce_params& p = n.p;
+  L->host_in = mode == FLCE_MODE_FORWARD_BACKWARD_HOST;
+  if (L->host_in) mode = FLCE_MODE_FORWARD_BACKWARD;
   const bool ce = mode == FLCE_MODE_CROSS_ENTROPY;
   const bool simt = !ce && (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool bwd = mode == FLCE_MODE_FORWARD_BACKWARD && (gh || gw);
@@ -259,6 +265,10 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
   L->off_ht = L->need_ht ? take(es * p.hidden * L->ldht) : 0;
   L->off_gh32 = L->need_gh32 ? take(sizeof(float) * L->C * p.hidden) : 0;
+  L->hstage_bytes = L->host_in ? (static_cast<size_t>(L->C) * p.hidden * 2 + 255) / 256 * 256 : 0;
+  L->off_hstage = L->host_in ? take(2 * L->hstage_bytes) : 0;
+  L->off_labels = L->host_in ? take(sizeof(int64_t) * std::max<int64_t>(p.n_rows, 1)) : 0;
+  L->off_out = L->host_in ? take(2 * sizeof(float)) : 0;
   L->total = off;
 }
 
@@ -286,7 +296,7 @@ bool pick_wide(int flags, const GemmParams& g, int sms) {
   } while (0)
 
 struct Call {
-  int mode;
+  int mode;  // FLCE_MODE_*; host inputs come as FORWARD_BACKWARD with host_in set
   const void* h;
   const void* W;
   const int64_t* labels;
@@ -299,9 +309,77 @@ struct Call {
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
+  // host inputs: h and labels are host pointers, staged chunk by chunk on
+  // copy_stream; loss / acc are then host pointers written at the end
+  bool host_in = false;
+  cudaStream_t copy_stream = nullptr;
 };
 
 int run_f32(const Norm& n, const Call& c);
+// Chunked host-to-device staging of h for host inputs. Chunk k (rows
+// [kC, kC + C)) is copied on the copy stream into buffer k % 2 of the
+// workspace: `copied[b]` tells the compute stream it has landed, `freed[b]`
+// tells the copy stream that every kernel of the chunk that used the buffer
+// before has been enqueued ahead of it, so the copy may overwrite it.
+struct HostStaging {
+  uint8_t* buf[2] = {nullptr, nullptr};
+  const uint8_t* src = nullptr;
+  size_t ld_bytes = 0, row_bytes = 0;
+  int64_t n_rows = 0, C = 0;
+  cudaStream_t compute = nullptr, copy = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+
+  bool init(uint8_t* base, size_t buf_bytes, const void* h_host, int64_t ld_h, int64_t H, int64_t rows,
+            int64_t chunk, cudaStream_t comp, cudaStream_t cp) {
+    buf[0] = base;
+    buf[1] = base + buf_bytes;
+    src = static_cast<const uint8_t*>(h_host);
+    ld_bytes = static_cast<size_t>(ld_h) * 2;
+    row_bytes = static_cast<size_t>(H) * 2;
+    n_rows = rows;
+    C = chunk;
+    compute = comp;
+    copy = cp;
+    for (int b = 0; b < 2; ++b) {
+      if (cudaEventCreateWithFlags(&copied[b], cudaEventDisableTiming) != cudaSuccess) return false;
+      if (cudaEventCreateWithFlags(&freed[b], cudaEventDisableTiming) != cudaSuccess) return false;
+    }
+    // The first copies wait for everything already on the compute stream: an
+    // earlier call on the same workspace may still be reading the buffers.
+    if (cudaEventRecord(freed[0], compute) != cudaSuccess) return false;
+    if (cudaStreamWaitEvent(copy, freed[0], 0) != cudaSuccess) return false;
+    return issue(0) && issue(1);
+  }
+  bool issue(int64_t k) {
+    const int64_t r0 = k * C;
+    if (r0 >= n_rows) return true;
+    const int64_t rows = std::min<int64_t>(C, n_rows - r0);
+    const int b = static_cast<int>(k & 1);
+    if (k >= 2 && cudaStreamWaitEvent(copy, freed[b], 0) != cudaSuccess) return false;
+    if (cudaMemcpy2DAsync(buf[b], row_bytes, src + r0 * ld_bytes, ld_bytes, row_bytes, static_cast<size_t>(rows),
+                          cudaMemcpyHostToDevice, copy) != cudaSuccess)
+      return false;
+    return cudaEventRecord(copied[b], copy) == cudaSuccess;
+  }
+  // Called before chunk k's first kernel: releases chunk k - 1's buffer (all
+  // its kernels are enqueued), starts the copy of chunk k + 1 into it, and
+  // makes the compute stream wait for chunk k. Returns chunk k's rows.
+  const uint16_t* wait_chunk(int64_t k) {
+    if (k >= 1) {
+      if (cudaEventRecord(freed[(k - 1) & 1], compute) != cudaSuccess) return nullptr;
+      if (!issue(k + 1)) return nullptr;
+    }
+    if (cudaStreamWaitEvent(compute, copied[k & 1], 0) != cudaSuccess) return nullptr;
+    return reinterpret_cast<const uint16_t*>(buf[k & 1]);
+  }
+  ~HostStaging() {
+    for (int b = 0; b < 2; ++b) {  // released once the work recorded on them is done
+      if (copied[b]) cudaEventDestroy(copied[b]);
+      if (freed[b]) cudaEventDestroy(freed[b]);
+    }
+  }
+};
+
 
 int run(const flce_params* params, const Call& c) {
   Norm n;
@@ -313,11 +391,12 @@ int run(const flce_params* params, const Call& c) {
   const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
   if (!c.loss || !c.ws || !c.W) return FLCE_ERR_ARG;
   if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
-  if (!aligned16(c.ws) || (c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
+  if (!aligned16(c.ws) || (!c.host_in && c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
   if (gh && !aligned16(c.grad_h)) return FLCE_ERR_ALIGN;
   if (gw && !aligned16(c.grad_W)) return FLCE_ERR_ALIGN;
+  if (c.host_in && (p.flags & (FLCE_FLAG_SIMT_GEMM | FLCE_FLAG_KMAJOR_BWD))) return FLCE_ERR_UNSUPPORTED;
   Layout L;
-  make_layout(n, c.mode, gh, gw, &L);
+  make_layout(n, c.host_in ? FLCE_MODE_FORWARD_BACKWARD_HOST : c.mode, gh, gw, &L);
   if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   rc = device_info(&sms, &cc);
@@ -346,11 +425,31 @@ int run(const flce_params* params, const Call& c) {
   const int N = static_cast<int>(p.n_rows), H = static_cast<int>(p.hidden), V = static_cast<int>(p.vocab);
   const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
 
-  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(c.labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+  // Host inputs: the labels go over first (the prologue counts them all);
+  // chunk k of h goes to staging buffer k % 2 on copy_stream, at most two
+  // chunks ahead of the compute stream, so the copy of chunk k + 1 runs under
+  // the GEMMs of chunk k. Events order the two streams both ways.
+  const int64_t* labels = c.labels;
+  float* out_loss = c.loss;
+  float* out_acc = c.acc;
+  HostStaging hs;
+  if (c.host_in) {
+    labels = reinterpret_cast<const int64_t*>(ws + L.off_labels);
+    out_loss = reinterpret_cast<float*>(ws + L.off_out);
+    out_acc = out_loss + 1;
+    if (p.n_rows > 0 &&
+        cudaMemcpyAsync(const_cast<int64_t*>(labels), c.labels, sizeof(int64_t) * p.n_rows, cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (!hs.init(ws + L.off_hstage, L.hstage_bytes, c.h, n.ld_h, H, p.n_rows, L.C, stream, c.copy_stream))
+      return FLCE_ERR_CUDA;
+  }
+
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
 
   CUtensorMap map_h, map_w, map_wt;
   if (!simt && N > 0) {
-    if (!encode_bf16(&map_h, c.h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+    if (!c.host_in && !encode_bf16(&map_h, c.h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
     if (!encode_bf16(&map_w, c.W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
   }
   if (L.need_wt && N > 0) {  // debug paths only
@@ -361,7 +460,22 @@ int run(const flce_params* params, const Call& c) {
 
   for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
     const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
-    const int64_t* lab_c = c.labels + r0;
+    const int64_t* lab_c = labels + r0;
+    // where this chunk's rows of h are: the caller's array (row r0 of map_h)
+    // or the staging buffer the chunk was copied to (row 0 of its own map)
+    const uint16_t* h_c = static_cast<const uint16_t*>(c.h) + r0 * n.ld_h;
+    int64_t ld_hc = n.ld_h;
+    int h_row0 = static_cast<int>(r0);
+    CUtensorMap map_hc;
+    if (c.host_in) {
+      h_c = hs.wait_chunk(r0 / L.C);
+      if (!h_c) return FLCE_ERR_CUDA;
+      ld_hc = H;
+      h_row0 = 0;
+      if (!encode_bf16(&map_hc, h_c, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+    } else if (!simt) {
+      map_hc = map_h;
+    }
 
     // ---- forward GEMM with the statistics epilogue
     GemmParams g{};
@@ -379,7 +493,7 @@ int run(const flce_params* params, const Call& c) {
     // logits, written once here, do carry evict-first (store_hint): that keeps
     // them from displacing the operands, 1.5-3% on this GEMM.
     g.group_m = std::min(g.m_tiles, 16);
-    g.a_row0 = static_cast<int>(r0);
+    g.a_row0 = h_row0;
     g.b_row0 = 0;
     g.alpha = p.out_mult;
     g.M_valid = rows;
@@ -407,7 +521,7 @@ int run(const flce_params* params, const Call& c) {
       const int tiles = g.m_tiles * g.n_tiles;
       CUtensorMap map_z;
       if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, wide_for(g), &map_h, &map_w,
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, wide_for(g), &map_hc, &map_w,
                                              store ? &map_z : nullptr, g, std::min(tiles, sms), stream));
     }
 
@@ -449,7 +563,7 @@ int run(const flce_params* params, const Call& c) {
         r.n_tiles = (vs + kBN - 1) / kBN;
         r.k_iters = (H + kBK - 1) / kBK;
         r.group_m = std::min(r.m_tiles, 16);
-        r.a_row0 = static_cast<int>(r0);
+        r.a_row0 = h_row0;
         r.b_row0 = v0;
         r.alpha = p.out_mult;
         r.M_valid = rows;
@@ -467,7 +581,7 @@ int run(const flce_params* params, const Call& c) {
         r.col0 = v0;
         r.status = &hdr->status;
         r.timeout_ns = timeout;
-        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), &map_h, &map_w, nullptr, r,
+        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), &map_hc, &map_w, nullptr, r,
                                                      std::min(r.m_tiles * r.n_tiles, sms), stream));
         if (gh) {
           // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
@@ -501,7 +615,7 @@ int run(const flce_params* params, const Call& c) {
           // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
           CUtensorMap map_a, map_b;
           if (!encode_bf16(&map_a, dz, vs, rows, slab, 64)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
+          if (!encode_bf16(&map_b, h_c, H, rows, ld_hc, 64))
             return FLCE_ERR_UNSUPPORTED;
           GemmParams b{};
           std::memset(&b, 0, sizeof(b));
@@ -620,7 +734,7 @@ int run(const flce_params* params, const Call& c) {
         } else {
           // dz [C][V] and h_c [C][H] read in place: MN-major A and B (K = chunk rows)
           if (!encode_bf16(&map_a, dz, V, rows, L.ldd, 64)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
+          if (!encode_bf16(&map_b, h_c, H, rows, ld_hc, 64))
             return FLCE_ERR_UNSUPPORTED;
         }
         CUtensorMap map_o;
@@ -631,7 +745,13 @@ int run(const flce_params* params, const Call& c) {
     }
   }
 
-  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, out_loss, out_acc, stream));
+  if (c.host_in) {
+    if (cudaMemcpyAsync(c.loss, out_loss, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (c.acc && cudaMemcpyAsync(c.acc, out_acc, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+  }
   return FLCE_OK;
 }
 
@@ -908,7 +1028,7 @@ void flce_default_params(flce_params* p) {
 
 size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W) {
   Norm n;
-  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_CROSS_ENTROPY) return 0;
+  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_FORWARD_BACKWARD_HOST) return 0;
   if (normalise(p, &n, mode != FLCE_MODE_CROSS_ENTROPY) != FLCE_OK) return 0;
   Layout L;
   make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
@@ -935,6 +1055,18 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W, co
                           size_t workspace_bytes, void* stream) {
   Call c{FLCE_MODE_FORWARD_BACKWARD, h, W, labels, loss, token_accuracy, predicted, nullptr, grad_h, grad_W,
          workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  return run(p, c);
+}
+
+int flce_forward_backward_from_host(const flce_params* p, const void* h_host, const void* W,
+                                   const int64_t* labels_host, float* loss_host, float* token_accuracy_host,
+                                   int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* copy_stream) {
+  if (p && p->dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
+  Call c{FLCE_MODE_FORWARD_BACKWARD, h_host, W, labels_host, loss_host, token_accuracy_host, predicted, nullptr,
+         grad_h, grad_W, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.host_in = true;
+  c.copy_stream = static_cast<cudaStream_t>(copy_stream);
   return run(p, c);
 }
 

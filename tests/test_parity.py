@@ -351,3 +351,29 @@ def test_exact_tie_across_vocab_tiles_keeps_lowest_index(flce, flags):
     assert torch.all(pred == j1)
     valid = (y != -100)
     assert round(float(out["token_accuracy"]) * int(valid.sum())) == int(((y == j1) & valid).sum())
+
+
+def test_empty_batch(flce):
+    """No rows: the loss and accuracy are 0 (no valid rows), the per-row outputs
+    are empty, grad_W is left as it was, and the call launches only the
+    prologue and the finish kernels."""
+    H, V = 128, 1000
+    h = torch.zeros((0, H), dtype=torch.bfloat16, device=DEV)
+    W = workloads.make_weight(V, H, 1).to(DEV)
+    y = torch.zeros((0,), dtype=torch.int64, device=DEV)
+    gW = torch.full((V, H), 0.5, dtype=torch.float32, device=DEV)
+    n0 = flce.flce_launch_count()
+    out = flce.flce_forward_backward(h, W, y, grad_W=gW, return_predicted=True)
+    torch.cuda.synchronize()
+    assert flce.flce_launch_count() - n0 == 2
+    assert flce.flce_get_status() == 0
+    assert float(out["loss"]) == 0.0 and float(out["token_accuracy"]) == 0.0
+    assert out["grad_h"].shape == (0, H) and out["predicted"].shape == (0,)
+    assert torch.all(gW == 0.5)
+    f = flce.flce_forward(h, W, y, return_lse=True)
+    loss, acc = flce.flce_ce_only(h, W, y)
+    ce = flce.flce_cross_entropy(torch.zeros((0, V), dtype=torch.bfloat16, device=DEV), y, reduction="none")
+    torch.cuda.synchronize()
+    assert float(f["loss"]) == 0.0 and f["lse"].shape == (0,)
+    assert float(loss) == 0.0 and float(acc) == 0.0
+    assert float(ce["loss"]) == 0.0 and ce["row_loss"].shape == (0,) and ce["grad_logits"].shape == (0, V)
