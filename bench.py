@@ -204,14 +204,23 @@ KERNEL_SOURCES = ["gemm_tc.cu", "flce_device.cuh", "flce_epilogue.cuh", "flce_in
                   "kernels_ce.cu"]
 
 
+def code_only(src: str) -> str:
+    """C++ / CUDA source without comments, trailing blanks and empty lines: what
+    the compiler sees, so that editing a comment keeps a recorded figure valid."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the kernel sources: a recorded DRAM traffic figure is only
-    reported while the kernels are the ones it was measured on."""
+    """sha256 over the code of the kernel sources: a recorded DRAM traffic
+    figure is only reported while the kernels are the ones it was measured on."""
     import hashlib
     hsh = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "linear_cross_entropy_02_gb300", "csrc", f), "rb") as fh:
-            hsh.update(fh.read())
+        with open(os.path.join(ROOT, "linear_cross_entropy_02_gb300", "csrc", f)) as fh:
+            hsh.update(code_only(fh.read()).encode())
     return hsh.hexdigest()
 
 

@@ -9,9 +9,11 @@
 
 namespace flce {
 
-// Tile of the tensor-core GEMMs: 128 rows of D per CTA (one TMEM lane per row),
-// 256 columns (fp32 accumulator = 256 TMEM columns, two buffers = all 512),
-// 64-element K slices (one 128-byte swizzle row per operand row).
+// Tile of one tensor-core MMA: 128 rows of D (one TMEM lane per row), 256
+// columns (fp32 accumulator = 256 TMEM columns), 64-element K slices (one
+// 128-byte swizzle row per operand row). A CTA owns one such tile with two
+// accumulator buffers (all 512 columns, kStages-deep ring), or two stacked
+// (256 x 256, one buffer, a 3-stage ring of the same bytes).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;

@@ -1,15 +1,20 @@
 // Persistent tcgen05 GEMM with fused epilogues: D [M, N] = A [M, K] * B [N, K]^T.
 //
-// One CTA per SM, 192 threads, warp-specialised:
-//   warp 0      one lane issues TMA loads of 128x64 A and 256x64 B slices into a
-//               4-stage shared-memory ring (128-byte swizzle);
+// One CTA per SM, warp-specialised, in two tile shapes (template TMH):
+//   warp 0      one lane issues TMA loads of the A and B slices of each 64-deep
+//               K step into a shared-memory ring (128-byte swizzle);
 //   warp 1      owns the 512 TMEM columns; one lane issues tcgen05.mma
-//               (M=128, N=256, K=16 per instruction, fp32 accumulate) into one
-//               of two 256-column accumulators, so the epilogue of tile t
-//               overlaps the main loop of tile t+1;
-//   warps 2-5   the epilogue: thread r of the 128 owns row r of the tile
-//               (TMEM lane r), reads 32 columns at a time with tcgen05.ld and
-//               applies the mode's epilogue.
+//               (M=128, N=256, K=16 per instruction, fp32 accumulate);
+//   warps 2..   the epilogue: the thread on TMEM lane r owns row r of a 128-row
+//               half of the tile, reads 32 columns at a time with tcgen05.ld
+//               and applies the mode's epilogue.
+// TMH = 1: 128 x 256 tiles, 192 threads, a 4-stage ring of 48 KB stages and two
+//   256-column accumulators, so the epilogue of tile t overlaps the main loop
+//   of tile t+1 (four epilogue warps).
+// TMH = 2: 256 x 256 tiles, 320 threads, a 3-stage ring of 64 KB stages; two
+//   MMAs per K step (one per 128-row half of A) share the B slice, which takes
+//   a third less operand traffic into the SM per flop; the single 512-column
+//   accumulator is drained by eight epilogue warps.
 // Epilogue modes: forward statistics of the linear cross-entropy (softcap,
 // running max / sum of exponentials, argmax, label logit) with or without
 // storing the capped logits; bf16 store of alpha*acc (grad_h); fp32
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * ABytes;
-  uint8_t* sStage = smem + kStages * (kAStageBytes + kBStageBytes);  // epilogue staging, 4 warps x 2 buffers
+  uint8_t* sStage = smem + kStages * (kAStageBytes + kBStageBytes);  // epilogue staging, 32 KB
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kEpiStagingBytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
