@@ -302,6 +302,8 @@ def test_zipf_labels_and_row_sums(flce):
     dict(N=5, H=64, V=100),                                   # one partial row tile, V < one vocab tile
     dict(N=130, H=128, V=257, ignore_index=-1),               # custom ignore index, one column past a tile
     dict(N=200, H=64, V=1000, out_mult=-0.5, softcap=3.0),    # negative multiplier: the argmax flips
+    dict(N=70, H=8, V=300),                                   # H = 8: one 16-byte row per operand row
+    dict(N=40, H=64, V=1),                                    # one class: loss 0, every gradient 0
 ])
 def test_small_and_unusual_heads(flce, flags, case):
     c = dict(case)
