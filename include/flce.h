@@ -76,6 +76,7 @@ extern "C" {
 #define FLCE_MODE_FORWARD_BACKWARD 2
 #define FLCE_MODE_CROSS_ENTROPY 3   /* flce_cross_entropy on materialised logits */
 #define FLCE_MODE_FORWARD_BACKWARD_HOST 4  /* flce_forward_backward_from_host */
+#define FLCE_MODE_CE_ONLY_HOST 5           /* flce_ce_only_from_host */
 
 #define FLCE_REDUCTION_MEAN 0
 #define FLCE_REDUCTION_SUM 1
@@ -192,6 +193,14 @@ int flce_forward_backward_from_host(const flce_params* p, const void* h_host, co
                                    const int64_t* labels_host, float* loss_host, float* token_accuracy_host,
                                    int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
                                    size_t workspace_bytes, void* stream, void* copy_stream);
+
+/* CE-only pass with h and labels in HOST memory, staged as in
+ * flce_forward_backward_from_host; loss_host and token_accuracy_host (nullable)
+ * are host floats, valid once `stream` has finished. Workspace:
+ * flce_workspace_size(p, FLCE_MODE_CE_ONLY_HOST, 0, 0). */
+int flce_ce_only_from_host(const flce_params* p, const void* h_host, const void* W, const int64_t* labels_host,
+                           float* loss_host, float* token_accuracy_host, void* workspace, size_t workspace_bytes,
+                           void* stream, void* copy_stream);
 
 /* Cross-entropy on logits that are already materialised, [N, V] with row
  * stride ld_logits (>= V) in bf16 or fp32 (logits_dtype): the non-fused branch

@@ -28,7 +28,7 @@ from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEM
 
 __all__ = [
     "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward",
-    "flce_forward_backward_from_host", "flce_cross_entropy",
+    "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
     "flce_scale_gradient", "flce_workspace_size", "flce_get_status", "flce_launch_count", "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
 ]
@@ -231,6 +231,40 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
 _copy_streams: dict = {}
 
 
+def _host_inputs(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags,
+                 timeout_ns, vocab_slab, mode, need_gh, need_gw):
+    """Checks and marshals the host-input calls: h and labels on the host, W on
+    the device; returns (params, h rows, W, labels, workspace, bytes, copy stream)."""
+    for name, t in (("h", h), ("labels", labels)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{name} must be a host (CPU) tensor here")
+    if not isinstance(W, torch.Tensor) or W.device.type != "cuda" or W.dtype != torch.bfloat16 or W.dim() != 2:
+        raise ValueError("W must be a bf16 [V, H] CUDA tensor")
+    if h.dtype != torch.bfloat16 or h.shape[-1] != W.shape[1]:
+        raise ValueError("h must be bf16 [..., H] with W's H")
+    if labels.dtype != torch.int64 or labels.shape != h.shape[:-1]:
+        raise ValueError("labels must be int64 with h's leading shape")
+    H, V = W.shape[1], W.shape[0]
+    h2 = h.reshape(-1, H)
+    if h2.stride(1) != 1 or h2.stride(0) % 8 != 0:
+        h2 = h2.contiguous()
+    if W.stride(1) != 1 or W.stride(0) % 8 != 0 or W.data_ptr() % 16 != 0:
+        W = W.contiguous()
+    lab = labels.reshape(-1).contiguous()
+    p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
+                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _lib.FLCE_DTYPE_BF16)
+    nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_gh), int(need_gw))
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
+    dev = W.device
+    ws = _workspace(dev, nbytes)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    cs = _copy_streams.get(idx)
+    if cs is None:
+        cs = _copy_streams[idx] = torch.cuda.Stream(device=idx)
+    return p, h2, W, lab, ws, nbytes, cs
+
+
 def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tensor] = None, need_grad_h=True,
                                     softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
                                     grad_scale=1.0, return_predicted=False, chunk_rows=0, flags=0, timeout_ns=0,
@@ -244,37 +278,14 @@ def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tens
     labels must stay unchanged until then)."""
     if low_memory:
         flags |= FLCE_FLAG_RECOMPUTE
-    for name, t in (("h", h), ("labels", labels)):
-        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
-            raise ValueError(f"{name} must be a host (CPU) tensor here")
-    if not isinstance(W, torch.Tensor) or W.device.type != "cuda" or W.dtype != torch.bfloat16 or W.dim() != 2:
-        raise ValueError("W must be a bf16 [V, H] CUDA tensor")
-    if h.dtype != torch.bfloat16 or h.shape[-1] != W.shape[1]:
-        raise ValueError("h must be bf16 [..., H] with W's H")
-    if labels.dtype != torch.int64 or labels.shape != h.shape[:-1]:
-        raise ValueError("labels must be int64 with h's leading shape")
     if grad_W is not None and (grad_W.dtype != torch.float32 or grad_W.shape != W.shape or
                                not grad_W.is_contiguous() or grad_W.device != W.device):
         raise ValueError("grad_W must be a contiguous fp32 tensor shaped like W, on W's device")
-    H, V = W.shape[1], W.shape[0]
-    h2 = h.reshape(-1, H)
-    if h2.stride(1) != 1 or h2.stride(0) % 8 != 0:
-        h2 = h2.contiguous()
-    if W.stride(1) != 1 or W.stride(0) % 8 != 0 or W.data_ptr() % 16 != 0:
-        W = W.contiguous()
-    lab = labels.reshape(-1).contiguous()
-    dev = W.device
-    p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
-                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _lib.FLCE_DTYPE_BF16)
-    nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), _lib.FLCE_MODE_FORWARD_BACKWARD_HOST, int(need_grad_h),
-                                            int(grad_W is not None))
-    if nbytes == 0:
-        raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
-    ws = _workspace(dev, nbytes)
-    idx = dev.index if dev.index is not None else torch.cuda.current_device()
-    cs = _copy_streams.get(idx)
-    if cs is None:
-        cs = _copy_streams[idx] = torch.cuda.Stream(device=idx)
+    p, h2, W, lab, ws, nbytes, cs = _host_inputs(h, W, labels, softcap, out_mult, ignore_index, reduction,
+                                                 grad_scale, chunk_rows, flags, timeout_ns, vocab_slab,
+                                                 _lib.FLCE_MODE_FORWARD_BACKWARD_HOST, need_grad_h,
+                                                 grad_W is not None)
+    dev, H = W.device, W.shape[1]
     loss = torch.empty((), dtype=torch.float32).pin_memory()
     acc = torch.empty((), dtype=torch.float32).pin_memory()
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
@@ -286,6 +297,24 @@ def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tens
     lead = h.shape[:-1]
     return {"loss": loss, "token_accuracy": acc, "predicted": None if pred is None else pred.view(lead),
             "grad_h": None if gh is None else gh.view(*lead, H), "grad_W": grad_W}
+
+
+def flce_ce_only_from_host(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
+                           chunk_rows=0, flags=0, timeout_ns=0):
+    """CE-only pass with h and labels in (page-locked) host memory, copied by
+    the library chunk by chunk under its kernels. Returns (loss,
+    token_accuracy) as 0-d page-locked host tensors, valid once the current
+    stream has been synchronised."""
+    p, h2, W, lab, ws, nbytes, cs = _host_inputs(h, W, labels, softcap, out_mult, ignore_index, reduction, 1.0,
+                                                 chunk_rows, flags, timeout_ns, 0, _lib.FLCE_MODE_CE_ONLY_HOST,
+                                                 False, False)
+    loss = torch.empty((), dtype=torch.float32).pin_memory()
+    acc = torch.empty((), dtype=torch.float32).pin_memory()
+    rc = _lib.lib().flce_ce_only_from_host(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+                                           _ptr(ws), nbytes, _stream_handle(W.device),
+                                           ctypes.c_void_p(cs.cuda_stream))
+    _raise(rc, "flce_ce_only_from_host")
+    return loss, acc
 
 
 def flce_cross_entropy(logits, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",

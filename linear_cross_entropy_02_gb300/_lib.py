@@ -22,6 +22,7 @@ FLCE_MODE_FORWARD = 1
 FLCE_MODE_FORWARD_BACKWARD = 2
 FLCE_MODE_CROSS_ENTROPY = 3
 FLCE_MODE_FORWARD_BACKWARD_HOST = 4
+FLCE_MODE_CE_ONLY_HOST = 5
 
 FLCE_REDUCTION_MEAN = 0
 FLCE_REDUCTION_SUM = 1
@@ -41,8 +42,9 @@ FLCE_NUM_KERNELS = 15
 
 EXPORTED = [
     "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
-    "flce_forward_backward", "flce_forward_backward_from_host", "flce_cross_entropy", "flce_scale_gradient", "flce_get_status", "flce_status_string", "flce_launch_count",
-    "flce_profile_begin", "flce_profile_read", "flce_kernel_name",
+    "flce_forward_backward", "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
+    "flce_scale_gradient", "flce_get_status", "flce_status_string", "flce_launch_count", "flce_profile_begin",
+    "flce_profile_read", "flce_kernel_name",
 ]
 
 
@@ -112,6 +114,8 @@ def lib() -> ctypes.CDLL:
         L.flce_forward_backward_from_host.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                                       _vp]
         L.flce_forward_backward_from_host.restype = ctypes.c_int
+        L.flce_ce_only_from_host.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+        L.flce_ce_only_from_host.restype = ctypes.c_int
         L.flce_scale_gradient.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int64, _vp, _vp]
         L.flce_scale_gradient.restype = ctypes.c_int
         L.flce_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]

@@ -206,8 +206,9 @@ int normalise(const flce_params* in, Norm* out, bool need_hidden = true) {
 
 void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   const flce_params& p = n.p;
-  L->host_in = mode == FLCE_MODE_FORWARD_BACKWARD_HOST;
-  if (L->host_in) mode = FLCE_MODE_FORWARD_BACKWARD;
+  L->host_in = mode == FLCE_MODE_FORWARD_BACKWARD_HOST || mode == FLCE_MODE_CE_ONLY_HOST;
+  if (mode == FLCE_MODE_FORWARD_BACKWARD_HOST) mode = FLCE_MODE_FORWARD_BACKWARD;
+  if (mode == FLCE_MODE_CE_ONLY_HOST) mode = FLCE_MODE_CE_ONLY;
   const bool ce = mode == FLCE_MODE_CROSS_ENTROPY;
   const bool simt = !ce && (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool bwd = mode == FLCE_MODE_FORWARD_BACKWARD && (gh || gw);
@@ -296,7 +297,7 @@ bool pick_wide(int flags, const GemmParams& g, int sms) {
   } while (0)
 
 struct Call {
-  int mode;  // FLCE_MODE_*; host inputs come as FORWARD_BACKWARD with host_in set
+  int mode;  // FLCE_MODE_*; host inputs come as FORWARD_BACKWARD or CE_ONLY with host_in set
   const void* h;
   const void* W;
   const int64_t* labels;
@@ -396,7 +397,9 @@ int run(const flce_params* params, const Call& c) {
   if (gw && !aligned16(c.grad_W)) return FLCE_ERR_ALIGN;
   if (c.host_in && (p.flags & (FLCE_FLAG_SIMT_GEMM | FLCE_FLAG_KMAJOR_BWD))) return FLCE_ERR_UNSUPPORTED;
   Layout L;
-  make_layout(n, c.host_in ? FLCE_MODE_FORWARD_BACKWARD_HOST : c.mode, gh, gw, &L);
+  make_layout(n, !c.host_in ? c.mode
+                             : c.mode == FLCE_MODE_CE_ONLY ? FLCE_MODE_CE_ONLY_HOST : FLCE_MODE_FORWARD_BACKWARD_HOST,
+              gh, gw, &L);
   if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   rc = device_info(&sms, &cc);
@@ -1028,7 +1031,7 @@ void flce_default_params(flce_params* p) {
 
 size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W) {
   Norm n;
-  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_FORWARD_BACKWARD_HOST) return 0;
+  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_CE_ONLY_HOST) return 0;
   if (normalise(p, &n, mode != FLCE_MODE_CROSS_ENTROPY) != FLCE_OK) return 0;
   Layout L;
   make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
@@ -1065,6 +1068,17 @@ int flce_forward_backward_from_host(const flce_params* p, const void* h_host, co
   if (p && p->dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
   Call c{FLCE_MODE_FORWARD_BACKWARD, h_host, W, labels_host, loss_host, token_accuracy_host, predicted, nullptr,
          grad_h, grad_W, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.host_in = true;
+  c.copy_stream = static_cast<cudaStream_t>(copy_stream);
+  return run(p, c);
+}
+
+int flce_ce_only_from_host(const flce_params* p, const void* h_host, const void* W, const int64_t* labels_host,
+                           float* loss_host, float* token_accuracy_host, void* workspace, size_t workspace_bytes,
+                           void* stream, void* copy_stream) {
+  if (p && p->dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
+  Call c{FLCE_MODE_CE_ONLY, h_host, W, labels_host, loss_host, token_accuracy_host, nullptr, nullptr, nullptr,
+         nullptr, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.host_in = true;
   c.copy_stream = static_cast<cudaStream_t>(copy_stream);
   return run(p, c);

@@ -1,5 +1,5 @@
-"""flce_forward_backward_from_host: h and labels in host memory, copied chunk by
-chunk by the library under its own kernels. The kernels and their inputs are the
+"""flce_forward_backward_from_host and flce_ce_only_from_host: h and labels in
+host memory, copied chunk by chunk by the library under its own kernels. The kernels and their inputs are the
 same as with device inputs, so every output must equal the device-input call's
 bit for bit; the parity of that call with the oracle is covered elsewhere, and
 one case here also goes to the oracle directly."""
@@ -83,6 +83,18 @@ def test_host_inputs_strided_pageable_and_back_to_back(flce):
         torch.cuda.synchronize()
         assert float(outs[i]["loss"]) == float(r["loss"]), i
         assert torch.equal(outs[i]["grad_h"], r["grad_h"]), i
+
+
+def test_ce_only_from_host_equals_device_inputs(flce):
+    N, H, V = 1000, 256, 3000
+    h = workloads.make_hidden(N, H, 31).view(4, 250, H).pin_memory()   # leading dims are flattened
+    W = workloads.make_weight(V, H, 31, std=0.05).to(DEV)
+    y = workloads.make_labels(N, V, 31, 0.1).view(4, 250).pin_memory()
+    l1, a1 = flce.flce_ce_only_from_host(h, W, y, softcap=30.0, chunk_rows=128)
+    l2, a2 = flce.flce_ce_only(h.to(DEV), W, y.to(DEV), softcap=30.0, chunk_rows=128)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    assert float(l1) == float(l2) and float(a1) == float(a2)
 
 
 def test_host_inputs_rejections(flce):
