@@ -39,6 +39,8 @@ METRIC = "FLCE fwd+bwd tokens/s and TFLOP/s (6·N·H·V) as % of GB300 bf16 tens
 # path's peak is the measured bf16 peak scaled by it.
 TF32_OVER_BF16 = 1.1 / 2.25
 NOMINAL_TF32_TFLOPS = 1100.0  # GB300 dense tf32, nominal
+CPU_SAMPLE_SECONDS = 15.0      # oracle work in the cpu_baseline sample
+REFERENCE_STEP_ROWS = 16       # rows per step of the reference (oracle) arm
 UNIT = "tokens/s"
 
 
@@ -177,9 +179,9 @@ def run_reference(args, w):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    h, W, lab = workloads.make_inputs(w, n_rows=args.sample_rows * (args.steps + args.warmup))
+    R = args.sample_rows or REFERENCE_STEP_ROWS
+    h, W, lab = workloads.make_inputs(w, n_rows=R * (args.steps + args.warmup))
     W64 = weight_f64(W)
-    R = args.sample_rows
     times = []
     for s in range(args.warmup + args.steps):
         hs, ls = h[s * R:(s + 1) * R], lab[s * R:(s + 1) * R]
@@ -373,11 +375,17 @@ def run_ours(args, w):
                 roof["frac_of_nominal"] = achieved / NOMINAL_TF32_TFLOPS
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            R = args.sample_rows
-            n, t = cpu_oracle_rate(w, weight_f64(W_cpu), h_cpu[:R], lab_cpu[:R], warmup=True)
+            # A bounded sample sized to about CPU_SAMPLE_SECONDS of oracle work: an
+            # untimed call on a few rows (thread start-up, first touch) gives the
+            # time per row, then the first R rows are timed.
+            W64 = weight_f64(W_cpu)
+            r0 = min(4, w.n_rows)
+            _, t0 = cpu_oracle_rate(w, W64, h_cpu[:r0], lab_cpu[:r0])
+            R = args.sample_rows or int(max(16, min(w.n_rows, CPU_SAMPLE_SECONDS * r0 / max(t0[0], 1e-9))))
+            n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
             cpu = {"value": n / t[0], "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                    "sample": f"first {R} rows of the workload, full fp64 forward+backward over all "
-                             f"{w.vocab} logits (numpy), after one untimed warm-up call", "seconds": t[0],
+                             f"{w.vocab} logits (numpy), after an untimed call on {r0} rows", "seconds": t[0],
                    "extrapolated_full_step_s": t[0] * w.n_rows / n,
                    "extrapolation": "measured seconds per sampled row x the workload's rows (the oracle's "
                                     "cost is linear in rows); extrapolated, not measured"}
@@ -412,6 +420,26 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def cpu_ce_logits_rate(args, w, x_cpu, lab_cpu):
+    """The oracle of cross-entropy on materialised logits, as it stands, on a
+    bounded row sample sized to about CPU_SAMPLE_SECONDS."""
+    if args.no_cpu_baseline:
+        return None
+    from oracle import oracle_ce_logits
+    kw = dict(softcap=w.softcap, out_mult=w.out_mult, need_grad=True)
+    r0 = min(64, w.n_rows)
+    t0 = time.perf_counter()
+    oracle_ce_logits(x_cpu[:r0], lab_cpu[:r0], **kw)        # untimed: thread start-up, first touch
+    per_row = (time.perf_counter() - t0) / r0
+    R = args.sample_rows or int(max(16, min(w.n_rows, CPU_SAMPLE_SECONDS / max(per_row, 1e-9))))
+    t1 = time.perf_counter()
+    oracle_ce_logits(x_cpu[:R], lab_cpu[:R], **kw)
+    sec = time.perf_counter() - t1
+    return {"value": R / sec, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"first {R} rows of the {w.n_rows} x {w.vocab} bf16 logits, fp64 loss and gradient (numpy), "
+                      f"after an untimed call on {r0} rows", "seconds": sec}
 
 
 def run_ce_logits(args, w, world, rank, local, dist, flce):
@@ -502,7 +530,7 @@ def run_ce_logits(args, w, world, rank, local, dist, flce):
                          "peak_source": f"hbm_gbs ({peaks['source']})",
                          "traffic": recorded_traffic(w.name + "-ce_logits", dom),
                          "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": tms / n_launch},
-            "cpu_baseline": None,
+            "cpu_baseline": cpu_ce_logits_rate(args, w, x_cpu, lab_cpu) if world == 1 else None,
             "e2e": {"value": rows_total / e2e_max, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2 + lab.numel() * 8,
                     "d2h_bytes_per_step": 8},
             "gpu_launches": launches, "clocks": clk.summary(),
@@ -521,7 +549,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--chunk-rows", type=int, default=0)
-    ap.add_argument("--sample-rows", type=int, default=16)
+    ap.add_argument("--sample-rows", type=int, default=0,
+                    help="rows per oracle sample (0: 16 per reference-arm step; the cpu_baseline sizes its own "
+                         "sample to about %d s)" % CPU_SAMPLE_SECONDS)
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling captures only)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures only)")
     ap.add_argument("--low-memory", action="store_true",
