@@ -375,14 +375,19 @@ def run_ours(args, w):
                 roof["frac_of_nominal"] = achieved / NOMINAL_TF32_TFLOPS
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            # A bounded sample sized to about CPU_SAMPLE_SECONDS of oracle work: an
-            # untimed call on a few rows (thread start-up, first touch) gives the
-            # time per row, then the first R rows are timed.
+            # A bounded sample of about CPU_SAMPLE_SECONDS of oracle work: an untimed
+            # call on a few rows (thread start-up, first touch), then the first R
+            # rows are timed, R grown once from the time of 16 rows.
             W64 = weight_f64(W_cpu)
             r0 = min(4, w.n_rows)
-            _, t0 = cpu_oracle_rate(w, W64, h_cpu[:r0], lab_cpu[:r0])
-            R = args.sample_rows or int(max(16, min(w.n_rows, CPU_SAMPLE_SECONDS * r0 / max(t0[0], 1e-9))))
+            cpu_oracle_rate(w, W64, h_cpu[:r0], lab_cpu[:r0])
+            R = args.sample_rows or min(16, w.n_rows)
             n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
+            if not args.sample_rows and t[0] < CPU_SAMPLE_SECONDS / 2 and R < w.n_rows:
+                # the oracle's time has a fixed part (the [V, H] weight gradient), so
+                # the first sample is a lower bound on the rate: time a larger one
+                R = int(min(w.n_rows, R * CPU_SAMPLE_SECONDS / max(t[0], 1e-9)))
+                n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
             cpu = {"value": n / t[0], "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                    "sample": f"first {R} rows of the workload, full fp64 forward+backward over all "
                              f"{w.vocab} logits (numpy), after an untimed call on {r0} rows", "seconds": t[0],
