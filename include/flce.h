@@ -188,7 +188,8 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W,
  * FLCE_FLAG_KMAJOR_BWD. Workspace: flce_workspace_size(p,
  * FLCE_MODE_FORWARD_BACKWARD_HOST, ...), which adds two chunks of h and N
  * labels to the FORWARD_BACKWARD size. The host buffers must stay valid and
- * unchanged until `stream` has finished the call's work. */
+ * unchanged until `stream` has finished the call's work. The call creates and
+ * releases CUDA events, so it is not meant for stream capture. */
 int flce_forward_backward_from_host(const flce_params* p, const void* h_host, const void* W,
                                    const int64_t* labels_host, float* loss_host, float* token_accuracy_host,
                                    int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
