@@ -29,7 +29,8 @@ from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEM
 __all__ = [
     "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward",
     "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
-    "flce_scale_gradient", "flce_workspace_size", "flce_get_status", "flce_launch_count", "flce_profile_begin",
+    "flce_scale_gradient", "flce_workspace_size", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
+    "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
 ]
 
@@ -104,6 +105,13 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
         ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
+
+
+def flce_release_workspaces() -> None:
+    """Drops the cached workspaces (one per device and stream, grown to the
+    largest call so far); torch's allocator then holds the memory for reuse.
+    Call it after the last use on a stream, not while a call may still run."""
+    _workspaces.clear()
 
 
 def _raise(rc: int, what: str):
