@@ -133,6 +133,34 @@ def test_kernel_names(L):
     assert L.flce_kernel_name(99) == b"unknown"
 
 
+def test_host_buffer_entries_host_errors(L):
+    """The host-buffer entry points reject bad arguments before touching the
+    device or the host buffers (the pointers below are never dereferenced)."""
+    from linear_cross_entropy_02_gb300 import _lib as B
+    fake = ctypes.c_void_p(1 << 20)
+    p = _params(L)
+    need = L.flce_workspace_size(ctypes.byref(p), B.FLCE_MODE_FORWARD_BACKWARD_HOST, 1, 1)
+    base = L.flce_workspace_size(ctypes.byref(p), B.FLCE_MODE_FORWARD_BACKWARD, 1, 1)
+    # two chunks of h (bf16) and the labels on top of the device-input workspace
+    assert need >= base + 2 * 4096 * 512 * 2 + 4096 * 8
+    assert L.flce_workspace_size(ctypes.byref(p), B.FLCE_MODE_CE_ONLY_HOST, 0, 0) > \
+        L.flce_workspace_size(ctypes.byref(p), B.FLCE_MODE_CE_ONLY, 0, 0)
+    assert L.flce_workspace_size(ctypes.byref(p), 6, 0, 0) == 0             # unknown mode
+    rc = L.flce_forward_backward_from_host(ctypes.byref(p), fake, fake, fake, fake, None, None, fake, fake, fake,
+                                           need - 256, None, None)
+    assert rc == B.FLCE_ERR_WORKSPACE
+    rc = L.flce_forward_backward_from_host(ctypes.byref(p), fake, fake, fake, None, None, None, fake, fake, fake,
+                                           need, None, None)
+    assert rc == B.FLCE_ERR_ARG                                                  # no loss output
+    ps = _params(L, flags=B.FLCE_FLAG_SIMT_GEMM)
+    rc = L.flce_forward_backward_from_host(ctypes.byref(ps), fake, fake, fake, fake, None, None, fake, fake, fake,
+                                           1 << 40, None, None)
+    assert rc == B.FLCE_ERR_UNSUPPORTED
+    pf = _params(L, dtype=B.FLCE_DTYPE_F32)
+    rc = L.flce_ce_only_from_host(ctypes.byref(pf), fake, fake, fake, fake, None, fake, 1 << 40, None, None)
+    assert rc == B.FLCE_ERR_UNSUPPORTED
+
+
 def test_scale_gradient_host_errors(L):
     """Argument errors come back before any device call (the pointers are never
     dereferenced), and n = 0 is a no-op."""
