@@ -40,7 +40,7 @@ METRIC = "FLCE fwd+bwd tokens/s and TFLOP/s (6·N·H·V) as % of GB300 bf16 tens
 TF32_OVER_BF16 = 1.1 / 2.25
 NOMINAL_TF32_TFLOPS = 1100.0  # GB300 dense tf32, nominal
 CPU_SAMPLE_SECONDS = 15.0      # oracle work in the cpu_baseline sample
-REFERENCE_STEP_ROWS = 16       # rows per step of the reference (oracle) arm
+REFERENCE_STEP_ROWS = 256      # rows per step of the reference (oracle) arm
 UNIT = "tokens/s"
 
 
@@ -173,6 +173,43 @@ def cpu_oracle_rate(w: workloads.Workload, W64: np.ndarray, h_rows: torch.Tensor
                     need_grad_h=need_h, need_grad_W=need_w)
         times.append(time.perf_counter() - t0)
     return R, times
+
+
+def cpu_baseline_fwd_bwd(args, w, W_cpu, h_cpu, lab_cpu) -> dict:
+    """The oracle, as it stands, on a bounded sample of the workload's rows: an
+    untimed call on a few rows (thread start-up, first touch), then samples of
+    16 and 64 rows, then one grown to about CPU_SAMPLE_SECONDS. The oracle's
+    time has a fixed part (the [V, H] weight gradient) and a part per row; the
+    last two samples give both, and the full-step time is extrapolated from
+    them."""
+    W64 = weight_f64(W_cpu)
+    N = w.n_rows
+    r0 = min(4, N)
+    cpu_oracle_rate(w, W64, h_cpu[:r0], lab_cpu[:r0])
+    sizes = [args.sample_rows] if args.sample_rows else [min(16, N), min(64, N)]
+    runs = []
+    for R in sizes:
+        n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
+        runs.append((n, t[0]))
+    if not args.sample_rows and len(runs) == 2 and runs[1][0] > runs[0][0]:
+        per_row = max((runs[1][1] - runs[0][1]) / (runs[1][0] - runs[0][0]), 1e-9)
+        if runs[1][1] < CPU_SAMPLE_SECONDS / 2 and runs[1][0] < N:
+            R = int(min(N, runs[1][0] + (CPU_SAMPLE_SECONDS - runs[1][1]) / per_row))
+            n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
+            runs.append((n, t[0]))
+    n, sec = runs[-1]
+    out = {"value": n / sec, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+           "sample": f"first {n} rows of the workload, full fp64 forward+backward over all {w.vocab} logits "
+                     f"(numpy), after an untimed call on {r0} rows and timed samples of "
+                     f"{', '.join(str(r[0]) for r in runs[:-1]) or 'none'} rows",
+           "seconds": sec, "samples": [{"rows": r[0], "seconds": r[1]} for r in runs]}
+    if len(runs) >= 2 and runs[-1][0] > runs[-2][0]:
+        per_row = max((runs[-1][1] - runs[-2][1]) / (runs[-1][0] - runs[-2][0]), 0.0)
+        fixed = max(runs[-1][1] - per_row * runs[-1][0], 0.0)
+        out["extrapolated_full_step_s"] = fixed + per_row * N
+        out["extrapolation"] = ("fixed seconds + seconds per row x the workload's rows, fitted to the last two "
+                                "samples; extrapolated, not measured")
+    return out
 
 
 def run_reference(args, w):
@@ -375,25 +412,7 @@ def run_ours(args, w):
                 roof["frac_of_nominal"] = achieved / NOMINAL_TF32_TFLOPS
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            # A bounded sample of about CPU_SAMPLE_SECONDS of oracle work: an untimed
-            # call on a few rows (thread start-up, first touch), then the first R
-            # rows are timed, R grown once from the time of 16 rows.
-            W64 = weight_f64(W_cpu)
-            r0 = min(4, w.n_rows)
-            cpu_oracle_rate(w, W64, h_cpu[:r0], lab_cpu[:r0])
-            R = args.sample_rows or min(16, w.n_rows)
-            n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
-            if not args.sample_rows and t[0] < CPU_SAMPLE_SECONDS / 2 and R < w.n_rows:
-                # the oracle's time has a fixed part (the [V, H] weight gradient), so
-                # the first sample is a lower bound on the rate: time a larger one
-                R = int(min(w.n_rows, R * CPU_SAMPLE_SECONDS / max(t[0], 1e-9)))
-                n, t = cpu_oracle_rate(w, W64, h_cpu[:R], lab_cpu[:R])
-            cpu = {"value": n / t[0], "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                   "sample": f"first {R} rows of the workload, full fp64 forward+backward over all "
-                             f"{w.vocab} logits (numpy), after an untimed call on {r0} rows", "seconds": t[0],
-                   "extrapolated_full_step_s": t[0] * w.n_rows / n,
-                   "extrapolation": "measured seconds per sampled row x the workload's rows (the oracle's "
-                                    "cost is linear in rows); extrapolated, not measured"}
+            cpu = cpu_baseline_fwd_bwd(args, w, W_cpu, h_cpu, lab_cpu)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -555,8 +574,8 @@ def main():
     ap.add_argument("--workload", default="dsv3", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--sample-rows", type=int, default=0,
-                    help="rows per oracle sample (0: 16 per reference-arm step; the cpu_baseline sizes its own "
-                         "sample to about %d s)" % CPU_SAMPLE_SECONDS)
+                    help="rows per oracle sample (0: %d per reference-arm step; the cpu_baseline sizes its own "
+                         "sample to about %d s)" % (REFERENCE_STEP_ROWS, CPU_SAMPLE_SECONDS))
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling captures only)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures only)")
     ap.add_argument("--low-memory", action="store_true",
