@@ -158,3 +158,73 @@ def test_largest_chunk_matches_default_chunking(flce):
     assert abs(float(o1["loss"]) - float(o2["loss"])) <= 1e-6 * abs(float(o1["loss"]))
     d = (g1 - g2).abs().max().item()
     assert d <= 1e-4 * g1.abs().max().item(), d
+
+
+@pytest.fixture(scope="module")
+def dsv3_inputs():
+    w = workloads.WORKLOADS["dsv3"]
+    h, W, y = workloads.make_inputs(w)
+    return w, h, W, y
+
+
+def _fwd_bwd(flce, hd, Wd, yd, **kw):
+    gW = torch.zeros(Wd.shape, dtype=torch.float32, device=DEV)
+    o = flce.flce_forward_backward(hd, Wd, yd, grad_W=gW, return_predicted=True, **kw)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    flce.flce_release_workspaces()
+    return o
+
+
+def test_tile_shapes_agree_bit_for_bit_full_head(flce, dsv3_inputs):
+    """The DSV3 head in the benchmark's configuration on 256 x 256 tiles (the
+    default) and on 128 x 256 tiles: each output element is accumulated over
+    the same K order either way, so every output agrees bit for bit."""
+    w, h, W, y = dsv3_inputs
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    a = _fwd_bwd(flce, hd, Wd, yd)
+    b = _fwd_bwd(flce, hd, Wd, yd, flags=flce.FLCE_FLAG_TILE128)
+    assert float(a["loss"]) == float(b["loss"]) and float(a["token_accuracy"]) == float(b["token_accuracy"])
+    for k in ("predicted", "grad_h", "grad_W"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_low_memory_backward_matches_stored_logits_full_head(flce, dsv3_inputs):
+    """The recompute backward on the full DSV3 head: the forward is the same
+    kernel, so loss, accuracy and predictions are equal; the gradients differ
+    only by how dlogits' exponential is evaluated before the bf16 rounding."""
+    w, h, W, y = dsv3_inputs
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    a = _fwd_bwd(flce, hd, Wd, yd)
+    b = _fwd_bwd(flce, hd, Wd, yd, low_memory=True)
+    assert float(a["loss"]) == float(b["loss"]) and float(a["token_accuracy"]) == float(b["token_accuracy"])
+    assert torch.equal(a["predicted"], b["predicted"])
+    # grad_h is bf16: one rounding flip of its largest entries is 2^-8 of them;
+    # grad_W (fp32) differs by the few dz entries whose bf16 rounding flipped
+    for k, tol in (("grad_h", 2.0 ** -7), ("grad_W", 1e-3)):
+        x, z = a[k].float(), b[k].float()
+        assert (x - z).abs().max().item() <= tol * x.abs().max().item(), k
+
+
+def test_fp32_inputs_full_size_sampled_rows(flce, dsv3_inputs):
+    """The tf32 path on the full DSV3 head (fp32 h and W holding the bf16
+    values): per-row lse, predicted token and grad_h on sampled rows against
+    the oracle one by one, and the loss against the bf16 path's."""
+    w, h, W, y = dsv3_inputs
+    hd, Wd, yd = h.float().to(DEV), W.float().to(DEV), y.to(DEV)
+    o = flce.flce_forward_backward(hd, Wd, yd, return_predicted=True)
+    f = flce.flce_forward(hd, Wd, yd, return_lse=True)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    n_valid = int((y != -100).sum())
+    rows = workloads.sample_indices(w.n_rows, 128, seed=300)
+    ref = oracle_rows(h[rows], W, y[rows], n_valid)
+    lse = f["lse"].cpu().double().numpy()[rows]
+    assert np.abs(lse - ref["lse"]).max() <= 1e-4 * np.abs(ref["lse"]).max()
+    pred = o["predicted"].cpu().numpy()[rows]
+    assert np.all((pred == ref["predicted"]) | (ref["top2_gap"] < 1e-3))
+    g = o["grad_h"][torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * np.abs(ref["grad_h"]).max()
+    flce.flce_release_workspaces()
+    b = _fwd_bwd(flce, h.to(DEV), W.to(DEV), yd)
+    assert abs(float(o["loss"]) - float(b["loss"])) <= 2e-3 * abs(float(b["loss"]))
