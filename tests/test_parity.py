@@ -379,3 +379,54 @@ def test_empty_batch(flce):
     assert float(f["loss"]) == 0.0 and f["lse"].shape == (0,)
     assert float(loss) == 0.0 and float(acc) == 0.0
     assert float(ce["loss"]) == 0.0 and ce["row_loss"].shape == (0,) and ce["grad_logits"].shape == (0, V)
+
+
+@pytest.mark.parametrize("flags", [0, 8, 16, 32])
+def test_guard_bands_around_every_output_and_the_workspace(flce, flags):
+    """Through the C ABI with caller-made buffers: every output and the
+    workspace sit between guard bands filled with a sentinel, on a ragged
+    shape (several chunks, a partial vocab tile, H not a multiple of 64). No
+    kernel writes outside the bytes it owns, and the results still match the
+    oracle."""
+    import ctypes
+    from linear_cross_entropy_02_gb300 import _lib
+    L = _lib.lib()
+    N, H, V, C = 300, 136, 777, 128
+    h, W, y = _inputs(N, H, V, seed=44, W_scale=0.05)
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    G = 4096                                            # guard elements on each side
+
+    def guarded(n, dtype, fill):
+        buf = torch.full((n + 2 * G,), fill, dtype=dtype, device=DEV)
+        return buf, buf[G:G + n]
+
+    p = _lib.FlceParams()
+    L.flce_default_params(ctypes.byref(p))
+    p.n_rows, p.hidden, p.vocab, p.ld_h, p.ld_w, p.chunk_rows, p.flags = N, H, V, H, H, C, flags
+    p.vocab_slab = 256 if flags & 8 else 0
+    ws_bytes = L.flce_workspace_size(ctypes.byref(p), _lib.FLCE_MODE_FORWARD_BACKWARD, 1, 1)
+    ws_buf, ws = guarded(ws_bytes, torch.uint8, 0xA5)
+    gh_buf, gh = guarded(N * H, torch.bfloat16, -3.0)
+    gw_buf, gw = guarded(V * H, torch.float32, 0.0)
+    gw.fill_(0.0)
+    gw_buf[:G].fill_(-7.0)
+    gw_buf[G + V * H:].fill_(-7.0)
+    pr_buf, pr = guarded(N, torch.int64, -12345)
+    sc_buf, sc = guarded(2, torch.float32, -9.0)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = L.flce_forward_backward(ctypes.byref(p), ptr(hd), ptr(Wd), ptr(yd), ptr(sc[0:1]), ptr(sc[1:2]), ptr(pr),
+                                 ptr(gh), ptr(gw), ptr(ws), ws_bytes,
+                                 ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    st = ctypes.c_int32(-1)
+    assert L.flce_get_status(ptr(ws), ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream),
+                             ctypes.byref(st)) == 0 and st.value == 0
+    for name, buf, n, fill in (("workspace", ws_buf, ws_bytes, 0xA5), ("grad_h", gh_buf, N * H, -3.0),
+                               ("grad_W", gw_buf, V * H, -7.0), ("predicted", pr_buf, N, -12345),
+                               ("scalars", sc_buf, 2, -9.0)):
+        assert torch.all(buf[:G] == fill) and torch.all(buf[G + n:] == fill), name
+    out = {"loss": sc[0], "token_accuracy": sc[1], "predicted": pr, "grad_h": gh.view(N, H),
+           "grad_W": gw.view(V, H)}
+    ref = flce_oracle(h, W, y)
+    check_against_oracle(out, ref, y, what=f"guard bands flags={flags}")
