@@ -430,3 +430,25 @@ def test_guard_bands_around_every_output_and_the_workspace(flce, flags):
            "grad_W": gw.view(V, H)}
     ref = flce_oracle(h, W, y)
     check_against_oracle(out, ref, y, what=f"guard bands flags={flags}")
+
+
+@pytest.mark.parametrize("flags", [0, 32])
+def test_last_vocab_column_and_large_logits(flce, flags):
+    """Labels and argmax on the last vocabulary column (inside a partial vocab
+    tile), and logits of several hundred in magnitude: the max-subtracted sums
+    stay finite and match the oracle."""
+    N, H, V = 260, 128, 777
+    h, W, _ = _inputs(N, H, V, seed=51, W_scale=0.05)
+    W = W.float()
+    W[V - 1] = h.float()[: N].mean(0) * 4.0          # pushes column V-1 to the top for many rows
+    W = (W * 60.0).to(torch.bfloat16)                 # logits of O(100s)
+    y = torch.full((N,), V - 1, dtype=torch.int64)
+    y[::3] = torch.arange(0, N, 3) % V
+    y[5] = -100
+    out = run_fwd_bwd(flce, h, W, y, flags=flags)
+    assert torch.isfinite(out["loss"]).item() and torch.isfinite(out["grad_h"].float()).all()
+    assert torch.isfinite(out["grad_W"]).all()
+    ref = flce_oracle(h, W, y)
+    assert np.abs(ref["lse"]).max() > 100.0
+    assert int((out["predicted"].cpu() == V - 1).sum()) > 0
+    check_against_oracle(out, ref, y, what=f"large logits flags={flags}")
