@@ -394,3 +394,44 @@ def test_ce_logits_equals_fused_with_identity_weight():
     assert a["loss"] == pytest.approx(b["loss"], rel=1e-14)
     np.testing.assert_allclose(a["grad_logits"], b["grad_h"], atol=1e-16)
     np.testing.assert_array_equal(a["predicted"], b["predicted"])
+
+
+# --- randomised: finite differences and the textbook routine on drawn shapes -------
+def test_randomised_gradients_and_loss_against_autograd():
+    """Hypothesis draws small shapes, softcaps, multipliers (negative too),
+    reductions and ignored rows; the oracle's loss must equal torch's
+    cross_entropy on the fp64 capped logits, and its gradients fp64 autograd
+    through the same expression (an implementation that shares nothing with
+    the oracle's closed-form backward)."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    import torch
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(N=st.integers(1, 6), H=st.integers(1, 7), V=st.integers(2, 12),
+               T=st.sampled_from([0.0, 0.3, 2.5, 30.0]), m=st.sampled_from([1.0, 0.5, -1.25, 3.0]),
+               red=st.sampled_from(["mean", "sum"]), seed=st.integers(0, 10_000))
+    def check(N, H, V, T, m, red, seed):
+        rng = np.random.default_rng(seed)
+        h = rng.standard_normal((N, H))
+        W = rng.standard_normal((V, H)) * 0.8
+        lab = rng.integers(0, V, N)
+        lab[rng.random(N) < 0.25] = -100
+        out = flce_oracle(h, W, lab, softcap=T, out_mult=m, reduction=red, grad_scale=1.3)
+        ht = torch.tensor(h, requires_grad=True)
+        Wt = torch.tensor(W, requires_grad=True)
+        z = m * (ht @ Wt.T)
+        s = T * torch.tanh(z / T) if T > 0 else z
+        y = torch.tensor(lab)
+        if (y != -100).any():
+            loss = torch.nn.functional.cross_entropy(s, y, ignore_index=-100, reduction=red)
+            (1.3 * loss).backward()
+            assert abs(out["loss"] - loss.item()) <= 1e-12 * max(1.0, abs(loss.item()))
+            np.testing.assert_allclose(out["grad_h"], ht.grad.numpy(), rtol=1e-10, atol=1e-13)
+            np.testing.assert_allclose(out["grad_W"], Wt.grad.numpy(), rtol=1e-10, atol=1e-13)
+        else:
+            assert out["loss"] == 0.0 and not out["grad_h"].any() and not out["grad_W"].any()
+        pred = s.detach().numpy().argmax(1)             # numpy's argmax takes the first maximum
+        np.testing.assert_array_equal(out["predicted"], pred)
+
+    check()
