@@ -452,3 +452,29 @@ def test_last_vocab_column_and_large_logits(flce, flags):
     assert np.abs(ref["lse"]).max() > 100.0
     assert int((out["predicted"].cpu() == V - 1).sum()) > 0
     check_against_oracle(out, ref, y, what=f"large logits flags={flags}")
+
+
+def _fuzz_cases(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        cases.append(dict(
+            N=int(rng.integers(1, 700)), H=int(8 * rng.integers(1, 40)), V=int(rng.integers(2, 3000)),
+            softcap=float(rng.choice([0.0, 0.0, 1.5, 30.0])), out_mult=float(rng.choice([1.0, 0.5, -0.75, 2.0])),
+            chunk_rows=int(rng.choice([0, 128, 256, 384])), flags=int(rng.choice([0, 8, 16, 32, 40])),
+            reduction=str(rng.choice(["mean", "sum"])), ign=float(rng.choice([0.0, 0.1, 0.5])), seed=i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"N{c['N']}-H{c['H']}-V{c['V']}-f{c['flags']}")
+def test_fuzzed_shapes_and_options(flce, case):
+    """Seeded random shapes (any N, H a multiple of 8, any V), softcaps,
+    multipliers, chunk sizes, reductions, ignore fractions and GEMM paths,
+    each against the oracle in full."""
+    c = dict(case)
+    N, H, V, flags, ign, seed = c.pop("N"), c.pop("H"), c.pop("V"), c.pop("flags"), c.pop("ign"), c.pop("seed")
+    h, W, y = _inputs(N, H, V, seed=1000 + seed, ign=ign, W_scale=0.08)
+    G0 = (np.random.default_rng(seed).standard_normal((V, H)) * 1e-3).astype(np.float32).astype(np.float64)
+    out = run_fwd_bwd(flce, h, W, y, grad_W0=G0, flags=flags, **c)
+    ref = flce_oracle(h, W, y, grad_W0=G0, softcap=c["softcap"], out_mult=c["out_mult"], reduction=c["reduction"])
+    check_against_oracle(out, ref, y, grad_W0=G0, what=f"fuzz {case}")
