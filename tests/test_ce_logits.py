@@ -102,3 +102,28 @@ def test_ce_logits_llama_vocab_rows(flce):
     torch.cuda.synchronize()
     ref = oracle_ce_logits(x, y)
     _check(out, ref, y, "llama vocab")
+
+
+def _fuzz_cases(n=24, seed=77):
+    rng = np.random.default_rng(seed)
+    return [dict(N=int(rng.integers(1, 500)), V=int(rng.integers(2, 20000)),
+                 softcap=float(rng.choice([0.0, 2.0, 30.0])), out_mult=float(rng.choice([1.0, 0.5, -1.0])),
+                 reduction=str(rng.choice(["mean", "sum", "none"])), bf16=bool(rng.integers(0, 2)),
+                 ign=float(rng.choice([0.0, 0.2])), seed=i) for i in range(n)]
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"N{c['N']}-V{c['V']}-{c['reduction']}")
+def test_ce_logits_fuzzed(flce, case):
+    """Seeded random shapes (V anywhere, including inside the 8-column vectors
+    and across 8192-column tiles), dtypes, softcaps, multipliers, reductions and
+    ignore fractions, against the oracle."""
+    c = dict(case)
+    N, V, ign, seed = c.pop("N"), c.pop("V"), c.pop("ign"), c.pop("seed")
+    dtype = torch.bfloat16 if c.pop("bf16") else torch.float32
+    x = _logits(N, V, 900 + seed, dtype)
+    y = workloads.make_labels(N, V, 900 + seed, ign)
+    out = flce.flce_cross_entropy(x.to(DEV), y.to(DEV), **c)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = oracle_ce_logits(x, y, **c)
+    _check(out, ref, y, f"fuzz {case}")

@@ -88,3 +88,26 @@ def test_fp32_rejects_unsupported_modes(flce):
         flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), low_memory=True)
     with pytest.raises(ValueError):
         flce.flce_forward_backward(h.to(DEV), W.to(DEV).bfloat16(), y.to(DEV))
+
+
+def _fuzz_cases(n=16, seed=32):
+    rng = np.random.default_rng(seed)
+    return [dict(N=int(rng.integers(1, 600)), H=int(8 * rng.integers(1, 40)), V=int(rng.integers(2, 2500)),
+                 softcap=float(rng.choice([0.0, 2.0, 30.0])), out_mult=float(rng.choice([1.0, 0.5, -1.5])),
+                 chunk_rows=int(rng.choice([0, 128, 256])), flags=int(rng.choice([0, 16, 32])), seed=i)
+            for i in range(n)]
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"N{c['N']}-H{c['H']}-V{c['V']}-f{c['flags']}")
+def test_fp32_fuzzed_shapes(flce, case):
+    """Seeded random shapes and options on the tf32 path, against the oracle
+    on the exact fp32 inputs."""
+    c = dict(case)
+    N, H, V, seed = c.pop("N"), c.pop("H"), c.pop("V"), c.pop("seed")
+    h, W, y = _inputs_f32(N, H, V, seed=500 + seed)
+    out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=torch.zeros(V, H, device=DEV),
+                                     return_predicted=True, **c)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = flce_oracle(h, W, y, softcap=c["softcap"], out_mult=c["out_mult"])
+    check_against_oracle(out, ref, y, what=f"fp32 fuzz {case}")

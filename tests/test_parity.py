@@ -454,7 +454,7 @@ def test_last_vocab_column_and_large_logits(flce, flags):
     check_against_oracle(out, ref, y, what=f"large logits flags={flags}")
 
 
-def _fuzz_cases(n=24, seed=2024):
+def _fuzz_cases(n=64, seed=2024):
     rng = np.random.default_rng(seed)
     cases = []
     for i in range(n):
