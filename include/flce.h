@@ -184,8 +184,8 @@ int flce_forward_backward(const flce_params* p, const void* h, const void* W,
  * written by copies on `stream` at the end: read them after synchronising
  * `stream`. W, predicted, grad_h and grad_W are device pointers as in
  * flce_forward_backward. copy_stream may equal stream (the copies then do not
- * overlap). bf16 only; FLCE_ERR_UNSUPPORTED with FLCE_FLAG_SIMT_GEMM or
- * FLCE_FLAG_KMAJOR_BWD. Workspace: flce_workspace_size(p,
+ * overlap). h is bf16, or fp32 with p->dtype = FLCE_DTYPE_F32;
+ * FLCE_ERR_UNSUPPORTED with FLCE_FLAG_SIMT_GEMM or FLCE_FLAG_KMAJOR_BWD. Workspace: flce_workspace_size(p,
  * FLCE_MODE_FORWARD_BACKWARD_HOST, ...), which adds two chunks of h and N
  * labels to the FORWARD_BACKWARD size. The host buffers must stay valid and
  * unchanged until `stream` has finished the call's work. The call creates and

@@ -246,10 +246,11 @@ def _host_inputs(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_
     for name, t in (("h", h), ("labels", labels)):
         if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
             raise ValueError(f"{name} must be a host (CPU) tensor here")
-    if not isinstance(W, torch.Tensor) or W.device.type != "cuda" or W.dtype != torch.bfloat16 or W.dim() != 2:
-        raise ValueError("W must be a bf16 [V, H] CUDA tensor")
-    if h.dtype != torch.bfloat16 or h.shape[-1] != W.shape[1]:
-        raise ValueError("h must be bf16 [..., H] with W's H")
+    if not isinstance(W, torch.Tensor) or W.device.type != "cuda" or W.dim() != 2 or \
+            W.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("W must be a bf16 or fp32 [V, H] CUDA tensor")
+    if h.dtype != W.dtype or h.shape[-1] != W.shape[1]:
+        raise ValueError("h must be [..., H] with W's H and dtype")
     if labels.dtype != torch.int64 or labels.shape != h.shape[:-1]:
         raise ValueError("labels must be int64 with h's leading shape")
     H, V = W.shape[1], W.shape[0]
@@ -260,7 +261,7 @@ def _host_inputs(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_
         W = W.contiguous()
     lab = labels.reshape(-1).contiguous()
     p = _params(h2.shape[0], H, V, h2.stride(0), W.stride(0), softcap, out_mult, ignore_index, reduction,
-                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _lib.FLCE_DTYPE_BF16)
+                grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _dtype_code(W))
     nbytes = _lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_gh), int(need_gw))
     if nbytes == 0:
         raise FlceError(_lib.FLCE_ERR_ARG, "flce_workspace_size")
@@ -277,8 +278,8 @@ def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tens
                                     softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",
                                     grad_scale=1.0, return_predicted=False, chunk_rows=0, flags=0, timeout_ns=0,
                                     low_memory=False, vocab_slab=0):
-    """Forward + backward with h ([..., H] bf16) and labels (int64) in host
-    memory, page-locked for the copies to overlap the kernels: the library
+    """Forward + backward with h ([..., H], bf16 or fp32 like W) and labels
+    (int64) in host memory, page-locked for the copies to overlap the kernels: the library
     copies h chunk by chunk on a side stream while it computes the previous
     chunk. W, grad_W and the returned grad_h / predicted are CUDA tensors on
     the current device; loss and token_accuracy come back as 0-d page-locked
@@ -297,7 +298,7 @@ def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tens
     loss = torch.empty((), dtype=torch.float32).pin_memory()
     acc = torch.empty((), dtype=torch.float32).pin_memory()
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
-    gh = torch.empty((h2.shape[0], H), dtype=torch.bfloat16, device=dev) if need_grad_h else None
+    gh = torch.empty((h2.shape[0], H), dtype=W.dtype, device=dev) if need_grad_h else None
     rc = _lib.lib().flce_forward_backward_from_host(
         ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc), _ptr(pred), _ptr(gh), _ptr(grad_W),
         _ptr(ws), nbytes, _stream_handle(dev), ctypes.c_void_p(cs.cuda_stream))

@@ -266,7 +266,8 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
   L->off_ht = L->need_ht ? take(es * p.hidden * L->ldht) : 0;
   L->off_gh32 = L->need_gh32 ? take(sizeof(float) * L->C * p.hidden) : 0;
-  L->hstage_bytes = L->host_in ? (static_cast<size_t>(L->C) * p.hidden * 2 + 255) / 256 * 256 : 0;
+  const size_t h_es = p.dtype == FLCE_DTYPE_F32 ? 4 : 2;
+  L->hstage_bytes = L->host_in ? (static_cast<size_t>(L->C) * p.hidden * h_es + 255) / 256 * 256 : 0;
   L->off_hstage = L->host_in ? take(2 * L->hstage_bytes) : 0;
   L->off_labels = L->host_in ? take(sizeof(int64_t) * std::max<int64_t>(p.n_rows, 1)) : 0;
   L->off_out = L->host_in ? take(2 * sizeof(float)) : 0;
@@ -330,13 +331,13 @@ struct HostStaging {
   cudaStream_t compute = nullptr, copy = nullptr;
   cudaEvent_t copied[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
 
-  bool init(uint8_t* base, size_t buf_bytes, const void* h_host, int64_t ld_h, int64_t H, int64_t rows,
-            int64_t chunk, cudaStream_t comp, cudaStream_t cp) {
+  bool init(uint8_t* base, size_t buf_bytes, const void* h_host, int64_t ld_h, int64_t H, size_t elem_bytes,
+            int64_t rows, int64_t chunk, cudaStream_t comp, cudaStream_t cp) {
     buf[0] = base;
     buf[1] = base + buf_bytes;
     src = static_cast<const uint8_t*>(h_host);
-    ld_bytes = static_cast<size_t>(ld_h) * 2;
-    row_bytes = static_cast<size_t>(H) * 2;
+    ld_bytes = static_cast<size_t>(ld_h) * elem_bytes;
+    row_bytes = static_cast<size_t>(H) * elem_bytes;
     n_rows = rows;
     C = chunk;
     compute = comp;
@@ -365,13 +366,13 @@ struct HostStaging {
   // Called before chunk k's first kernel: releases chunk k - 1's buffer (all
   // its kernels are enqueued), starts the copy of chunk k + 1 into it, and
   // makes the compute stream wait for chunk k. Returns chunk k's rows.
-  const uint16_t* wait_chunk(int64_t k) {
+  const void* wait_chunk(int64_t k) {
     if (k >= 1) {
       if (cudaEventRecord(freed[(k - 1) & 1], compute) != cudaSuccess) return nullptr;
       if (!issue(k + 1)) return nullptr;
     }
     if (cudaStreamWaitEvent(compute, copied[k & 1], 0) != cudaSuccess) return nullptr;
-    return reinterpret_cast<const uint16_t*>(buf[k & 1]);
+    return buf[k & 1];
   }
   ~HostStaging() {
     for (int b = 0; b < 2; ++b) {  // released once the work recorded on them is done
@@ -444,7 +445,7 @@ int run(const flce_params* params, const Call& c) {
         cudaMemcpyAsync(const_cast<int64_t*>(labels), c.labels, sizeof(int64_t) * p.n_rows, cudaMemcpyHostToDevice,
                         stream) != cudaSuccess)
       return FLCE_ERR_CUDA;
-    if (!hs.init(ws + L.off_hstage, L.hstage_bytes, c.h, n.ld_h, H, p.n_rows, L.C, stream, c.copy_stream))
+    if (!hs.init(ws + L.off_hstage, L.hstage_bytes, c.h, n.ld_h, H, 2, p.n_rows, L.C, stream, c.copy_stream))
       return FLCE_ERR_CUDA;
   }
 
@@ -471,7 +472,7 @@ int run(const flce_params* params, const Call& c) {
     int h_row0 = static_cast<int>(r0);
     CUtensorMap map_hc;
     if (c.host_in) {
-      h_c = hs.wait_chunk(r0 / L.C);
+      h_c = static_cast<const uint16_t*>(hs.wait_chunk(r0 / L.C));
       if (!h_c) return FLCE_ERR_CUDA;
       ld_hc = H;
       h_row0 = 0;
@@ -767,11 +768,13 @@ int run_f32(const Norm& n, const Call& c) {
   const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
   if (!c.loss || !c.ws || !c.W) return FLCE_ERR_ARG;
   if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
-  if (!aligned16(c.ws) || (c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
+  if (!aligned16(c.ws) || (!c.host_in && c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
   if ((gh && !aligned16(c.grad_h)) || (gw && !aligned16(c.grad_W))) return FLCE_ERR_ALIGN;
   if (p.flags & (FLCE_FLAG_SIMT_GEMM | FLCE_FLAG_RECOMPUTE)) return FLCE_ERR_UNSUPPORTED;
   Layout L;
-  make_layout(n, c.mode, gh, gw, &L);
+  make_layout(n, !c.host_in ? c.mode
+                             : c.mode == FLCE_MODE_CE_ONLY ? FLCE_MODE_CE_ONLY_HOST : FLCE_MODE_FORWARD_BACKWARD_HOST,
+              gh, gw, &L);
   if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   int rc = device_info(&sms, &cc);
@@ -799,10 +802,27 @@ int run_f32(const Norm& n, const Call& c) {
   const float* W = static_cast<const float*>(c.W);
   constexpr int kSlice = kBK / 2;  // fp32 elements per 128-byte K slice
 
-  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(c.labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+  // host inputs: staged as in run(), with 4-byte elements
+  const int64_t* labels = c.labels;
+  float* out_loss = c.loss;
+  float* out_acc = c.acc;
+  HostStaging hs;
+  if (c.host_in) {
+    labels = reinterpret_cast<const int64_t*>(ws + L.off_labels);
+    out_loss = reinterpret_cast<float*>(ws + L.off_out);
+    out_acc = out_loss + 1;
+    if (p.n_rows > 0 &&
+        cudaMemcpyAsync(const_cast<int64_t*>(labels), c.labels, sizeof(int64_t) * p.n_rows, cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (!hs.init(ws + L.off_hstage, L.hstage_bytes, c.h, n.ld_h, H, 4, p.n_rows, L.C, stream, c.copy_stream))
+      return FLCE_ERR_CUDA;
+  }
+
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
   CUtensorMap map_h, map_w, map_wt;
   if (N > 0) {
-    if (!encode_f32_in(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+    if (!c.host_in && !encode_f32_in(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
     if (!encode_f32_in(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
   }
   if (L.need_wt && N > 0) {
@@ -811,7 +831,19 @@ int run_f32(const Norm& n, const Call& c) {
   }
   for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
     const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
-    const int64_t* lab_c = c.labels + r0;
+    const int64_t* lab_c = labels + r0;
+    // this chunk's rows of h: the caller's array or the staging buffer
+    const float* h_c = h + r0 * n.ld_h;
+    int64_t ld_hc = n.ld_h;
+    int h_row0 = static_cast<int>(r0);
+    CUtensorMap map_hc = map_h;
+    if (c.host_in) {
+      h_c = static_cast<const float*>(hs.wait_chunk(r0 / L.C));
+      if (!h_c) return FLCE_ERR_CUDA;
+      ld_hc = H;
+      h_row0 = 0;
+      if (!encode_f32_in(&map_hc, h_c, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+    }
     GemmParams g{};
     std::memset(&g, 0, sizeof(g));
     g.M = rows;
@@ -821,7 +853,7 @@ int run_f32(const Norm& n, const Call& c) {
     g.n_tiles = static_cast<int>(L.n_vtiles);
     g.k_iters = (H + kSlice - 1) / kSlice;
     g.group_m = std::min(g.m_tiles, 16);
-    g.a_row0 = static_cast<int>(r0);
+    g.a_row0 = h_row0;
     g.alpha = p.out_mult;
     g.M_valid = rows;
     g.N_valid = V;
@@ -843,7 +875,7 @@ int run_f32(const Norm& n, const Call& c) {
     g.store_hint = store ? 1 : 0;
     CUtensorMap map_z;
     if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, pick_wide(p.flags, g, sms), &map_h, &map_w,
+    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, pick_wide(p.flags, g, sms), &map_hc, &map_w,
                                                 store ? &map_z : nullptr, g,
                                                 std::min(g.m_tiles * g.n_tiles, sms), stream));
     MergeParams mp{};
@@ -906,7 +938,7 @@ int run_f32(const Norm& n, const Call& c) {
                                                     std::min(b.m_tiles * b.n_tiles, sms), stream));
     }
     if (gw) {  // grad_W += m dz^T h_c: A = dz^T [V][C], B = h_c^T [H][C]
-      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_f32(h + r0 * n.ld_h, n.ld_h, rows, H, ht, L.ldht, stream));
+      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_f32(h_c, ld_hc, rows, H, ht, L.ldht, stream));
       GemmParams b{};
       std::memset(&b, 0, sizeof(b));
       b.M = V;
@@ -929,7 +961,13 @@ int run_f32(const Norm& n, const Call& c) {
                                                     std::min(b.m_tiles * b.n_tiles, sms), stream));
     }
   }
-  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, c.loss, c.acc, stream));
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, out_loss, out_acc, stream));
+  if (c.host_in) {
+    if (cudaMemcpyAsync(c.loss, out_loss, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (c.acc && cudaMemcpyAsync(c.acc, out_acc, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+  }
   return FLCE_OK;
 }
 
@@ -1065,7 +1103,6 @@ int flce_forward_backward_from_host(const flce_params* p, const void* h_host, co
                                    const int64_t* labels_host, float* loss_host, float* token_accuracy_host,
                                    int64_t* predicted, void* grad_h, float* grad_W, void* workspace,
                                    size_t workspace_bytes, void* stream, void* copy_stream) {
-  if (p && p->dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
   Call c{FLCE_MODE_FORWARD_BACKWARD, h_host, W, labels_host, loss_host, token_accuracy_host, predicted, nullptr,
          grad_h, grad_W, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.host_in = true;
@@ -1076,7 +1113,6 @@ int flce_forward_backward_from_host(const flce_params* p, const void* h_host, co
 int flce_ce_only_from_host(const flce_params* p, const void* h_host, const void* W, const int64_t* labels_host,
                            float* loss_host, float* token_accuracy_host, void* workspace, size_t workspace_bytes,
                            void* stream, void* copy_stream) {
-  if (p && p->dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
   Call c{FLCE_MODE_CE_ONLY, h_host, W, labels_host, loss_host, token_accuracy_host, nullptr, nullptr, nullptr,
          nullptr, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.host_in = true;

@@ -156,7 +156,7 @@ def test_host_buffer_entries_host_errors(L):
     rc = L.flce_forward_backward_from_host(ctypes.byref(ps), fake, fake, fake, fake, None, None, fake, fake, fake,
                                            1 << 40, None, None)
     assert rc == B.FLCE_ERR_UNSUPPORTED
-    pf = _params(L, dtype=B.FLCE_DTYPE_F32)
+    pf = _params(L, dtype=B.FLCE_DTYPE_F32, flags=B.FLCE_FLAG_SIMT_GEMM)     # fp32: no SIMT path
     rc = L.flce_ce_only_from_host(ctypes.byref(pf), fake, fake, fake, fake, None, fake, 1 << 40, None, None)
     assert rc == B.FLCE_ERR_UNSUPPORTED
 

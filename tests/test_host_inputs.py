@@ -97,6 +97,31 @@ def test_ce_only_from_host_equals_device_inputs(flce):
     assert float(l1) == float(l2) and float(a1) == float(a2)
 
 
+@pytest.mark.parametrize("flags", [0, 32])
+def test_fp32_host_inputs_equal_device_inputs(flce, flags):
+    """The tf32 path from host buffers: fp32 h staged with 4-byte rows."""
+    N, H, V = 500, 136, 1000
+    g = torch.Generator().manual_seed(9)
+    h = torch.randn((N, H), generator=g).pin_memory()
+    W = torch.randn((V, H), generator=g) * 0.05
+    y = workloads.make_labels(N, V, 9, 0.1).pin_memory()
+    Wd = W.to(DEV)
+    gW1 = torch.zeros((V, H), device=DEV)
+    gW2 = torch.zeros((V, H), device=DEV)
+    o1 = flce.flce_forward_backward_from_host(h, Wd, y, grad_W=gW1, return_predicted=True, chunk_rows=128,
+                                              flags=flags)
+    o2 = flce.flce_forward_backward(h.to(DEV), Wd, y.to(DEV), grad_W=gW2, return_predicted=True, chunk_rows=128,
+                                    flags=flags)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    assert float(o1["loss"]) == float(o2["loss"]) and o1["grad_h"].dtype == torch.float32
+    for k in ("predicted", "grad_h", "grad_W"):
+        assert _same(o1[k], o2[k]), k
+    l1, a1 = flce.flce_ce_only_from_host(h, Wd, y, chunk_rows=128)
+    torch.cuda.synchronize()
+    assert float(l1) == float(o2["loss"])
+
+
 def test_host_inputs_rejections(flce):
     h = workloads.make_hidden(16, 64, 1)
     W = workloads.make_weight(100, 64, 1).to(DEV)
@@ -104,7 +129,7 @@ def test_host_inputs_rejections(flce):
     with pytest.raises(ValueError):
         flce.flce_forward_backward_from_host(h.to(DEV), W, y)            # h must be on the host
     with pytest.raises(ValueError):
-        flce.flce_forward_backward_from_host(h.float(), W.float(), y)    # bf16 only
+        flce.flce_forward_backward_from_host(h.float(), W, y)            # dtypes must match
     with pytest.raises(flce.FlceError):
         flce.flce_forward_backward_from_host(h, W, y, flags=flce.FLCE_FLAG_SIMT_GEMM)
     np.testing.assert_equal(flce.flce_get_status(), 0)
