@@ -33,9 +33,10 @@
  * Changes: only the backbone CE during the graph-free accumulation prepass).
  *
  * Conventions for every entry point:
- *  - All data pointers are DEVICE pointers owned by the caller. The library
- *    allocates nothing and keeps no state between calls except a launch
- *    counter and optional profiling events.
+ *  - All data pointers are DEVICE pointers owned by the caller, except the
+ *    host inputs and host results of the *_from_host entry points. The
+ *    library allocates no memory and keeps no state between calls except a
+ *    launch counter and optional profiling events.
  *  - Row-major layouts: h [N, ld_h] (ld_h >= H), W [V, ld_w] (ld_w >= H),
  *    grad_h [N, H] contiguous, grad_W [V, H] contiguous, labels/predicted/
  *    row_lse [N] contiguous. h, W and the workspace must be 16-byte aligned,
