@@ -334,6 +334,25 @@ def test_strided_hidden_rows(flce):
     check_against_oracle(out, flce_oracle(h, W, y), y, what="strided h")
 
 
+@pytest.mark.parametrize("flags", [0, 8, 32])
+def test_strided_weight_rows(flce, flags):
+    """W with a row stride larger than H (the vocabulary rows of a wider
+    matrix) is read in place by the forward GEMM (K-major) and by grad_h
+    (MN-major), and by the recompute path's slabs."""
+    N, H, V = 300, 128, 2000
+    h, Wbig, y = _inputs(N, H + 64, V, seed=14, W_scale=0.05)
+    h = h[:, :H].contiguous()
+    W = Wbig[:, :H]
+    assert W.stride(0) == H + 64
+    Wd = Wbig.to(DEV)[:, :H]
+    gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
+    out = flce.flce_forward_backward(h.to(DEV), Wd, y.to(DEV), grad_W=gW, return_predicted=True, flags=flags,
+                                     chunk_rows=128, vocab_slab=512 if flags & 8 else 0)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    check_against_oracle(out, flce_oracle(h, W.contiguous(), y), y, what=f"strided W flags={flags}")
+
+
 @pytest.mark.parametrize("flags", [0, 1])
 def test_exact_tie_across_vocab_tiles_keeps_lowest_index(flce, flags):
     """Two identical rows of W in different 256-column vocab tiles (and chunks of
