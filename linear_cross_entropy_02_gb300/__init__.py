@@ -29,7 +29,7 @@ from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEM
 __all__ = [
     "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward",
     "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
-    "flce_scale_gradient", "flce_workspace_size", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
+    "flce_scale_gradient", "flce_workspace_size", "flce_chunk_rows_for_budget", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
     "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
 ]
@@ -105,6 +105,25 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
         ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
+
+
+def flce_chunk_rows_for_budget(n_rows: int, hidden: int, vocab: int, budget_bytes: int, *,
+                               mode: int = FLCE_MODE_FORWARD_BACKWARD, need_grad_h: bool = True,
+                               need_grad_W: bool = True, flags: int = 0, dtype=torch.bfloat16) -> int:
+    """The largest chunk (a multiple of 128 rows, at most 32768) whose workspace
+    fits in budget_bytes, from flce_workspace_size; 0 if not even 128 rows fit
+    (then the recompute backward, FLCE_FLAG_RECOMPUTE, needs far less)."""
+    best, lo, hi = 0, 1, 32768 // 128
+    code = _lib.FLCE_DTYPE_F32 if dtype == torch.float32 else _lib.FLCE_DTYPE_BF16
+    while lo <= hi:                      # the workspace grows with the chunk
+        mid = (lo + hi) // 2
+        p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, mid * 128, flags, 0, 0, code)
+        need = int(_lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
+        if 0 < need <= budget_bytes:
+            best, lo = mid * 128, mid + 1
+        else:
+            hi = mid - 1
+    return best
 
 
 def flce_release_workspaces() -> None:

@@ -201,3 +201,24 @@ def test_params_struct_matches_header():
     ctype = {"int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "float": ctypes.c_float}
     assert [(n, ctype[t]) for t, n in decl] == list(FlceParams._fields_)
     assert ctypes.sizeof(FlceParams) == 104
+
+
+def test_chunk_rows_for_budget(L):
+    """The budget helper returns the largest 128-multiple chunk whose workspace
+    fits, and smaller budgets never give larger chunks."""
+    import linear_cross_entropy_02_gb300 as flce
+    from linear_cross_entropy_02_gb300 import _lib as B
+    N, H, V = 32768, 7168, 129280
+    last = 1 << 30
+    for gb in (20, 8, 4, 1):
+        c = flce.flce_chunk_rows_for_budget(N, H, V, gb << 30)
+        assert c % 128 == 0 and c <= last
+        last = c
+        if c:
+            assert flce.flce_workspace_size(N, H, V, chunk_rows=c) <= gb << 30
+            if c < 32768:
+                assert flce.flce_workspace_size(N, H, V, chunk_rows=c + 128) > gb << 30
+    # the recompute backward fits budgets the stored-logits one does not
+    tiny = 64 << 20
+    assert flce.flce_chunk_rows_for_budget(N, H, V, tiny) == 0
+    assert flce.flce_chunk_rows_for_budget(N, H, V, tiny, flags=B.FLCE_FLAG_RECOMPUTE) > 0
