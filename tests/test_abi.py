@@ -222,3 +222,26 @@ def test_chunk_rows_for_budget(L):
     tiny = 64 << 20
     assert flce.flce_chunk_rows_for_budget(N, H, V, tiny) == 0
     assert flce.flce_chunk_rows_for_budget(N, H, V, tiny, flags=B.FLCE_FLAG_RECOMPUTE) > 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library there is no fallback: the first call raises
+    and names the build step (checked in a fresh interpreter that points the
+    loader at a path with no library)."""
+    import subprocess
+    import sys
+    code = (
+        "import sys, torch\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "from linear_cross_entropy_02_gb300 import _lib\n"
+        f"_lib.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "import linear_cross_entropy_02_gb300 as flce\n"
+        "try:\n"
+        "    flce.flce_workspace_size(16, 64, 100)\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', e)\n"
+        "    sys.exit(0)\n"
+        "sys.exit(3)\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "no CPU or PyTorch fallback" in r.stdout
