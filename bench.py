@@ -263,11 +263,22 @@ def kernel_source_hash() -> str:
     return hsh.hexdigest()
 
 
-def recorded_traffic(workload: str, kernel: str):
+def _traffic_key(args, w):
+    """The key of a bench line's recorded traffic: the workload and the variant
+    of the path it runs. Lines with overridden sizes have none."""
+    if args.rows or args.vocab or args.chunk_rows or args.vocab_slab:
+        return None
+    if args.ce_logits:
+        return w.name + "-ce_logits"
+    return (w.name + ("-lowmem" if args.low_memory else "") + ("-fp32" if args.fp32 else "")
+            + ("-tile128" if args.tile128 else ""))
+
+
+def recorded_traffic(workload, kernel: str):
     """Per-launch dram__bytes_read.sum + dram__bytes_write.sum from the committed
     ncu capture summary, or None when absent or taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if workload is None or not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
@@ -382,7 +393,7 @@ def run_ours(args, w):
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": (f"bf16_tflops_sustained ({peaks['source']}) x 1.1/2.25 nominal tf32/bf16"
                                     if args.fp32 else f"bf16_tflops_sustained ({peaks['source']})"),
-                    "traffic": recorded_traffic(w.name + ("-lowmem" if args.low_memory else ""), dom),
+                    "traffic": recorded_traffic(_traffic_key(args, w), dom),
                     "traffic_unit": "bytes per launch (dram read + write, ncu)",
                     "algorithmic_flops_per_launch": per_launch_flops,
                     "avg_launch_ms": tms / n_launch}
@@ -532,7 +543,7 @@ def run_ce_logits(args, w, world, rank, local, dist, flce):
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "peak_source": f"hbm_gbs ({peaks['source']})",
-                         "traffic": recorded_traffic(w.name + "-ce_logits", dom),
+                         "traffic": recorded_traffic(_traffic_key(args, w), dom),
                          "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": tms / n_launch},
             "cpu_baseline": cpu_ce_logits_rate(args, w, x_cpu, lab_cpu) if world == 1 else None,
             "e2e": {"value": rows_total / e2e_max, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2 + lab.numel() * 8,
