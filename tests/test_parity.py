@@ -133,6 +133,9 @@ def test_tiny_head_full(flce, flags):
     dict(N=129, H=64, V=4100, chunk_rows=0),                 # H = one K slice, V tail of 4 columns
     dict(N=513, H=136, V=777, chunk_rows=256, softcap=30.0, out_mult=0.5),  # H % 64 != 0, softcap, m
     dict(N=256, H=256, V=2048, softcap=2.0, out_mult=0.5, reduction="sum", grad_scale=0.75),
+    # chunks of 768 and 332 rows: three 256-row units, then two (the second
+    # ending 180 rows past the data); V = 1500 gives six vocab units for grad_W
+    dict(N=1100, H=192, V=1500, chunk_rows=768),
 ])
 def test_edge_shapes(flce, flags, case):
     c = dict(case)
@@ -400,17 +403,18 @@ def test_empty_batch(flce):
     assert float(ce["loss"]) == 0.0 and ce["row_loss"].shape == (0,) and ce["grad_logits"].shape == (0, V)
 
 
-@pytest.mark.parametrize("flags", [0, 8, 16, 32])
+@pytest.mark.parametrize("flags", [0, 8, 16, 32, 40])
 def test_guard_bands_around_every_output_and_the_workspace(flce, flags):
     """Through the C ABI with caller-made buffers: every output and the
     workspace sit between guard bands filled with a sentinel, on a ragged
     shape (several chunks, a partial vocab tile, H not a multiple of 64). No
     kernel writes outside the bytes it owns, and the results still match the
-    oracle."""
+    oracle. On 256-row tiles the 300 rows are one chunk of two 256-row units,
+    the second ending 212 rows past the data."""
     import ctypes
     from linear_cross_entropy_02_gb300 import _lib
     L = _lib.lib()
-    N, H, V, C = 300, 136, 777, 128
+    N, H, V, C = 300, 136, 777, (384 if flags & 32 else 128)
     h, W, y = _inputs(N, H, V, seed=44, W_scale=0.05)
     hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
     G = 4096                                            # guard elements on each side
