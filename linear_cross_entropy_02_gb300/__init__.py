@@ -449,14 +449,31 @@ class _LinearCrossEntropy(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, grad_loss, grad_acc):
+        # The saved gradients are scaled in place (no second copy of grad_h, or
+        # of an fp32 grad_W). Their version counters are bumped so that a second
+        # backward through the same node (retain_graph=True) raises autograd's
+        # in-place modification error instead of scaling them twice.
         gh, gW = ctx.saved_tensors
         g = grad_loss.reshape(1)
         if gh is not None:
             flce_scale_gradient(gh, g, out=gh)
+            _bump_version(gh)
         if gW is not None:
-            gW = flce_scale_gradient(gW, g, out=gW if ctx.w_dtype == torch.float32 else None,
-                                     out_dtype=ctx.w_dtype)
+            in_place = ctx.w_dtype == torch.float32
+            gW_saved = gW
+            gW = flce_scale_gradient(gW, g, out=gW if in_place else None, out_dtype=ctx.w_dtype)
+            if in_place:
+                _bump_version(gW_saved)
         return gh, gW, None, None, None, None, None, None, None
+
+
+def _bump_version(t: torch.Tensor) -> None:
+    """Marks t as modified in place (its data was written through the C ABI)."""
+    inc = getattr(torch.autograd.graph, "increment_version", None)
+    if inc is not None:
+        inc(t)
+    else:
+        torch._C._increment_version(t)
 
 
 def linear_cross_entropy(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, reduction="mean",

@@ -161,3 +161,35 @@ def test_autograd_rejects_per_row_reduction(flce):
     h, W, y = _inputs(16, 64, 100, seed=3)
     with pytest.raises(ValueError):
         flce.linear_cross_entropy(h.to(DEV), W.to(DEV), y.to(DEV), reduction="none")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("need_gh", [True, False])
+def test_second_backward_through_the_node_raises(flce, dtype, need_gh):
+    """The backward scales the saved gradients in place (grad_h, and an fp32
+    grad_W); a second backward through the same node (retain_graph=True) would
+    scale them twice, so it must fail loudly with autograd's in-place error.
+    With bf16 W and no grad_h nothing saved is modified, and a second backward
+    gives the same gradient again."""
+    N, H, V = 128, 64, 500
+    h, W, y = _inputs(N, H, V, seed=31)
+    hd = h.to(DEV).to(dtype).requires_grad_(need_gh)
+    Wd = W.to(DEV).to(dtype).requires_grad_(True)
+    loss, _ = flce.linear_cross_entropy(hd, Wd, y.to(DEV))
+    (3.0 * loss).backward(retain_graph=True)
+    if not need_gh:
+        gW1 = Wd.grad.clone()
+        if dtype == torch.bfloat16:
+            Wd.grad = None
+            (3.0 * loss).backward()
+            assert torch.equal(Wd.grad, gW1)
+        else:
+            with pytest.raises(RuntimeError, match="inplace"):
+                loss.backward()
+            assert torch.equal(Wd.grad, gW1)
+        return
+    g1 = hd.grad.clone()
+    with pytest.raises(RuntimeError, match="inplace"):
+        loss.backward()
+    torch.cuda.synchronize()
+    assert torch.equal(hd.grad, g1)                  # the failed backward left the gradient as it was
