@@ -328,6 +328,35 @@ def test_sampled_helpers_agree_with_full(T, m):
     np.testing.assert_allclose(gw, full["grad_W"][ids], atol=1e-16)
 
 
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (2.5, 0.5)])
+def test_sampled_helpers_against_torch_autograd(T, m):
+    """The sampled helpers pinned directly, not only through the full oracle:
+    per-row lse, row loss and predicted token, grad_h rows and grad_W rows
+    against torch's fp64 logsumexp, cross_entropy and autograd on the capped
+    logits of the whole batch."""
+    N, H, V = 30, 12, 45
+    h, W, lab = _rand(N, H, V, 23, ign=3, scale=0.7)
+    ht = torch.tensor(h, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    z = m * ht @ Wt.T
+    s = T * torch.tanh(z / T) if T > 0 else z
+    loss = torch.nn.functional.cross_entropy(s, torch.tensor(lab), ignore_index=-100)
+    loss.backward()
+    n_valid = int((lab != -100).sum())
+    rows = np.array([0, 4, 11, 29])
+    r = oracle_rows(h[rows], W, lab[rows], n_valid, softcap=T, out_mult=m)
+    st = s.detach()
+    np.testing.assert_allclose(r["lse"], torch.logsumexp(st, 1).numpy()[rows], rtol=1e-14)
+    rl = torch.nn.functional.cross_entropy(st, torch.tensor(lab), ignore_index=-100, reduction="none").numpy()
+    np.testing.assert_allclose(r["row_loss"], rl[rows], rtol=1e-13, atol=1e-15)
+    np.testing.assert_array_equal(r["predicted"], st.argmax(1).numpy()[rows])
+    np.testing.assert_allclose(r["grad_h"], ht.grad.numpy()[rows], rtol=1e-12, atol=1e-16)
+    ids = np.array([1, 7, lab[5], 44])
+    gw = oracle_grad_W_rows(h, W, lab, ids, torch.logsumexp(st, 1).numpy(), n_valid, softcap=T, out_mult=m,
+                            block_rows=8)
+    np.testing.assert_allclose(gw, Wt.grad.numpy()[ids], rtol=1e-12, atol=1e-16)
+
+
 # --- the pages' printed accumulator sizes pin fp32 [V, H] ----------------------------
 def test_page_accumulator_sizes():
     with open(os.path.join(GOLDEN, "page_figures.json")) as f:
