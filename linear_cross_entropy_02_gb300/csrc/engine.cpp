@@ -54,10 +54,14 @@ struct LaunchScope {
   cudaEvent_t start = nullptr, stop = nullptr;
   LaunchScope(int k, cudaStream_t s) : kernel(k), stream(s) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    if (g_prof_on && cudaEventCreate(&start) == cudaSuccess && cudaEventCreate(&stop) == cudaSuccess) {
-      cudaEventRecord(start, stream);
-    } else {
+    if (!g_prof_on) return;
+    if (cudaEventCreate(&start) != cudaSuccess) {
+      start = nullptr;
+    } else if (cudaEventCreate(&stop) != cudaSuccess) {
+      cudaEventDestroy(start);
       start = stop = nullptr;
+    } else {
+      cudaEventRecord(start, stream);
     }
   }
   ~LaunchScope() {
