@@ -45,7 +45,7 @@ def test_cuda_graph_capture_and_replay(flce):
         assert float(out["loss"]) == float(ref["loss"])
         assert float(out["token_accuracy"]) == float(ref["token_accuracy"])
         assert torch.equal(out["grad_h"], ref["grad_h"])
-        assert torch.allclose(gW, ref_gW, rtol=0, atol=1e-6 * ref_gW.abs().max().item())
+        assert torch.equal(gW, ref_gW)              # the same launches, so the same sums
 
 
 def test_two_streams_use_separate_workspaces(flce):
