@@ -54,13 +54,14 @@ def _peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def _config(w: workloads.Workload, chunk_rows: int):
+def _config(w: workloads.Workload, chunk_rows: int, chunk_used: int = 0):
     return {"workload": f"{w.name}: N={w.n_rows} H={w.hidden} V={w.vocab} "
                         f"{'zipf(%g)' % w.zipf_s if w.labels == 'zipf' else 'uniform'} labels, "
                         f"{int(round(w.ignore_frac * 100))}% ignored, T={w.softcap}, m={w.out_mult}, "
                         f"mode={w.mode}",
             "n_rows": w.n_rows, "hidden": w.hidden, "vocab": w.vocab, "softcap": w.softcap,
             "out_mult": w.out_mult, "mode": w.mode, "chunk_rows": chunk_rows,
+            **({"chunk_rows_used": chunk_used} if chunk_used else {}),
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
@@ -448,7 +449,11 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "ms_per_step_median": statistics.median(per_step), "ms_per_step_min": min(per_step),
             "vs_baseline": None, "dtype": "f32 (tf32 tensor cores)" if args.fp32 else "bf16", "data": "synthetic",
-            "config": _config(w, args.chunk_rows),
+            "config": _config(w, args.chunk_rows, flce.flce_chunk_rows(
+                w.n_rows, w.hidden, w.vocab,
+                mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
+                need_grad_W=w.mode == "fwd_bwd", chunk_rows=args.chunk_rows,
+                flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"])),
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
             "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,

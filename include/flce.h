@@ -137,6 +137,14 @@ void flce_default_params(flce_params* p);
  * Returns 0 for invalid parameters. */
 size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int need_grad_W);
 
+/* Rows per chunk that a call with these arguments uses: chunk_rows rounded up
+ * to a multiple of 128 (at most 32768 and at most N rounded up), or, when
+ * chunk_rows is 0, the library's choice: 8192, except for the stored-logits
+ * bf16 backward, which takes the multiple of 256 from 8192 to 10240 whose
+ * chunks fill the tensor-core GEMMs' waves best on 152 SMs (8192 on ties).
+ * Returns 0 for invalid parameters. */
+int64_t flce_chunk_rows(const flce_params* p, int mode, int need_grad_h, int need_grad_W);
+
 /* CE-only pass: loss and (optionally) token_accuracy, no gradients, no saved
  * state. loss: device float scalar; token_accuracy: device float scalar or NULL. */
 int flce_ce_only(const flce_params* p, const void* h, const void* W, const int64_t* labels,

@@ -29,7 +29,7 @@ from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEM
 __all__ = [
     "flce_ce_only", "flce_ce_only_noalloc", "flce_forward", "flce_forward_backward",
     "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
-    "flce_scale_gradient", "flce_workspace_size", "flce_chunk_rows_for_budget", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
+    "flce_scale_gradient", "flce_workspace_size", "flce_chunk_rows", "flce_chunk_rows_for_budget", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
     "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
 ]
@@ -143,6 +143,14 @@ def flce_workspace_size(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_M
                         flags: int = 0) -> int:
     p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0)
     return int(_lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
+
+
+def flce_chunk_rows(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_MODE_FORWARD_BACKWARD,
+                    need_grad_h: bool = True, need_grad_W: bool = True, chunk_rows: int = 0,
+                    flags: int = 0) -> int:
+    """Rows per chunk a call with these arguments uses (the library's choice when chunk_rows is 0)."""
+    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0)
+    return int(_lib.lib().flce_chunk_rows(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
 
 
 def _prepare(h, W, labels, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags,

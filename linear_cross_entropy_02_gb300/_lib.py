@@ -41,7 +41,7 @@ FLCE_FLAG_TILE256 = 32
 FLCE_NUM_KERNELS = 15
 
 EXPORTED = [
-    "flce_default_params", "flce_workspace_size", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
+    "flce_default_params", "flce_workspace_size", "flce_chunk_rows", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
     "flce_forward_backward", "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
     "flce_scale_gradient", "flce_get_status", "flce_status_string", "flce_launch_count", "flce_profile_begin",
     "flce_profile_read", "flce_kernel_name",
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.flce_default_params.restype = None
         L.flce_workspace_size.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.flce_workspace_size.restype = _sz
+        L.flce_chunk_rows.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.flce_chunk_rows.restype = ctypes.c_int64
         L.flce_ce_only.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.flce_ce_only.restype = ctypes.c_int
         L.flce_ce_only_noalloc.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]

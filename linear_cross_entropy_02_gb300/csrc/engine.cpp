@@ -208,6 +208,57 @@ int normalise(const flce_params* in, Norm* out, bool need_hidden = true) {
   return FLCE_OK;
 }
 
+// ------------------------------------------------------------ default chunk
+// Predicted cost of one tcgen05 GEMM in units of one 128-row tile's K step:
+// the waves of its persistent grid in 128 x 256 tiles, or 1.82 per wave of
+// 256 x 256 tiles where those finish first (the rule pick_wide applies at
+// launch), times its K steps.
+constexpr int kTunedSms = 152;  // GB300
+
+double gemm_cost(int64_t m_tiles, int64_t n_tiles, int64_t k_iters, int flags) {
+  const int64_t narrow = (m_tiles * n_tiles + kTunedSms - 1) / kTunedSms;
+  const int64_t wide = (((m_tiles + 1) / 2) * n_tiles + kTunedSms - 1) / kTunedSms;
+  double waves = std::min<double>(static_cast<double>(narrow), 1.82 * static_cast<double>(wide));
+  if (flags & FLCE_FLAG_TILE128) waves = static_cast<double>(narrow);
+  if (flags & FLCE_FLAG_TILE256) waves = 1.82 * static_cast<double>(wide);
+  return waves * static_cast<double>(k_iters);
+}
+
+// The forward, grad_h and grad_W GEMMs of one chunk of `rows` rows.
+double chunk_cost(int64_t rows, int64_t H, int64_t V, bool gh, bool gw, int flags) {
+  const int64_t m = (rows + kBM - 1) / kBM;
+  double t = gemm_cost(m, (V + kBN - 1) / kBN, (H + kBK - 1) / kBK, flags);
+  if (gh) t += gemm_cost(m, (H + kBN - 1) / kBN, (V + kBK - 1) / kBK, flags);
+  if (gw) t += gemm_cost((V + kBM - 1) / kBM, (H + kBN - 1) / kBN, (rows + kBK - 1) / kBK, flags);
+  return t;
+}
+
+// Rows per chunk when the caller leaves chunk_rows at 0, for the stored-logits
+// backward: among multiples of 256 from 8192 to 10240, the one whose chunks
+// (the last one ragged) give the lowest predicted GEMM cost; 8192 on ties.
+// It matters where a GEMM's tile count leaves its last wave nearly empty: on
+// the frozen 131072 x 4096 x 151936 head, grad_h on 8192-row chunks takes 7
+// waves of 128-row tiles per chunk, on 9728-row chunks exactly 4 waves of
+// 256-row tiles, and the forward + grad_h step went from 212.0 to 202.4 ms.
+// The other calls keep 8192 rows.
+int64_t default_chunk_rows(int64_t N, int64_t H, int64_t V, bool gh, bool gw, int flags) {
+  auto total = [&](int64_t C) {
+    const int64_t full = N / C, rem = N % C;
+    return static_cast<double>(full) * chunk_cost(C, H, V, gh, gw, flags) +
+           (rem > 0 ? chunk_cost(rem, H, V, gh, gw, flags) : 0.0);
+  };
+  int64_t best = kDefaultChunkRows;
+  double best_t = total(best);
+  for (int64_t C = kDefaultChunkRows + 256; C <= 10240; C += 256) {
+    const double t = total(C);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best = C;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   const flce_params& p = n.p;
   L->host_in = mode == FLCE_MODE_FORWARD_BACKWARD_HOST || mode == FLCE_MODE_CE_ONLY_HOST;
@@ -216,7 +267,11 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   const bool ce = mode == FLCE_MODE_CROSS_ENTROPY;
   const bool simt = !ce && (p.flags & FLCE_FLAG_SIMT_GEMM) != 0;
   const bool bwd = mode == FLCE_MODE_FORWARD_BACKWARD && (gh || gw);
-  int64_t c = p.chunk_rows > 0 ? p.chunk_rows : kDefaultChunkRows;
+  const bool tuned = bwd && !simt && p.dtype == FLCE_DTYPE_BF16 &&
+                     (p.flags & (FLCE_FLAG_RECOMPUTE | FLCE_FLAG_KMAJOR_BWD)) == 0 && p.n_rows > kDefaultChunkRows;
+  int64_t c = p.chunk_rows > 0 ? p.chunk_rows
+              : tuned        ? default_chunk_rows(p.n_rows, p.hidden, p.vocab, gh, gw, p.flags)
+                             : kDefaultChunkRows;
   c = std::min<int64_t>(c, std::max<int64_t>(p.n_rows, 1));
   c = std::min<int64_t>(c, 32768);  // grid.y of the row-streaming kernels stays below 65536
   L->C = round_up(c, kBM);
@@ -1078,6 +1133,15 @@ size_t flce_workspace_size(const flce_params* p, int mode, int need_grad_h, int 
   Layout L;
   make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
   return L.total;
+}
+
+int64_t flce_chunk_rows(const flce_params* p, int mode, int need_grad_h, int need_grad_W) {
+  Norm n;
+  if (mode < FLCE_MODE_CE_ONLY || mode > FLCE_MODE_CE_ONLY_HOST) return 0;
+  if (normalise(p, &n, mode != FLCE_MODE_CROSS_ENTROPY) != FLCE_OK) return 0;
+  Layout L;
+  make_layout(n, mode, need_grad_h != 0, need_grad_W != 0, &L);
+  return L.C;
 }
 
 int flce_ce_only(const flce_params* p, const void* h, const void* W, const int64_t* labels, float* loss,

@@ -84,6 +84,34 @@ def test_workspace_independent_of_n_beyond_a_chunk(L):
     assert 0 < L.flce_workspace_size(ctypes.byref(pc), 3, 0, 0) < 100e6
 
 
+def test_default_chunk_fills_the_gemm_waves(L):
+    """chunk_rows = 0 on the stored-logits backward: 8192 rows unless another
+    multiple of 256 up to 10240 fills the GEMMs' waves better. On the frozen
+    131072 x 4096 x 151936 head with grad_h only that is 9728 rows: 38 units of
+    256 rows x 16 column tiles = 608 tiles, exactly 4 waves on 152 SMs. The
+    DSV3, Llama and Muse heads keep 8192, and so do the recompute backward and
+    an explicit chunk size."""
+    def ws(N, H, V, gw, chunk=0, flags=0):
+        p = _params(L, N=N, H=H, V=V, chunk_rows=chunk, flags=flags)
+        return L.flce_workspace_size(ctypes.byref(p), 2, 1, int(gw))
+    assert ws(131072, 4096, 151936, False) == ws(131072, 4096, 151936, False, 9728)
+    assert ws(131072, 4096, 151936, False) > ws(131072, 4096, 151936, False, 8192)
+    for N, H, V in ((32768, 7168, 129280), (8192, 4096, 128256), (8192, 6656, 202048)):
+        assert ws(N, H, V, True) == ws(N, H, V, True, 8192), (N, H, V)
+    assert ws(131072, 4096, 151936, False, flags=8) == ws(131072, 4096, 151936, False, 8192, flags=8)
+
+    def rows(N, H, V, gw, mode=2, chunk=0, flags=0):
+        p = _params(L, N=N, H=H, V=V, chunk_rows=chunk, flags=flags)
+        return L.flce_chunk_rows(ctypes.byref(p), mode, 1, int(gw))
+    assert rows(131072, 4096, 151936, False) == 9728
+    assert rows(32768, 7168, 129280, True) == 8192
+    assert rows(131072, 4096, 151936, False, mode=0) == 8192           # CE-only
+    assert rows(131072, 4096, 151936, False, flags=8) == 8192          # recompute backward
+    assert rows(300, 64, 100, True) == 384 and rows(300, 64, 100, True, chunk=200) == 256
+    assert rows(300, 64, 100, True, chunk=100000) == 384                # at most N rounded up
+    assert rows(300, 12, 100, True) == 0                                # H % 8 != 0
+
+
 @pytest.mark.parametrize("field,value", [("hidden", 0), ("vocab", 0), ("n_rows", -1), ("softcap", -1.0),
                                          ("reduction", 7), ("chunk_rows", -5), ("ld_h", 100)])
 def test_workspace_size_rejects_bad_params(L, field, value):
