@@ -330,16 +330,17 @@ def _traffic_key(args, w):
             + ("-tile128" if args.tile128 else ""))
 
 
-def recorded_traffic(workload, kernel: str):
+def recorded_traffic(workload, kernel: str, chunk_rows: int = 8192):
     """Per-launch dram__bytes_read.sum + dram__bytes_write.sum from the committed
-    ncu capture summary, or None when absent or taken on other kernel sources."""
+    ncu capture summary, or None when absent, taken on other kernel sources, or
+    taken with another number of rows per chunk (launches of another size)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if workload is None or not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_sha256") != kernel_source_hash():
+    if not e or e.get("source_sha256") != kernel_source_hash() or e.get("chunk_rows", 8192) != chunk_rows:
         return None
     return e["bytes_per_launch"]
 
@@ -415,6 +416,11 @@ def run_ours(args, w):
     step_peak = peaks["bf16_sustained"] * (TF32_OVER_BF16 if args.fp32 else 1.0)
     line = None
     if rank == 0:
+        chunk_used = flce.flce_chunk_rows(
+            w.n_rows, w.hidden, w.vocab,
+            mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
+            need_grad_W=w.mode == "fwd_bwd", chunk_rows=args.chunk_rows,
+            flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"])
         # roofline of the dominant kernel, from the per-launch events of the timed region
         gemm_flops = {"fwd_gemm_stats": 2.0 * w.n_rows * w.hidden * w.vocab,
                       "grad_h_gemm": 2.0 * w.n_rows * w.hidden * w.vocab,
@@ -432,7 +438,7 @@ def run_ours(args, w):
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": (f"bf16_tflops_sustained ({peaks['source']}) x 1.1/2.25 nominal tf32/bf16"
                                     if args.fp32 else f"bf16_tflops_sustained ({peaks['source']})"),
-                    "traffic": recorded_traffic(_traffic_key(args, w), dom),
+                    "traffic": recorded_traffic(_traffic_key(args, w), dom, chunk_used),
                     "traffic_unit": "bytes per launch (dram read + write, ncu)",
                     "algorithmic_flops_per_launch": per_launch_flops,
                     "avg_launch_ms": tms / n_launch}
@@ -449,11 +455,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "ms_per_step_median": statistics.median(per_step), "ms_per_step_min": min(per_step),
             "vs_baseline": None, "dtype": "f32 (tf32 tensor cores)" if args.fp32 else "bf16", "data": "synthetic",
-            "config": _config(w, args.chunk_rows, flce.flce_chunk_rows(
-                w.n_rows, w.hidden, w.vocab,
-                mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
-                need_grad_W=w.mode == "fwd_bwd", chunk_rows=args.chunk_rows,
-                flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"])),
+            "config": _config(w, args.chunk_rows, chunk_used),
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
             "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,

@@ -47,6 +47,19 @@ def test_each_variant_reports_its_own_capture():
     assert bench.recorded_traffic(None, "grad_W_gemm") is None
 
 
+def test_other_chunk_sizes_report_no_traffic():
+    """A capture holds launches of one chunk size; a line whose call chunks
+    differently (the frozen head's default of 9728 rows, say) gets none."""
+    rec = _recorded()
+    if rec["dsv3"]["fwd_gemm_stats"]["source_sha256"] != bench.kernel_source_hash():
+        return
+    assert bench.recorded_traffic("dsv3", "fwd_gemm_stats", 8192) is not None
+    assert bench.recorded_traffic("dsv3", "fwd_gemm_stats", 9728) is None
+    for key, kernels in rec.items():
+        if not key.startswith("_"):
+            assert all(e["chunk_rows"] == 8192 for e in kernels.values()), key
+
+
 def test_changed_kernels_report_no_traffic(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
     assert bench.recorded_traffic("dsv3", "fwd_gemm_stats") is None
