@@ -420,7 +420,8 @@ def run_ours(args, w):
             w.n_rows, w.hidden, w.vocab,
             mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
             need_grad_W=w.mode == "fwd_bwd", chunk_rows=args.chunk_rows,
-            flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"])
+            flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"],
+            dtype=torch.float32 if args.fp32 else torch.bfloat16)
         # roofline of the dominant kernel, from the per-launch events of the timed region
         gemm_flops = {"fwd_gemm_stats": 2.0 * w.n_rows * w.hidden * w.vocab,
                       "grad_h_gemm": 2.0 * w.n_rows * w.hidden * w.vocab,
@@ -476,7 +477,9 @@ def run_ours(args, w):
             "workspace_bytes": flce.flce_workspace_size(
                 w.n_rows, w.hidden, w.vocab, chunk_rows=args.chunk_rows,
                 mode=flce.FLCE_MODE_CE_ONLY if w.mode == "ce_only" else flce.FLCE_MODE_FORWARD_BACKWARD,
-                need_grad_W=w.mode == "fwd_bwd", flags=flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0),
+                need_grad_W=w.mode == "fwd_bwd",
+                flags=(flce.FLCE_FLAG_RECOMPUTE if args.low_memory else 0) | kw["flags"],
+                dtype=torch.float32 if args.fp32 else torch.bfloat16),
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -140,16 +140,19 @@ def _raise(rc: int, what: str):
 
 def flce_workspace_size(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_MODE_FORWARD_BACKWARD,
                         need_grad_h: bool = True, need_grad_W: bool = True, chunk_rows: int = 0,
-                        flags: int = 0) -> int:
-    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0)
+                        flags: int = 0, dtype=torch.bfloat16) -> int:
+    """Bytes of device workspace a call with these arguments needs (dtype: of h and W)."""
+    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0, 0,
+                _lib.FLCE_DTYPE_F32 if dtype == torch.float32 else _lib.FLCE_DTYPE_BF16)
     return int(_lib.lib().flce_workspace_size(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
 
 
 def flce_chunk_rows(n_rows: int, hidden: int, vocab: int, mode: int = FLCE_MODE_FORWARD_BACKWARD,
                     need_grad_h: bool = True, need_grad_W: bool = True, chunk_rows: int = 0,
-                    flags: int = 0) -> int:
+                    flags: int = 0, dtype=torch.bfloat16) -> int:
     """Rows per chunk a call with these arguments uses (the library's choice when chunk_rows is 0)."""
-    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0)
+    p = _params(n_rows, hidden, vocab, 0, 0, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0, 0,
+                _lib.FLCE_DTYPE_F32 if dtype == torch.float32 else _lib.FLCE_DTYPE_BF16)
     return int(_lib.lib().flce_chunk_rows(ctypes.byref(p), mode, int(need_grad_h), int(need_grad_W)))
 
 
