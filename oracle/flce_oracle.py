@@ -51,6 +51,9 @@ __all__ = [
     "oracle_rows",
     "oracle_grad_W_rows",
     "oracle_ce_logits",
+    "oracle_shard_partials",
+    "oracle_merge_shards",
+    "oracle_shard_grad_h",
 ]
 
 
@@ -302,3 +305,105 @@ def oracle_ce_logits(logits, labels, *, softcap: float = 0.0, out_mult: float = 
         acc = correct / n_valid
     return {"loss": loss, "token_accuracy": acc, "n_valid": n_valid, "correct": correct,
             "predicted": pred, "lse": lse, "row_loss": row_loss, "top2_gap": gap, "grad_logits": grad}
+
+
+def oracle_shard_partials(h, W, labels, offsets, *, softcap: float = 0.0, out_mult: float = 1.0,
+                          ignore_index: int = -100, block_rows: int = 256) -> dict:
+    """Per-row partials of each vocabulary shard of W, the quantities a
+    vocabulary-sharded head exchanges (the distributed DDP / FSDP runs of the
+    SpecForge DSpine PR, section Validation, split W by vocabulary rows).
+
+    offsets: S + 1 increasing vocab ids from 0 to V; shard k holds W's rows
+    [offsets[k], offsets[k+1]). For each shard k and row i, over j in the shard:
+        max[k, i]    = max_j s_ij
+        sumexp[k, i] = sum_j exp(s_ij - max[k, i])
+        argmax[k, i] = min { j : s_ij = max[k, i] }   (a global vocab id)
+        target[k, i] = s_{i, y_i} if y_i is in the shard, else 0
+    with s the capped logits of flce_oracle.
+    """
+    h = _f64(h)
+    W = _f64(W)
+    lab = _i64(labels)
+    off = [int(o) for o in offsets]
+    N = h.shape[0]
+    S = len(off) - 1
+    out = {k: np.zeros((S, N)) for k in ("max", "sumexp", "target")}
+    out["argmax"] = np.zeros((S, N), dtype=np.int64)
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        _, s = capped_logits(h[r0:r1], W, softcap, out_mult)
+        for k in range(S):
+            sk = s[:, off[k]:off[k + 1]]
+            mk = sk.max(axis=1)
+            out["max"][k, r0:r1] = mk
+            out["sumexp"][k, r0:r1] = np.exp(sk - mk[:, None]).sum(axis=1)
+            out["argmax"][k, r0:r1] = off[k] + sk.argmax(axis=1)
+            for i in range(r0, r1):
+                y = lab[i]
+                if y != ignore_index and off[k] <= y < off[k + 1]:
+                    out["target"][k, i] = s[i - r0, y]
+    return out
+
+
+def oracle_merge_shards(part: dict, labels, offsets, *, ignore_index: int = -100, reduction: str = "mean") -> dict:
+    """The batch outputs from every shard's partials (oracle_shard_partials):
+        M_i    = max_k max[k, i]
+        lse_i  = M_i + log sum_k sumexp[k, i] exp(max[k, i] - M_i)
+        pred_i = argmax[k*, i], k* the first (lowest-id) shard with max[k*, i] = M_i
+        l_i    = lse_i - target[k(y_i), i], k(y_i) the shard holding the label
+    and the loss and accuracy over the valid rows as in flce_oracle."""
+    lab = _i64(labels)
+    off = [int(o) for o in offsets]
+    mx = np.asarray(part["max"])
+    S, N = mx.shape
+    M = mx.max(axis=0)
+    lse = M + np.log((np.asarray(part["sumexp"]) * np.exp(mx - M[None, :])).sum(axis=0))
+    first = np.argmax(mx == M[None, :], axis=0)
+    pred = np.asarray(part["argmax"])[first, np.arange(N)]
+    valid = lab != ignore_index
+    row_loss = np.zeros(N)
+    for i in np.nonzero(valid)[0]:
+        k = max(kk for kk in range(S) if off[kk] <= lab[i])
+        row_loss[i] = lse[i] - part["target"][k][i]
+    n_valid = int(valid.sum())
+    correct = int(np.sum(valid & (pred == lab)))
+    total = float(row_loss[valid].sum())
+    if n_valid == 0:
+        loss, acc = 0.0, 0.0
+    else:
+        loss = total / n_valid if reduction == "mean" else total
+        acc = correct / n_valid
+    return {"loss": loss, "token_accuracy": acc, "n_valid": n_valid, "correct": correct, "predicted": pred,
+            "lse": lse, "row_loss": row_loss}
+
+
+def oracle_shard_grad_h(h, W, labels, lse, n_valid: int, v0: int, v1: int, *, softcap: float = 0.0,
+                        out_mult: float = 1.0, ignore_index: int = -100, reduction: str = "mean",
+                        grad_scale: float = 1.0, block_rows: int = 256) -> np.ndarray:
+    """One vocabulary shard's part of grad_h: m sum_{j in [v0, v1)} dz_ij W_j,
+    with dz as in flce_oracle from every row's full lse. Summed over shards
+    that tile [0, V) it is flce_oracle's grad_h."""
+    h = _f64(h)
+    W = _f64(W)
+    lab = _i64(labels)
+    lse = _f64(lse)
+    N, H = h.shape
+    valid = lab != ignore_index
+    coef = _coef(n_valid, reduction, grad_scale)
+    Wk = W[v0:v1]
+    out = np.zeros((N, H))
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        _, s = capped_logits(h[r0:r1], Wk, softcap, out_mult)
+        q = np.exp(s - lse[r0:r1, None])
+        lb = lab[r0:r1]
+        vb = valid[r0:r1]
+        for i in range(r1 - r0):
+            if vb[i] and v0 <= lb[i] < v1:
+                q[i, lb[i] - v0] -= 1.0
+        q *= coef
+        q[~vb] = 0.0
+        if softcap > 0.0:
+            q = q * (1.0 - (s / softcap) ** 2)
+        out[r0:r1] = out_mult * (q @ Wk)
+    return out

@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import flce_oracle, oracle_grad_W_rows, oracle_rows
+from oracle import (flce_oracle, oracle_ce_logits, oracle_grad_W_rows, oracle_merge_shards, oracle_rows,
+                    oracle_shard_grad_h, oracle_shard_partials)
 import workloads
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -464,3 +465,168 @@ def test_randomised_gradients_and_loss_against_autograd():
         np.testing.assert_array_equal(out["predicted"], pred)
 
     check()
+
+
+# --- top-2 gap: the rule that excuses near-tie rows from the predicted-token check ---
+# The gap of row i is (s1 - s2) / |s1|, s1 >= s2 the two largest capped logits
+# counted with multiplicity (a repeated maximum gives gap 0). These pins fix the
+# second-largest index (not the smallest or the maximum again), the absolute
+# value in the denominator, duplicates, and that the gap is taken on s = cap(m z),
+# not on z.
+def _gap_brute(s_row):
+    srt = sorted(s_row, reverse=True)
+    return (srt[0] - srt[1]) / abs(srt[0])
+
+
+def _logit_rows(c_rows):
+    """h = e_0 and W[j] = c_j e_0, so z_ij = c_ij exactly (one row per case)."""
+    c = np.asarray(c_rows, dtype=np.float64)
+    V = c.shape[1]
+    out = []
+    for row in c:
+        W = np.zeros((V, 3))
+        W[:, 0] = row
+        out.append((np.array([[1.0, 0.0, 0.0]]), W))
+    return out
+
+
+@pytest.mark.parametrize("case,expect", [
+    ([1.0, 5.0, 3.0, -2.0], 0.4),        # clear winner: (5 - 3) / 5
+    ([-3.0, -1.0, -2.0], 1.0),           # negative maximum: (-1 - -2) / |-1|
+    ([5.0, 5.0, 3.0], 0.0),              # repeated maximum counts twice
+    ([2.0, 7.0, 7.0, 7.0], 0.0),
+    ([0.25, -0.5, 0.125, 0.0], 0.5),     # (0.25 - 0.125) / 0.25
+])
+def test_top2_gap_closed_forms(case, expect):
+    (h, W), = _logit_rows([case])
+    for out in (flce_oracle(h, W, np.array([0]), need_grad_h=False, need_grad_W=False),
+                oracle_rows(h, W, np.array([0]), 1, need_grad_h=False),
+                oracle_ce_logits(np.array([case]), np.array([0]), need_grad=False)):
+        assert out["top2_gap"][0] == pytest.approx(expect, abs=1e-15)
+        assert out["predicted"][0] == int(np.argmax(case))
+
+
+def test_top2_gap_is_taken_on_capped_and_scaled_logits():
+    (h, W), = _logit_rows([[10.0, 20.0, -4.0]])
+    T, m = 5.0, 0.5
+    s = [T * math.tanh(m * c / T) for c in (10.0, 20.0, -4.0)]
+    out = flce_oracle(h, W, np.array([1]), softcap=T, out_mult=m, need_grad_h=False, need_grad_W=False)
+    assert out["top2_gap"][0] == pytest.approx(_gap_brute(s), rel=1e-14)
+    # on the raw z the gap would be (20 - 10) / 20 = 0.5, on m z also 0.5
+    assert abs(out["top2_gap"][0] - 0.5) > 0.1
+
+
+def test_top2_gap_exact_tie_between_identical_vocab_rows():
+    rng = np.random.default_rng(21)
+    N, H, V = 6, 5, 17
+    h = rng.standard_normal((N, H))
+    W = rng.standard_normal((V, H))
+    out0 = flce_oracle(h, W, np.zeros(N, dtype=np.int64), need_grad_h=False, need_grad_W=False)
+    # copy each row's winning vocab row to a higher index: an exact tie, gap 0,
+    # and the lowest index must still win
+    W2 = np.concatenate([W, W[out0["predicted"][:1]]], axis=0)
+    out = flce_oracle(h, W2, np.zeros(N, dtype=np.int64), need_grad_h=False, need_grad_W=False)
+    assert out["top2_gap"][0] == 0.0
+    assert out["predicted"][0] == out0["predicted"][0]
+
+
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (3.0, 0.5), (0.0, -1.5)])
+def test_top2_gap_brute_force_sorted_rows(T, m):
+    rng = np.random.default_rng(22)
+    N, H, V = 11, 4, 9
+    h = rng.standard_normal((N, H))
+    W = rng.standard_normal((V, H))
+    out = flce_oracle(h, W, np.zeros(N, dtype=np.int64), softcap=T, out_mult=m,
+                      need_grad_h=False, need_grad_W=False)
+    for i in range(N):
+        s = []
+        for j in range(V):
+            z = sum(m * h[i, k] * W[j, k] for k in range(H))
+            s.append(T * math.tanh(z / T) if T > 0 else z)
+        assert out["top2_gap"][i] == pytest.approx(_gap_brute(s), rel=1e-12, abs=1e-15)
+
+
+def test_top2_gap_single_column_vocab_is_infinite():
+    out = flce_oracle(np.ones((2, 3)), np.ones((1, 3)), np.array([0, -100]), need_grad_h=False, need_grad_W=False)
+    assert np.all(np.isinf(out["top2_gap"]))
+
+
+# --- vocabulary shards: per-shard partials, their merge, per-shard grad_h ------------
+def _torch_capped(h, W, T, m):
+    z = m * (torch.tensor(h) @ torch.tensor(W).T)
+    return T * torch.tanh(z / T) if T > 0 else z
+
+
+@pytest.mark.parametrize("offsets", [[0, 23], [0, 5, 13, 23], [0, 1, 2, 22, 23]])
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (4.0, 0.5)])
+def test_shard_partials_against_torch_slices(offsets, T, m):
+    N, H, V = 9, 6, 23
+    h, W, lab = _rand(N, H, V, 40, ign=2)
+    part = oracle_shard_partials(h, W, lab, offsets, softcap=T, out_mult=m)
+    s = _torch_capped(h, W, T, m)
+    for k in range(len(offsets) - 1):
+        sk = s[:, offsets[k]:offsets[k + 1]]
+        np.testing.assert_allclose(part["max"][k], sk.max(dim=1).values.numpy(), rtol=0, atol=1e-14)
+        lse_k = torch.logsumexp(sk, dim=1).numpy()
+        np.testing.assert_allclose(part["max"][k] + np.log(part["sumexp"][k]), lse_k, rtol=1e-14)
+        np.testing.assert_array_equal(part["argmax"][k], offsets[k] + sk.argmax(dim=1).numpy())
+        for i in range(N):
+            inside = lab[i] != -100 and offsets[k] <= lab[i] < offsets[k + 1]
+            assert part["target"][k][i] == pytest.approx(float(s[i, lab[i]]) if inside else 0.0, rel=1e-14, abs=0)
+
+
+@pytest.mark.parametrize("offsets", [[0, 23], [0, 5, 13, 23], [0, 11, 12, 23]])
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (4.0, 0.5)])
+def test_merged_shards_match_torch_on_the_full_vocabulary(offsets, T, m):
+    N, H, V = 12, 5, 23
+    h, W, lab = _rand(N, H, V, 41, ign=3)
+    part = oracle_shard_partials(h, W, lab, offsets, softcap=T, out_mult=m)
+    out = oracle_merge_shards(part, lab, offsets)
+    s = _torch_capped(h, W, T, m)
+    np.testing.assert_allclose(out["lse"], torch.logsumexp(s, dim=1).numpy(), rtol=1e-14)
+    np.testing.assert_array_equal(out["predicted"], s.argmax(dim=1).numpy())
+    ref = torch.nn.functional.cross_entropy(s, torch.tensor(lab), ignore_index=-100)
+    assert out["loss"] == pytest.approx(ref.item(), rel=1e-13)
+    assert out["n_valid"] == int((lab != -100).sum())
+
+
+def test_merged_shards_tie_across_shards_keeps_lowest_id():
+    # vocab row 3 (shard 0) copied to vocab row 17 (shard 2): an exact tie
+    # across shards for every row whose winner is row 3
+    N, H, V = 16, 4, 20
+    rng = np.random.default_rng(42)
+    h = rng.standard_normal((N, H))
+    W = rng.standard_normal((V, H))
+    W[3] = 3.0 * np.abs(W[3]).max() * np.sign(h.mean(axis=0))
+    W[17] = W[3]
+    lab = np.full(N, 17)
+    offsets = [0, 8, 12, 20]
+    out = oracle_merge_shards(oracle_shard_partials(h, W, lab, offsets), lab, offsets)
+    full = flce_oracle(h, W, lab, need_grad_h=False, need_grad_W=False)
+    assert np.sum(full["predicted"] == 3) >= 4
+    np.testing.assert_array_equal(out["predicted"], full["predicted"])
+    assert out["correct"] == 0
+
+
+@pytest.mark.parametrize("T,m", [(0.0, 1.0), (3.0, 0.5)])
+def test_shard_grad_h_parts_sum_to_autograd(T, m):
+    N, H, V = 7, 5, 19
+    h, W, lab = _rand(N, H, V, 43, ign=2)
+    ht = torch.tensor(h, requires_grad=True)
+    z = m * (ht @ torch.tensor(W).T)
+    s = T * torch.tanh(z / T) if T > 0 else z
+    torch.nn.functional.cross_entropy(s, torch.tensor(lab), ignore_index=-100).backward()
+    lse = torch.logsumexp(s.detach(), dim=1).numpy()
+    nv = int((lab != -100).sum())
+    offsets = [0, 4, 11, 19]
+    parts = [oracle_shard_grad_h(h, W, lab, lse, nv, offsets[k], offsets[k + 1], softcap=T, out_mult=m)
+             for k in range(3)]
+    np.testing.assert_allclose(sum(parts), ht.grad.numpy(), rtol=1e-10, atol=1e-14)
+    # a shard holding none of the labels contributes m sum_j p_ij W_j (T = 0) alone
+    if T == 0.0:
+        p = torch.softmax(s.detach(), dim=1).numpy()
+        k = 1
+        sel = (lab == -100) | (lab < offsets[k]) | (lab >= offsets[k + 1])
+        exp = m * (p[:, offsets[k]:offsets[k + 1]] @ W[offsets[k]:offsets[k + 1]]) / nv
+        exp[lab == -100] = 0.0
+        np.testing.assert_allclose(parts[k][sel], exp[sel], atol=1e-14)
