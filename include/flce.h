@@ -49,6 +49,15 @@
  *    gave up) are OR-ed into a status word in the workspace; read it with
  *    flce_get_status. On any error the outputs are unspecified.
  *  - Nothing traps, prints or throws across this boundary.
+ *  - The current CUDA device (cudaSetDevice) must be the device that owns
+ *    `stream` and every device pointer of the call: the library takes the SM
+ *    count, its one-time per-device kernel set-up and (flce_ce_only_noalloc)
+ *    its static scratch array from the current device.
+ *  - FLCE_ERR_TIMEOUT means a kernel gave up waiting and returned early. Its
+ *    own in-flight copies are drained under the same time limit, and if that
+ *    drain also runs out, copies may still land after the kernel has exited.
+ *    The outputs of such a call, and of work running beside it on the device,
+ *    are then undefined: synchronise, read the status, and discard them.
  */
 #ifndef FLCE_H
 #define FLCE_H
@@ -244,6 +253,58 @@ int flce_cross_entropy(const flce_params* p, const void* logits, int logits_dtyp
 int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_t n, const float* scale,
                         void* stream);
 
+/* ---------------------------------------------------------------- vocab-parallel
+ * The head's weight split by vocabulary rows over S shards, one per GPU (or run
+ * one after another on one GPU): shard k holds W's rows for vocab ids
+ * [o_k, o_{k+1}), 0 = o_0 < o_1 < ... < o_S = vocab_total, and sees all N rows
+ * of h and all labels (global vocab ids). This is the vocabulary-sharded form of
+ * the fused head for the distributed (DDP / FSDP) runs of the SpecForge DSpine
+ * PR (section Validation); each shard keeps its transients chunked as on the
+ * Liger-Kernel DeepSeek-V3 page (section Memory). One step is:
+ *   1. every shard: flce_vp_forward, its per-row partials (4 x N floats);
+ *   2. exchange: every shard obtains all S partial sets in shard order,
+ *      [S][4][N] (an all-gather: 16 bytes per row and shard cross GPUs);
+ *   3. every shard: flce_vp_backward, which merges them in shard order into the
+ *      loss, token accuracy, predicted tokens and lse (bit-identical on every
+ *      shard), then adds its own rows of grad_W and its part of grad_h, which
+ *      the caller sums over the shards (an all-reduce) and rounds.
+ * The backward recomputes the shard's logits per vocab slab, as
+ * FLCE_FLAG_RECOMPUTE does, so only the partials cross shards and no logits
+ * are kept between the calls: 8 N H V_k tensor flops per shard, transient
+ * memory O(C * vocab_slab + N). bf16 operands only (FLCE_ERR_UNSUPPORTED for
+ * fp32, FLCE_FLAG_SIMT_GEMM and FLCE_FLAG_KMAJOR_BWD).
+ * In both calls p->vocab is V_k, the shard's row count, and W_shard is
+ * [V_k, ld_w]; labels are checked against [0, vocab_total) (FLCE_ERR_LABEL).
+ * Partials, row i (float words, field stride N): [0] max of s over the shard,
+ * [1] sum of exp(s - max), [2] argmax as the bit pattern of an int32 global
+ * vocab id (the lowest on ties), [3] s at the label if the label is in the
+ * shard, else 0. */
+
+/* Workspace bytes of flce_vp_forward (backward = 0) or flce_vp_backward
+ * (backward = 1; need_grad_h / need_grad_W as that call will have them). The
+ * backward's includes 4 bytes of lse per row (all N rows). 0 if invalid. */
+size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_h, int need_grad_W);
+
+/* Forward of one shard: writes partials [4][N] (device). FLCE_ERR_ARG when
+ * [vocab_offset, vocab_offset + V_k) is not inside [0, vocab_total). */
+int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, const void* h,
+                    const void* W_shard, const int64_t* labels, float* partials, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Backward of one shard, given every shard's partials all_partials [S][4][N]
+ * (device) and the host table shard_offsets [S + 1] (S <= 64; FLCE_ERR_ARG if
+ * it is not increasing from 0 to vocab_total or does not contain this shard).
+ * Writes loss and token_accuracy (device floats; token_accuracy, predicted
+ * [N] int64 and row_lse [N] nullable) exactly as flce_forward would for the
+ * whole vocabulary, up to the order of the fp32 merge. grad_h_partial: fp32
+ * [N, H], ACCUMULATED (+= this shard's m dz_k W_k); summed over all shards it
+ * is grad_h. grad_W_shard: fp32 [V_k, H], ACCUMULATED. Either may be NULL. */
+int flce_vp_backward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, int n_shards,
+                     const int64_t* shard_offsets, const float* all_partials, const void* h, const void* W_shard,
+                     const int64_t* labels, float* loss, float* token_accuracy, int64_t* predicted,
+                     float* row_lse, float* grad_h_partial, float* grad_W_shard, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream` and returns (in *status) the device status word of the
  * last call that used this workspace: 0 or FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT.
  * Return value: FLCE_OK or FLCE_ERR_ARG / FLCE_ERR_CUDA. */
@@ -260,7 +321,7 @@ int64_t flce_launch_count(void);
  * flce_profile_begin(0) stops. flce_profile_read synchronises the recorded
  * events and fills, for kernel ids 0..n-1, the launch count and the summed
  * milliseconds; it returns the number of kernel ids (FLCE_NUM_KERNELS). */
-#define FLCE_NUM_KERNELS 15
+#define FLCE_NUM_KERNELS 16
 int flce_profile_begin(int enable);
 int flce_profile_read(int64_t* launches, double* total_ms, int n);
 const char* flce_kernel_name(int id);

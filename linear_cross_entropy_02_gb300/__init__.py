@@ -32,6 +32,8 @@ __all__ = [
     "flce_scale_gradient", "flce_workspace_size", "flce_chunk_rows", "flce_chunk_rows_for_budget", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
     "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
+    "flce_vp_forward", "flce_vp_backward", "vocab_parallel_linear_cross_entropy", "vp_shard_table",
+    "vp_gather_partials", "vp_reduce_grad_h",
 ]
 
 _REDUCTIONS = {"mean": FLCE_REDUCTION_MEAN, "sum": FLCE_REDUCTION_SUM, "none": _lib.FLCE_REDUCTION_NONE}
@@ -133,6 +135,14 @@ def flce_release_workspaces() -> None:
     _workspaces.clear()
 
 
+def _native(device: torch.device, name: str, *args):
+    """Calls a C entry point with `device` current. The library takes the SM
+    count, its per-device setup and the static scratch array from the current
+    device, so it must be the device that owns the tensors and the stream."""
+    with torch.cuda.device(device):
+        return getattr(_lib.lib(), name)(*args)
+
+
 def _raise(rc: int, what: str):
     if rc != 0:
         raise FlceError(rc, what)
@@ -182,7 +192,7 @@ def flce_ce_only(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, 
                                          chunk_rows, flags, timeout_ns, FLCE_MODE_CE_ONLY, False, False)
     loss = torch.empty((), dtype=torch.float32, device=h.device)
     acc = torch.empty((), dtype=torch.float32, device=h.device)
-    rc = _lib.lib().flce_ce_only(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(h.device, "flce_ce_only", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                  _ptr(ws), nbytes, _stream_handle(h.device))
     _raise(rc, "flce_ce_only")
     return loss, acc
@@ -206,7 +216,7 @@ def flce_ce_only_noalloc(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_inde
     loss = torch.empty((), dtype=torch.float32, device=dev)
     acc = torch.empty((), dtype=torch.float32, device=dev)
     status = torch.zeros((), dtype=torch.int32, device=dev)
-    rc = _lib.lib().flce_ce_only_noalloc(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(dev, "flce_ce_only_noalloc", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                          _ptr(status), _stream_handle(dev))
     _raise(rc, "flce_ce_only_noalloc")
     return loss, acc, status
@@ -223,7 +233,7 @@ def flce_forward(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_index=-100, 
     acc = torch.empty((), dtype=torch.float32, device=dev)
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
     lse = torch.empty(h2.shape[0], dtype=torch.float32, device=dev) if return_lse else None
-    rc = _lib.lib().flce_forward(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(dev, "flce_forward", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                  _ptr(pred), _ptr(lse), _ptr(ws), nbytes, _stream_handle(dev))
     _raise(rc, "flce_forward")
     lead = h.shape[:-1]
@@ -256,7 +266,7 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
     acc = torch.empty((), dtype=torch.float32, device=dev)
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
     gh = torch.empty((h2.shape[0], W.shape[1]), dtype=h2.dtype, device=dev) if need_grad_h else None
-    rc = _lib.lib().flce_forward_backward(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(dev, "flce_forward_backward", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                           _ptr(pred), _ptr(gh), _ptr(grad_W), _ptr(ws), nbytes,
                                           _stream_handle(dev))
     _raise(rc, "flce_forward_backward")
@@ -264,6 +274,163 @@ def flce_forward_backward(h, W, labels, *, grad_W: Optional[torch.Tensor] = None
     return {"loss": loss, "token_accuracy": acc,
             "predicted": None if pred is None else pred.view(lead),
             "grad_h": None if gh is None else gh.view(h.shape), "grad_W": grad_W}
+
+
+# ---------------------------------------------------------------- vocab-parallel
+def _vp_params(h2, W, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags, timeout_ns,
+               vocab_slab=0):
+    return _params(h2.shape[0], W.shape[1], W.shape[0], h2.stride(0), W.stride(0), softcap, out_mult, ignore_index,
+                   reduction, grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _dtype_code(h2))
+
+
+def flce_vp_forward(h, W_shard, labels, vocab_offset: int, vocab_total: int, *, softcap=0.0, out_mult=1.0,
+                    ignore_index=-100, chunk_rows=0, flags=0, timeout_ns=0) -> torch.Tensor:
+    """Forward of one vocab shard (W_shard holds the rows of vocab ids
+    [vocab_offset, vocab_offset + V_k) of vocab_total): returns this shard's
+    per-row partials, an fp32 [4, N] CUDA tensor (max, sum of exp, argmax id
+    as int32 bits, label logit or 0)."""
+    _check(h, W_shard, labels)
+    H = W_shard.shape[1]
+    h2 = _rows2d(h, H)
+    if W_shard.stride(1) != 1 or W_shard.stride(0) % 8 != 0 or W_shard.data_ptr() % 16 != 0:
+        W_shard = W_shard.contiguous()
+    lab = labels.reshape(-1).contiguous()
+    p = _vp_params(h2, W_shard, softcap, out_mult, ignore_index, "mean", 1.0, chunk_rows, flags, timeout_ns)
+    nbytes = _native(h.device, "flce_vp_workspace_size", ctypes.byref(p), 0, 0, 0)
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_vp_workspace_size")
+    ws = _workspace(h.device, nbytes)
+    part = torch.empty((4, h2.shape[0]), dtype=torch.float32, device=h.device)
+    rc = _native(h.device, "flce_vp_forward", ctypes.byref(p), int(vocab_offset), int(vocab_total), _ptr(h2),
+                 _ptr(W_shard), _ptr(lab), _ptr(part), _ptr(ws), nbytes, _stream_handle(h.device))
+    _raise(rc, "flce_vp_forward")
+    return part
+
+
+def flce_vp_backward(h, W_shard, labels, all_partials: torch.Tensor, shard_offsets, vocab_offset: int,
+                     vocab_total: int, *, grad_h_partial: Optional[torch.Tensor] = None,
+                     grad_W: Optional[torch.Tensor] = None, softcap=0.0, out_mult=1.0, ignore_index=-100,
+                     reduction="mean", grad_scale=1.0, return_predicted=True, return_lse=False, chunk_rows=0,
+                     vocab_slab=0, flags=0, timeout_ns=0) -> dict:
+    """Backward of one vocab shard given every shard's partials ([S, 4, N], in
+    shard order) and the shard table (S + 1 vocab offsets). grad_h_partial
+    (fp32 [N, H]) and grad_W (this shard's fp32 [V_k, H]) are ACCUMULATED in
+    place when given. Returns dict(loss, token_accuracy, predicted, lse)."""
+    _check(h, W_shard, labels)
+    H = W_shard.shape[1]
+    h2 = _rows2d(h, H)
+    if W_shard.stride(1) != 1 or W_shard.stride(0) % 8 != 0 or W_shard.data_ptr() % 16 != 0:
+        W_shard = W_shard.contiguous()
+    lab = labels.reshape(-1).contiguous()
+    N = h2.shape[0]
+    S = len(shard_offsets) - 1
+    if (all_partials.dtype != torch.float32 or tuple(all_partials.shape) != (S, 4, N)
+            or all_partials.device != h.device):
+        raise ValueError("all_partials must be an fp32 [S, 4, N] tensor on h's device")
+    all_partials = all_partials.contiguous()
+    for name, t, shape in (("grad_h_partial", grad_h_partial, (N, H)), ("grad_W", grad_W, tuple(W_shard.shape))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous()
+                              or t.device != h.device):
+            raise ValueError(f"{name} must be a contiguous fp32 {shape} tensor on h's device")
+    p = _vp_params(h2, W_shard, softcap, out_mult, ignore_index, reduction, grad_scale, chunk_rows, flags,
+                   timeout_ns, vocab_slab)
+    nbytes = _native(h.device, "flce_vp_workspace_size", ctypes.byref(p), 1, int(grad_h_partial is not None),
+                     int(grad_W is not None))
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_vp_workspace_size")
+    ws = _workspace(h.device, nbytes)
+    dev = h.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    pred = torch.empty(N, dtype=torch.int64, device=dev) if return_predicted else None
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if return_lse else None
+    offs = (ctypes.c_int64 * (S + 1))(*[int(o) for o in shard_offsets])
+    rc = _native(dev, "flce_vp_backward", ctypes.byref(p), int(vocab_offset), int(vocab_total), S, offs,
+                 _ptr(all_partials), _ptr(h2), _ptr(W_shard), _ptr(lab), _ptr(loss), _ptr(acc), _ptr(pred), _ptr(lse),
+                 _ptr(grad_h_partial), _ptr(grad_W), _ptr(ws), nbytes, _stream_handle(dev))
+    _raise(rc, "flce_vp_backward")
+    lead = h.shape[:-1]
+    return {"loss": loss, "token_accuracy": acc, "predicted": None if pred is None else pred.view(lead),
+            "lse": None if lse is None else lse.view(lead)}
+
+
+def _world(group) -> int:
+    """Ranks in `group` (None: the default group), 1 without torch.distributed."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return 1
+    return dist.get_world_size(group)
+
+
+def vp_shard_table(vocab_offset: int, vocab_shard: int, group=None):
+    """(offsets, order): the S + 1 vocab offsets of the shards of `group` (None:
+    the default group) in vocab order, and the ranks in that order, from every
+    rank's (offset, size). The shards must tile [0, vocab_total) without gaps
+    or overlap."""
+    import torch.distributed as dist
+    mine = torch.tensor([int(vocab_offset), int(vocab_shard)], dtype=torch.int64)
+    if _world(group) == 1:
+        table = [mine]
+    else:
+        table = [torch.empty_like(mine) for _ in range(_world(group))]
+        dist.all_gather(table, mine, group=group)
+    rows = sorted((int(t[0]), int(t[1]), r) for r, t in enumerate(table))
+    offsets, order = [0], []
+    for off, size, r in rows:
+        if off != offsets[-1] or size <= 0:
+            raise ValueError(f"vocab shards do not tile the vocabulary: {[(o, s) for o, s, _ in rows]}")
+        offsets.append(off + size)
+        order.append(r)
+    return offsets, order
+
+
+def vp_gather_partials(partials: torch.Tensor, order, group=None) -> torch.Tensor:
+    """Every rank's [4, N] partials gathered and put in vocab order ([S, 4, N])."""
+    import torch.distributed as dist
+    if _world(group) == 1:
+        return partials.unsqueeze(0)
+    W = _world(group)
+    out = torch.empty((W, *partials.shape), dtype=partials.dtype, device=partials.device)
+    dist.all_gather(list(out.unbind(0)), partials.contiguous(), group=group)
+    return out[torch.as_tensor(order, device=out.device)].contiguous()
+
+
+def vp_reduce_grad_h(grad_h_partial: torch.Tensor, group=None) -> torch.Tensor:
+    """Sums the shards' fp32 grad_h parts over `group` (in place)."""
+    import torch.distributed as dist
+    if _world(group) > 1:
+        dist.all_reduce(grad_h_partial, op=dist.ReduceOp.SUM, group=group)
+    return grad_h_partial
+
+
+def vocab_parallel_linear_cross_entropy(h, W_shard, labels, vocab_offset: int, *, group=None,
+                                        grad_W: Optional[torch.Tensor] = None, need_grad_h=True, softcap=0.0,
+                                        out_mult=1.0, ignore_index=-100, reduction="mean", grad_scale=1.0,
+                                        chunk_rows=0, vocab_slab=0) -> dict:
+    """The fused head with W split by vocabulary rows over the ranks of
+    `group` (one shard per rank, any order): shard forward, all-gather of the
+    per-row partials (16 bytes per row and rank), shard backward, all-reduce of
+    the fp32 grad_h parts, rounded to h's dtype by the library's kernel. Every
+    rank gets the same loss, token accuracy and predictions; grad_W (this
+    rank's fp32 [V_k, H], optional) is accumulated in place."""
+    offsets, order = vp_shard_table(vocab_offset, W_shard.shape[0], group)
+    V = offsets[-1]
+    part = flce_vp_forward(h, W_shard, labels, vocab_offset, V, softcap=softcap, out_mult=out_mult,
+                           ignore_index=ignore_index, chunk_rows=chunk_rows)
+    allp = vp_gather_partials(part, order, group)
+    gh32 = None
+    if need_grad_h:
+        gh32 = torch.zeros((h.reshape(-1, h.shape[-1]).shape[0], h.shape[-1]), dtype=torch.float32, device=h.device)
+    out = flce_vp_backward(h, W_shard, labels, allp, offsets, vocab_offset, V, grad_h_partial=gh32, grad_W=grad_W,
+                           softcap=softcap, out_mult=out_mult, ignore_index=ignore_index, reduction=reduction,
+                           grad_scale=grad_scale, chunk_rows=chunk_rows, vocab_slab=vocab_slab)
+    gh = None
+    if gh32 is not None:
+        vp_reduce_grad_h(gh32, group)
+        gh = flce_scale_gradient(gh32, None, out_dtype=h.dtype).view(h.shape)
+    out["grad_h"] = gh
+    out["grad_W"] = grad_W
+    return out
 
 
 _copy_streams: dict = {}
@@ -329,8 +496,8 @@ def flce_forward_backward_from_host(h, W, labels, *, grad_W: Optional[torch.Tens
     acc = torch.empty((), dtype=torch.float32).pin_memory()
     pred = torch.empty(h2.shape[0], dtype=torch.int64, device=dev) if return_predicted else None
     gh = torch.empty((h2.shape[0], H), dtype=W.dtype, device=dev) if need_grad_h else None
-    rc = _lib.lib().flce_forward_backward_from_host(
-        ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc), _ptr(pred), _ptr(gh), _ptr(grad_W),
+    rc = _native(
+        dev, "flce_forward_backward_from_host", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc), _ptr(pred), _ptr(gh), _ptr(grad_W),
         _ptr(ws), nbytes, _stream_handle(dev), ctypes.c_void_p(cs.cuda_stream))
     _raise(rc, "flce_forward_backward_from_host")
     lead = h.shape[:-1]
@@ -349,7 +516,7 @@ def flce_ce_only_from_host(h, W, labels, *, softcap=0.0, out_mult=1.0, ignore_in
                                                  False, False)
     loss = torch.empty((), dtype=torch.float32).pin_memory()
     acc = torch.empty((), dtype=torch.float32).pin_memory()
-    rc = _lib.lib().flce_ce_only_from_host(ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(W.device, "flce_ce_only_from_host", ctypes.byref(p), _ptr(h2), _ptr(W), _ptr(lab), _ptr(loss), _ptr(acc),
                                            _ptr(ws), nbytes, _stream_handle(W.device),
                                            ctypes.c_void_p(cs.cuda_stream))
     _raise(rc, "flce_ce_only_from_host")
@@ -396,7 +563,7 @@ def flce_cross_entropy(logits, labels, *, softcap=0.0, out_mult=1.0, ignore_inde
     if need_grad:
         grad = x if grad_in_place else torch.empty_like(x)
     dt = _lib.FLCE_DTYPE_BF16 if x.dtype == torch.bfloat16 else _lib.FLCE_DTYPE_F32
-    rc = _lib.lib().flce_cross_entropy(ctypes.byref(p), _ptr(x), dt, x.stride(0), _ptr(lab), _ptr(loss), _ptr(acc),
+    rc = _native(dev, "flce_cross_entropy", ctypes.byref(p), _ptr(x), dt, x.stride(0), _ptr(lab), _ptr(loss), _ptr(acc),
                                        _ptr(pred), _ptr(row_loss), _ptr(rs), _ptr(grad), _ptr(ws), nbytes,
                                        _stream_handle(dev))
     _raise(rc, "flce_cross_entropy")
@@ -427,7 +594,7 @@ def flce_scale_gradient(x: torch.Tensor, scale: Optional[torch.Tensor] = None, *
         out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
     elif out.dtype != out_dtype or out.shape != x.shape or not out.is_contiguous() or out.device != x.device:
         raise ValueError("out must be a contiguous tensor of x's shape and device in out_dtype")
-    rc = _lib.lib().flce_scale_gradient(_ptr(x), _dtype_code(x), _ptr(out), _dtype_code(out), x.numel(),
+    rc = _native(x.device, "flce_scale_gradient", _ptr(x), _dtype_code(x), _ptr(out), _dtype_code(out), x.numel(),
                                         _ptr(scale), _stream_handle(x.device))
     _raise(rc, "flce_scale_gradient")
     return out
@@ -525,7 +692,7 @@ def flce_get_status(device=None) -> int:
     if ws is None:
         return 0
     st = ctypes.c_int32(0)
-    _raise(_lib.lib().flce_get_status(_ptr(ws), _stream_handle(dev), ctypes.byref(st)), "flce_get_status")
+    _raise(_native(dev, "flce_get_status", _ptr(ws), _stream_handle(dev), ctypes.byref(st)), "flce_get_status")
     return int(st.value)
 
 

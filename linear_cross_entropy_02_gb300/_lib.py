@@ -38,13 +38,13 @@ FLCE_FLAG_RECOMPUTE = 8
 FLCE_FLAG_TILE128 = 16
 FLCE_FLAG_TILE256 = 32
 
-FLCE_NUM_KERNELS = 15
+FLCE_NUM_KERNELS = 16
 
 EXPORTED = [
     "flce_default_params", "flce_workspace_size", "flce_chunk_rows", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",
     "flce_forward_backward", "flce_forward_backward_from_host", "flce_ce_only_from_host", "flce_cross_entropy",
     "flce_scale_gradient", "flce_get_status", "flce_status_string", "flce_launch_count", "flce_profile_begin",
-    "flce_profile_read", "flce_kernel_name",
+    "flce_profile_read", "flce_kernel_name", "flce_vp_workspace_size", "flce_vp_forward", "flce_vp_backward",
 ]
 
 
@@ -133,6 +133,14 @@ def lib() -> ctypes.CDLL:
         L.flce_profile_read.restype = ctypes.c_int
         L.flce_kernel_name.argtypes = [ctypes.c_int]
         L.flce_kernel_name.restype = ctypes.c_char_p
+        L.flce_vp_workspace_size.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.flce_vp_workspace_size.restype = _sz
+        L.flce_vp_forward.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.flce_vp_forward.restype = ctypes.c_int
+        L.flce_vp_backward.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int64), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _vp, _vp, _vp, _sz, _vp]
+        L.flce_vp_backward.restype = ctypes.c_int
         _lib = L
         return L
 

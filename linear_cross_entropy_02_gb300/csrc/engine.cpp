@@ -77,25 +77,28 @@ struct LaunchScope {
 const char* const kKernelNames[FLCE_NUM_KERNELS] = {
     "prologue", "fwd_gemm_stats", "merge", "dlogits", "grad_h_gemm",
     "grad_W_gemm", "transpose_W", "transpose_h", "finish", "simt_stats",
-    "ce_stats", "ce_grad", "recompute_dz_gemm", "convert_grad_h", "scale_gradient"};
+    "ce_stats", "ce_grad", "recompute_dz_gemm", "convert_grad_h", "scale_gradient", "vp_merge"};
 
 // ------------------------------------------------------------ device info
-int g_sm_count[kMaxDevices] = {0};
-int g_cc[kMaxDevices] = {0};
+// Per-device cache of the SM count and compute capability, packed into one
+// atomic word (cc << 16 | sms; 0 = not yet queried) so that host threads
+// making their first calls at once neither race nor see half an entry.
+std::atomic<uint32_t> g_dev_info[kMaxDevices] = {};
 
 int device_info(int* sms, int* cc) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLCE_ERR_CUDA;
-  if (g_sm_count[dev] == 0) {
+  uint32_t v = g_dev_info[dev].load(std::memory_order_acquire);
+  if (v == 0) {
     int n = 0, major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FLCE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
-    g_cc[dev] = major * 10 + minor;
-    g_sm_count[dev] = n;
+    v = (static_cast<uint32_t>(major * 10 + minor) << 16) | (static_cast<uint32_t>(n) & 0xffffu);
+    g_dev_info[dev].store(v, std::memory_order_release);
   }
-  *sms = g_sm_count[dev];
-  *cc = g_cc[dev];
+  *sms = static_cast<int>(v & 0xffffu);
+  *cc = static_cast<int>(v >> 16);
   return FLCE_OK;
 }
 
@@ -374,6 +377,12 @@ struct Call {
   // copy_stream; loss / acc are then host pointers written at the end
   bool host_in = false;
   cudaStream_t copy_stream = nullptr;
+  // vocab shard (flce_vp_forward): W holds vocab ids [vocab_offset,
+  // vocab_offset + p->vocab) of vocab_total; the per-row partials go to
+  // shard_partials ([4][N]) instead of the loss and predictions
+  int64_t vocab_offset = 0;
+  int64_t vocab_total = 0;
+  float* shard_partials = nullptr;
 };
 
 int run_f32(const Norm& n, const Call& c);
@@ -442,6 +451,126 @@ struct HostStaging {
 };
 
 
+// Recompute backward of one chunk of rows over vocab slabs (the low-memory
+// mode, and each shard of the vocab-parallel backward): per slab of W's rows,
+// z is recomputed on the tensor cores and the EPI_DZ epilogue forms bf16
+// dlogits from it with the rows' lse; then grad_h += m dz W_slab (fp32
+// reduce-add into gh_acc) and grad_W_slab += m dz^T h_c.
+struct SlabArgs {
+  int rows, H, V, slab;
+  int col_base;              // vocab id of W's row 0 (the shard offset)
+  int h_row0;                // row of map_hc holding the chunk's first row
+  const CUtensorMap* map_hc; // h (K-major A of the recompute GEMM)
+  const CUtensorMap* map_w;  // W (K-major B)
+  const uint16_t* h_c;       // the chunk's rows of h, row stride ld_hc
+  int64_t ld_hc;
+  const uint16_t* W;
+  int64_t ld_w;
+  const int64_t* labels;     // the chunk's labels
+  const float* lse;          // the chunk's lse
+  const Header* hdr;
+  uint16_t* dz;              // [rows][slab] bf16 workspace
+  float* gh_acc;             // [rows][H] fp32, accumulated; null: no grad_h
+  float* grad_W;             // [V][H] fp32, accumulated; null: frozen
+  const flce_params* p;
+  float inv_cap;
+  uint64_t timeout;
+  int sms;
+};
+
+int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
+  const flce_params& p = *a.p;
+  Header* hdr = const_cast<Header*>(a.hdr);
+  auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, a.sms); };
+  const int rows = a.rows, H = a.H, V = a.V, slab = a.slab;
+  for (int v0 = 0; v0 < V; v0 += slab) {
+    const int vs = std::min(slab, V - v0);
+    GemmParams r{};
+    std::memset(&r, 0, sizeof(r));
+    r.M = rows;
+    r.N = vs;
+    r.K = H;
+    r.m_tiles = (rows + kBM - 1) / kBM;
+    r.n_tiles = (vs + kBN - 1) / kBN;
+    r.k_iters = (H + kBK - 1) / kBK;
+    r.group_m = std::min(r.m_tiles, 16);
+    r.a_row0 = a.h_row0;
+    r.b_row0 = v0;
+    r.alpha = p.out_mult;
+    r.M_valid = rows;
+    r.N_valid = vs;
+    r.softcap = p.softcap;
+    r.inv_softcap = a.inv_cap;
+    r.labels = a.labels;
+    r.ignore_index = p.ignore_index;
+    r.out = a.dz;
+    r.ldo = slab;
+    r.lse = a.lse;
+    r.hdr = hdr;
+    r.grad_scale = p.grad_scale;
+    r.reduction = p.reduction;
+    r.col0 = a.col_base + v0;
+    r.status = &hdr->status;
+    r.timeout_ns = a.timeout;
+    FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), a.map_hc, a.map_w, nullptr, r,
+                                                 std::min(r.m_tiles * r.n_tiles, a.sms), stream));
+    if (a.gh_acc) {
+      // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
+      CUtensorMap map_a, map_b;
+      if (!encode_bf16(&map_a, a.dz, vs, rows, slab, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_bf16(&map_b, a.W + static_cast<int64_t>(v0) * a.ld_w, H, vs, a.ld_w, 64))
+        return FLCE_ERR_UNSUPPORTED;
+      GemmParams b{};
+      std::memset(&b, 0, sizeof(b));
+      b.M = rows;
+      b.N = H;
+      b.K = vs;
+      b.m_tiles = (rows + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (vs + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 8);
+      b.alpha = p.out_mult;
+      b.M_valid = rows;
+      b.N_valid = H;
+      b.out = a.gh_acc;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = a.timeout;
+      CUtensorMap map_o;
+      if (!encode_f32_out(&map_o, a.gh_acc, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
+      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
+                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream));
+    }
+    if (a.grad_W) {
+      // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
+      CUtensorMap map_a, map_b;
+      if (!encode_bf16(&map_a, a.dz, vs, rows, slab, 64)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_bf16(&map_b, a.h_c, H, rows, a.ld_hc, 64)) return FLCE_ERR_UNSUPPORTED;
+      GemmParams b{};
+      std::memset(&b, 0, sizeof(b));
+      b.M = vs;
+      b.N = H;
+      b.K = rows;
+      b.m_tiles = (vs + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (rows + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = vs;
+      b.N_valid = H;
+      b.out = a.grad_W + static_cast<int64_t>(v0) * H;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = a.timeout;
+      CUtensorMap map_o;
+      if (!encode_f32_out(&map_o, a.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
+      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
+                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream));
+    }
+  }
+  return FLCE_OK;
+}
+
 int run(const flce_params* params, const Call& c) {
   Norm n;
   int rc = normalise(params, &n);
@@ -450,7 +579,8 @@ int run(const flce_params* params, const Call& c) {
   const flce_params& p = n.p;
   const bool gh = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_h != nullptr;
   const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
-  if (!c.loss || !c.ws || !c.W) return FLCE_ERR_ARG;
+  const bool shard = c.shard_partials != nullptr;
+  if ((!c.loss && !shard) || !c.ws || !c.W) return FLCE_ERR_ARG;
   if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
   if (!aligned16(c.ws) || (!c.host_in && c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
   if (gh && !aligned16(c.grad_h)) return FLCE_ERR_ALIGN;
@@ -508,7 +638,8 @@ int run(const flce_params* params, const Call& c) {
       return FLCE_ERR_CUDA;
   }
 
-  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
+  const int64_t vocab_total = c.vocab_total > 0 ? c.vocab_total : p.vocab;
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, vocab_total, p.ignore_index, hdr, stream));
 
   CUtensorMap map_h, map_w, map_wt;
   if (!simt && N > 0) {
@@ -575,6 +706,7 @@ int run(const flce_params* params, const Call& c) {
     g.status = &hdr->status;
     g.timeout_ns = timeout;
     g.debug_flags = p.flags;
+    g.col0 = static_cast<int>(c.vocab_offset);
     const bool store = L.need_z;
     g.store_hint = store ? 1 : 0;
     if (simt) {
@@ -605,6 +737,12 @@ int run(const flce_params* params, const Call& c) {
     mp.block_loss = reinterpret_cast<double*>(ws + L.off_bl);
     mp.block_correct = reinterpret_cast<int64_t*>(ws + L.off_bc);
     mp.hdr = hdr;
+    if (shard) {
+      mp.shard_out = c.shard_partials + r0;
+      mp.ld_shard = p.n_rows;
+      mp.vocab_offset = c.vocab_offset;
+      mp.vocab_shard = p.vocab;
+    }
     FLCE_LAUNCH(K_MERGE, launch_merge(mp, stream));
 
     if (!gh && !gw) continue;
@@ -614,94 +752,31 @@ int run(const flce_params* params, const Call& c) {
       // cores with dlogits formed in the epilogue, then both backward GEMMs.
       float* gh32 = L.need_gh32 ? reinterpret_cast<float*>(ws + L.off_gh32) : nullptr;
       if (gh32 && cudaMemsetAsync(gh32, 0, sizeof(float) * rows * H, stream) != cudaSuccess) return FLCE_ERR_CUDA;
-      const int slab = static_cast<int>(L.slab);
-      for (int v0 = 0; v0 < V; v0 += slab) {
-        const int vs = std::min(slab, V - v0);
-        GemmParams r{};
-        std::memset(&r, 0, sizeof(r));
-        r.M = rows;
-        r.N = vs;
-        r.K = H;
-        r.m_tiles = (rows + kBM - 1) / kBM;
-        r.n_tiles = (vs + kBN - 1) / kBN;
-        r.k_iters = (H + kBK - 1) / kBK;
-        r.group_m = std::min(r.m_tiles, 16);
-        r.a_row0 = h_row0;
-        r.b_row0 = v0;
-        r.alpha = p.out_mult;
-        r.M_valid = rows;
-        r.N_valid = vs;
-        r.softcap = p.softcap;
-        r.inv_softcap = inv_cap;
-        r.labels = lab_c;
-        r.ignore_index = p.ignore_index;
-        r.out = dz;
-        r.ldo = slab;
-        r.lse = lse;
-        r.hdr = hdr;
-        r.grad_scale = p.grad_scale;
-        r.reduction = p.reduction;
-        r.col0 = v0;
-        r.status = &hdr->status;
-        r.timeout_ns = timeout;
-        FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), &map_hc, &map_w, nullptr, r,
-                                                     std::min(r.m_tiles * r.n_tiles, sms), stream));
-        if (gh) {
-          // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
-          CUtensorMap map_a, map_b;
-          if (!encode_bf16(&map_a, dz, vs, rows, slab, kBM)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, static_cast<const uint16_t*>(c.W) + static_cast<int64_t>(v0) * n.ld_w, H, vs,
-                           n.ld_w, 64))
-            return FLCE_ERR_UNSUPPORTED;
-          GemmParams b{};
-          std::memset(&b, 0, sizeof(b));
-          b.M = rows;
-          b.N = H;
-          b.K = vs;
-          b.m_tiles = (rows + kBM - 1) / kBM;
-          b.n_tiles = (H + kBN - 1) / kBN;
-          b.k_iters = (vs + kBK - 1) / kBK;
-          b.group_m = std::min(b.m_tiles, 8);
-          b.alpha = p.out_mult;
-          b.M_valid = rows;
-          b.N_valid = H;
-          b.out = gh32;
-          b.ldo = H;
-          b.status = &hdr->status;
-          b.timeout_ns = timeout;
-          CUtensorMap map_o;
-          if (!encode_f32_out(&map_o, gh32, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-          FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                                   std::min(b.m_tiles * b.n_tiles, sms), stream));
-        }
-        if (gw) {
-          // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
-          CUtensorMap map_a, map_b;
-          if (!encode_bf16(&map_a, dz, vs, rows, slab, 64)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, h_c, H, rows, ld_hc, 64))
-            return FLCE_ERR_UNSUPPORTED;
-          GemmParams b{};
-          std::memset(&b, 0, sizeof(b));
-          b.M = vs;
-          b.N = H;
-          b.K = rows;
-          b.m_tiles = (vs + kBM - 1) / kBM;
-          b.n_tiles = (H + kBN - 1) / kBN;
-          b.k_iters = (rows + kBK - 1) / kBK;
-          b.group_m = std::min(b.m_tiles, 16);
-          b.alpha = p.out_mult;
-          b.M_valid = vs;
-          b.N_valid = H;
-          b.out = c.grad_W + static_cast<int64_t>(v0) * H;
-          b.ldo = H;
-          b.status = &hdr->status;
-          b.timeout_ns = timeout;
-          CUtensorMap map_o;
-          if (!encode_f32_out(&map_o, c.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
-          FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                                   std::min(b.m_tiles * b.n_tiles, sms), stream));
-        }
-      }
+      SlabArgs sa;
+      sa.rows = rows;
+      sa.H = H;
+      sa.V = V;
+      sa.slab = static_cast<int>(L.slab);
+      sa.col_base = 0;
+      sa.h_row0 = h_row0;
+      sa.map_hc = &map_hc;
+      sa.map_w = &map_w;
+      sa.h_c = h_c;
+      sa.ld_hc = ld_hc;
+      sa.W = static_cast<const uint16_t*>(c.W);
+      sa.ld_w = n.ld_w;
+      sa.labels = lab_c;
+      sa.lse = lse;
+      sa.hdr = hdr;
+      sa.dz = dz;
+      sa.gh_acc = gh32;
+      sa.grad_W = gw ? c.grad_W : nullptr;
+      sa.p = &p;
+      sa.inv_cap = inv_cap;
+      sa.timeout = timeout;
+      sa.sms = sms;
+      rc = recompute_slabs(sa, stream);
+      if (rc != FLCE_OK) return rc;
       if (gh) {
         FLCE_LAUNCH(K_CONVERT, launch_f32_to_bf16(gh32, static_cast<uint16_t*>(c.grad_h) + r0 * H,
                                                   static_cast<int64_t>(rows) * H, stream));
@@ -808,12 +883,148 @@ int run(const flce_params* params, const Call& c) {
     }
   }
 
+  if (shard) return FLCE_OK;  // the loss needs every shard's partials (flce_vp_backward)
   FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, out_loss, out_acc, stream));
   if (c.host_in) {
     if (cudaMemcpyAsync(c.loss, out_loss, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       return FLCE_ERR_CUDA;
     if (c.acc && cudaMemcpyAsync(c.acc, out_acc, sizeof(float), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       return FLCE_ERR_CUDA;
+  }
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------ vocab-parallel
+// Checks of a shard's place among the shards: offsets[0] = 0, increasing,
+// offsets[S] = vocab_total, and the shard [vocab_offset, vocab_offset + V_k)
+// one of the ranges.
+int check_shards(int64_t vocab_offset, int64_t vocab_shard, int64_t vocab_total, int n_shards,
+                 const int64_t* offsets) {
+  if (vocab_total <= 0 || vocab_total >= (int64_t(1) << 31) - 512) return FLCE_ERR_ARG;
+  if (vocab_offset < 0 || vocab_offset + vocab_shard > vocab_total) return FLCE_ERR_ARG;
+  if (n_shards < 0) return FLCE_ERR_ARG;
+  if (n_shards == 0) return FLCE_OK;  // forward: no table given
+  if (n_shards > kMaxShards || offsets == nullptr) return FLCE_ERR_ARG;
+  if (offsets[0] != 0 || offsets[n_shards] != vocab_total) return FLCE_ERR_ARG;
+  bool mine = false;
+  for (int k = 0; k < n_shards; ++k) {
+    if (offsets[k + 1] <= offsets[k]) return FLCE_ERR_ARG;
+    if (offsets[k] == vocab_offset && offsets[k + 1] - offsets[k] == vocab_shard) mine = true;
+  }
+  return mine ? FLCE_OK : FLCE_ERR_ARG;
+}
+
+struct VpLayout {
+  int64_t C, slab, blocks;
+  size_t off_hdr, off_bl, off_bc, off_lse, off_dz, total;
+};
+
+void make_vp_layout(const Norm& n, bool grads, VpLayout* L) {
+  const flce_params& p = n.p;
+  int64_t c = p.chunk_rows > 0 ? p.chunk_rows : kDefaultChunkRows;
+  c = std::min<int64_t>(c, std::max<int64_t>(p.n_rows, 1));
+  c = std::min<int64_t>(c, 32768);
+  L->C = round_up(c, kBM);
+  const int64_t want = p.vocab_slab > 0 ? p.vocab_slab : 16384;
+  L->slab = round_up(std::min<int64_t>(want, round_up(p.vocab, kVTile)), kVTile);
+  L->blocks = (std::max<int64_t>(p.n_rows, 1) + 31) / 32;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  L->off_hdr = take(sizeof(Header));
+  L->off_bl = take(sizeof(double) * L->blocks);
+  L->off_bc = take(sizeof(int64_t) * L->blocks);
+  L->off_lse = take(sizeof(float) * std::max<int64_t>(p.n_rows, 1));
+  L->off_dz = grads ? take(sizeof(uint16_t) * L->C * L->slab) : 0;
+  L->total = off;
+}
+
+// Backward of one vocab shard: merge of every shard's partials into lse, loss,
+// accuracy and predictions (the same on every shard), then the recompute
+// backward over the shard's vocab slabs, chunk by chunk.
+int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t vocab_total, int n_shards,
+                    const int64_t* offsets, const float* all_partials, const void* h, const void* W,
+                    const int64_t* labels, float* loss, float* acc, int64_t* predicted, float* row_lse,
+                    float* gh_acc, float* grad_W, void* wsv, size_t ws_bytes, cudaStream_t stream) {
+  Norm n;
+  int rc = normalise(params, &n);
+  if (rc != FLCE_OK) return rc;
+  const flce_params& p = n.p;
+  if (p.dtype != FLCE_DTYPE_BF16) return FLCE_ERR_UNSUPPORTED;
+  if (p.flags & (FLCE_FLAG_SIMT_GEMM | FLCE_FLAG_KMAJOR_BWD)) return FLCE_ERR_UNSUPPORTED;
+  if (n_shards < 1) return FLCE_ERR_ARG;
+  rc = check_shards(vocab_offset, p.vocab, vocab_total, n_shards, offsets);
+  if (rc != FLCE_OK) return rc;
+  if (!loss || !wsv || !W) return FLCE_ERR_ARG;
+  if (p.n_rows > 0 && (!h || !labels || !all_partials)) return FLCE_ERR_ARG;
+  if (!aligned16(wsv) || (h && !aligned16(h)) || !aligned16(W)) return FLCE_ERR_ALIGN;
+  if ((gh_acc && !aligned16(gh_acc)) || (grad_W && !aligned16(grad_W))) return FLCE_ERR_ALIGN;
+  const bool grads = gh_acc != nullptr || grad_W != nullptr;
+  VpLayout L;
+  make_vp_layout(n, grads, &L);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  int sms = 0, cc = 0;
+  rc = device_info(&sms, &cc);
+  if (rc != FLCE_OK) return rc;
+  if (cc != 103) return FLCE_ERR_UNSUPPORTED;
+  if (!load_encoder()) return FLCE_ERR_UNSUPPORTED;
+
+  uint8_t* ws = static_cast<uint8_t*>(wsv);
+  Header* hdr = reinterpret_cast<Header*>(ws + L.off_hdr);
+  float* lse_all = reinterpret_cast<float*>(ws + L.off_lse);
+  const int N = static_cast<int>(p.n_rows), H = static_cast<int>(p.hidden), V = static_cast<int>(p.vocab);
+  FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, vocab_total, p.ignore_index, hdr, stream));
+  VpMergeParams mp{};
+  mp.rows = N;
+  mp.n_shards = n_shards;
+  for (int k = 0; k <= n_shards; ++k) mp.offsets[k] = static_cast<int32_t>(offsets[k]);
+  mp.partials = all_partials;
+  mp.ld = p.n_rows;
+  mp.labels = labels;
+  mp.ignore_index = p.ignore_index;
+  mp.lse = lse_all;
+  mp.predicted = predicted;
+  mp.row_lse = row_lse;
+  mp.block_loss = reinterpret_cast<double*>(ws + L.off_bl);
+  mp.block_correct = reinterpret_cast<int64_t*>(ws + L.off_bc);
+  mp.hdr = hdr;
+  FLCE_LAUNCH(K_VP_MERGE, launch_vp_merge(mp, stream));
+  FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, loss, acc, stream));
+  if (!grads || N == 0) return FLCE_OK;
+
+  CUtensorMap map_h, map_w;
+  if (!encode_bf16(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+  if (!encode_bf16(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+  const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
+  for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
+    SlabArgs sa;
+    sa.rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
+    sa.H = H;
+    sa.V = V;
+    sa.slab = static_cast<int>(L.slab);
+    sa.col_base = static_cast<int>(vocab_offset);
+    sa.h_row0 = static_cast<int>(r0);
+    sa.map_hc = &map_h;
+    sa.map_w = &map_w;
+    sa.h_c = static_cast<const uint16_t*>(h) + r0 * n.ld_h;
+    sa.ld_hc = n.ld_h;
+    sa.W = static_cast<const uint16_t*>(W);
+    sa.ld_w = n.ld_w;
+    sa.labels = labels + r0;
+    sa.lse = lse_all + r0;
+    sa.hdr = hdr;
+    sa.dz = reinterpret_cast<uint16_t*>(ws + L.off_dz);
+    sa.gh_acc = gh_acc ? gh_acc + r0 * H : nullptr;
+    sa.grad_W = grad_W;
+    sa.p = &p;
+    sa.inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    sa.timeout = timeout;
+    sa.sms = sms;
+    rc = recompute_slabs(sa, stream);
+    if (rc != FLCE_OK) return rc;
   }
   return FLCE_OK;
 }
@@ -1186,6 +1397,44 @@ int flce_ce_only_from_host(const flce_params* p, const void* h_host, const void*
   c.host_in = true;
   c.copy_stream = static_cast<cudaStream_t>(copy_stream);
   return run(p, c);
+}
+
+size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_h, int need_grad_W) {
+  Norm n;
+  if (normalise(p, &n) != FLCE_OK) return 0;
+  if (!backward) {
+    Layout L;
+    make_layout(n, FLCE_MODE_CE_ONLY, false, false, &L);
+    return L.total;
+  }
+  VpLayout L;
+  make_vp_layout(n, need_grad_h != 0 || need_grad_W != 0, &L);
+  return L.total;
+}
+
+int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, const void* h,
+                    const void* W_shard, const int64_t* labels, float* partials, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!p || !partials) return FLCE_ERR_ARG;
+  const int rc = check_shards(vocab_offset, p->vocab, vocab_total, 0, nullptr);
+  if (rc != FLCE_OK) return rc;
+  if (p->dtype != FLCE_DTYPE_BF16 || (p->flags & FLCE_FLAG_SIMT_GEMM)) return FLCE_ERR_UNSUPPORTED;
+  Call c{FLCE_MODE_CE_ONLY, h, W_shard, labels, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.vocab_offset = vocab_offset;
+  c.vocab_total = vocab_total;
+  c.shard_partials = partials;
+  return run(p, c);
+}
+
+int flce_vp_backward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, int n_shards,
+                     const int64_t* shard_offsets, const float* all_partials, const void* h, const void* W_shard,
+                     const int64_t* labels, float* loss, float* token_accuracy, int64_t* predicted,
+                     float* row_lse, float* grad_h_partial, float* grad_W_shard, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return run_vp_backward(p, vocab_offset, vocab_total, n_shards, shard_offsets, all_partials, h, W_shard, labels,
+                         loss, token_accuracy, predicted, row_lse, grad_h_partial, grad_W_shard, workspace,
+                         workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int flce_cross_entropy(const flce_params* p, const void* logits, int logits_dtype, int64_t ld_logits,

@@ -61,6 +61,7 @@ enum KernelId {
   K_RECOMPUTE_GEMM = 12,
   K_CONVERT = 13,
   K_SCALE = 14,
+  K_VP_MERGE = 15,
 };
 
 enum EpiMode {
@@ -94,7 +95,10 @@ struct GemmParams {
   // plain epilogues
   void* out;
   int64_t ldo;
-  // dlogits epilogue (EPI_DZ): column j of D is vocab index col0 + j
+  // Column j of D is vocab index col0 + j: the statistics epilogues compare
+  // labels (global vocab ids) with it, and EPI_DZ places the one-hot term by
+  // it (0 unless D covers a vocab slab or a vocab shard).
+  // dlogits epilogue (EPI_DZ):
   const float* lse;  // [rows of D]
   const struct Header* hdr;
   float grad_scale;
@@ -152,8 +156,38 @@ struct MergeParams {
   double* block_loss;     // [blocks]
   int64_t* block_correct; // [blocks]
   Header* hdr;
+  // Vocab shard (flce_vp_forward): when shard_out is set, the merge writes the
+  // shard's per-row partials instead of lse / loss / predictions: shard_out +
+  // f * ld_shard + row for fields f = max, sum of exp, argmax (int32 global id
+  // in the float word: vocab_offset + the tile index), label logit (0 when the
+  // label is outside [vocab_offset, vocab_offset + vocab_shard)).
+  float* shard_out;
+  int64_t ld_shard;
+  int64_t vocab_offset;
+  int64_t vocab_shard;
 };
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+
+// Merge of the per-row partials of S vocab shards (flce_vp_backward), in
+// shard order: lse, argmax (lowest global id on ties), the label's logit from
+// the shard that holds the label, the row loss, and the fixed-order batch sums.
+constexpr int kMaxShards = 64;
+struct VpMergeParams {
+  int rows;                      // N
+  int n_shards;                  // S <= kMaxShards
+  int32_t offsets[kMaxShards + 1];  // vocab offset of each shard, then vocab_total
+  const float* partials;         // [S][4][ld]
+  int64_t ld;
+  const int64_t* labels;
+  int64_t ignore_index;
+  float* lse;                    // [rows] (workspace)
+  int64_t* predicted;            // [rows] or null
+  float* row_lse;                // [rows] or null
+  double* block_loss;            // [ceil(rows / 32)]
+  int64_t* block_correct;
+  Header* hdr;
+};
+cudaError_t launch_vp_merge(const VpMergeParams& p, cudaStream_t s);
 
 struct DlogitParams {
   int rows, vocab;

@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "flce_device.cuh"
 #include "flce_epilogue.cuh"
 
@@ -99,7 +101,8 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
   const bool row_ok = grow < p.M_valid;
   const int64_t label = row_ok ? __ldg(p.labels + grow) : p.ignore_index;
   const int n0 = nb * kBN;
-  const bool has_label = label != p.ignore_index && label >= n0 && label < n0 + kBN;
+  const int64_t ylocal = label - p.col0;  // the label as a column of D
+  const bool has_label = label != p.ignore_index && ylocal >= n0 && ylocal < n0 + kBN;
   const bool full_tile = n0 + kBN <= p.N_valid;  // no column past V: skip the mask
   RowStats st;
   row_stats_init(st, n0);
@@ -123,7 +126,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
         if (col0 + j >= p.N_valid) s[j] = -INFINITY;
     }
     if (STORE) stage_and_send<false>(es, zmap, lane, s, col0, mb * kBM + quarter * 32);
-    row_stats_update32(st, s, col0, has_label ? label : -1);
+    row_stats_update32(st, s, col0, has_label ? ylocal : -1);
   }
   if (row_ok) {
     const int64_t o = static_cast<int64_t>(nb) * p.ldp + grow;
@@ -493,16 +496,18 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
                                const GemmParams& p, int grid, cudaStream_t s) {
   // The shared-memory opt-in is a per-device function attribute: set it on the
   // first launch on each device (outside any stream capture that follows).
-  static bool configured[64] = {false};
+  // Two host threads may both set it on a first call; that is harmless, and
+  // the flags are atomic so the check itself is not a data race.
+  static std::atomic<bool> configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const int units = ((p.m_tiles + TMH - 1) / TMH) * p.n_tiles;
   if (grid > units) grid = units;

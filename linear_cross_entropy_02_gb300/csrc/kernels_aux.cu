@@ -108,6 +108,35 @@ __global__ void __launch_bounds__(kMergeRows * kMergeWarps) merge_kernel(const M
   s_s[warp][lane] = sum;
   s_a[warp][lane] = arg;
   __syncthreads();
+  if (p.shard_out != nullptr) {
+    // one vocab shard's partials; the batch sums wait for the merge of all shards
+    if (warp == 0 && row < p.rows) {
+      float M = -INFINITY, S = 0.f;
+      int A = 0x7fffffff;
+      for (int w = 0; w < kMergeWarps; ++w) {
+        const float m2 = s_m[w][lane];
+        const float s2 = s_s[w][lane];
+        const int a2 = s_a[w][lane];
+        if (m2 == -INFINITY) continue;
+        if (m2 > M) {
+          S = S * expf(M - m2) + s2;
+          M = m2;
+          A = a2;
+        } else {
+          S += s2 * expf(m2 - M);
+          if (m2 == M && a2 < A) A = a2;
+        }
+      }
+      const int64_t y = p.labels[row];
+      const int64_t yl = y - p.vocab_offset;
+      const bool here = y != p.ignore_index && yl >= 0 && yl < p.vocab_shard;
+      p.shard_out[row] = M;
+      p.shard_out[p.ld_shard + row] = S;
+      p.shard_out[2 * p.ld_shard + row] = __int_as_float(static_cast<int>(A + p.vocab_offset));
+      p.shard_out[3 * p.ld_shard + row] = here ? p.tgt[row] : 0.f;
+    }
+    return;
+  }
   if (warp == 0) {
     double loss_i = 0.0;
     long long corr_i = 0;
@@ -172,6 +201,79 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   const int blocks = (p.rows + kMergeRows - 1) / kMergeRows;
   if (blocks == 0) return cudaSuccess;
   merge_kernel<<<blocks, kMergeRows * kMergeWarps, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ vocab-shard merge
+// One warp of 32 rows per block. Row i folds the partials of shards 0..S-1 in
+// order: the running max is replaced only on a strict increase, so on ties the
+// lower shard (the lower vocab ids) keeps the argmax, as within a shard. The
+// label's logit comes from the shard whose range holds the label.
+__global__ void __launch_bounds__(32) vp_merge_kernel(const VpMergeParams p) {
+  const int lane = threadIdx.x;
+  const int row = blockIdx.x * 32 + lane;
+  double loss_i = 0.0;
+  long long corr_i = 0;
+  if (row < p.rows) {
+    float M = -INFINITY, S = 0.f;
+    int A = 0x7fffffff;
+    for (int k = 0; k < p.n_shards; ++k) {
+      const float* q = p.partials + static_cast<int64_t>(k) * 4 * p.ld;
+      const float m2 = q[row];
+      const float s2 = q[p.ld + row];
+      const int a2 = __float_as_int(q[2 * p.ld + row]);
+      if (m2 == -INFINITY) continue;
+      if (m2 > M) {
+        S = S * expf(M - m2) + s2;
+        M = m2;
+        A = a2;
+      } else {
+        S += s2 * expf(m2 - M);
+      }
+    }
+    const float lse = M + logf(S);
+    p.lse[row] = lse;
+    const int64_t y = p.labels[row];
+    if (y != p.ignore_index) {
+      int k = 0;
+      while (k + 1 < p.n_shards && y >= p.offsets[k + 1]) ++k;
+      const float t = p.partials[static_cast<int64_t>(k) * 4 * p.ld + 3 * p.ld + row];
+      loss_i = static_cast<double>(lse) - static_cast<double>(t);
+      corr_i = (static_cast<int64_t>(A) == y) ? 1 : 0;
+    }
+    if (p.predicted) p.predicted[row] = A;
+    if (p.row_lse) p.row_lse[row] = lse;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    loss_i += __shfl_xor_sync(0xffffffffu, loss_i, o);
+    corr_i += __shfl_xor_sync(0xffffffffu, corr_i, o);
+  }
+  unsigned int last = 0;
+  if (lane == 0) {
+    p.block_loss[blockIdx.x] = loss_i;
+    p.block_correct[blockIdx.x] = corr_i;
+    __threadfence();
+    last = atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1;
+  }
+  // the last block adds the block sums in block order (a fixed order)
+  if (lane == 0 && last) {
+    __threadfence();
+    double tl = 0.0;
+    long long tc = 0;
+    for (unsigned int b = 0; b < gridDim.x; ++b) {
+      tl += reinterpret_cast<volatile double*>(p.block_loss)[b];
+      tc += reinterpret_cast<volatile long long*>(p.block_correct)[b];
+    }
+    p.hdr->loss_sum += tl;
+    p.hdr->correct += tc;
+    p.hdr->ticket = 0;
+  }
+}
+
+cudaError_t launch_vp_merge(const VpMergeParams& p, cudaStream_t s) {
+  const int blocks = (p.rows + 31) / 32;
+  if (blocks == 0) return cudaSuccess;
+  vp_merge_kernel<<<blocks, 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

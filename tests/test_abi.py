@@ -156,7 +156,8 @@ def test_kernel_names(L):
     from linear_cross_entropy_02_gb300 import _lib as B
     names = [L.flce_kernel_name(i).decode() for i in range(B.FLCE_NUM_KERNELS)]
     assert names[1] == "fwd_gemm_stats" and names[4] == "grad_h_gemm" and names[5] == "grad_W_gemm"
-    assert names[-1] == "scale_gradient" and len(set(names)) == len(names) and "unknown" not in names
+    assert names[-2] == "scale_gradient" and names[-1] == "vp_merge"
+    assert len(set(names)) == len(names) and "unknown" not in names
     assert L.flce_kernel_name(B.FLCE_NUM_KERNELS) == b"unknown"
     assert L.flce_kernel_name(99) == b"unknown"
 
@@ -273,3 +274,34 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "no CPU or PyTorch fallback" in r.stdout
+
+
+def test_vocab_parallel_host_errors(L):
+    """The vocab-parallel entry points reject a shard that is not inside the
+    vocabulary, and shard tables that do not tile it or do not contain the
+    calling shard, before any device call (the pointers are never used)."""
+    from linear_cross_entropy_02_gb300 import _lib as B
+    fake = ctypes.c_void_p(1 << 20)
+    p = _params(L, n_rows=64, hidden=32, vocab=300)
+    assert L.flce_vp_workspace_size(ctypes.byref(p), 0, 0, 0) == \
+        L.flce_workspace_size(ctypes.byref(p), B.FLCE_MODE_CE_ONLY, 0, 0)
+    bwd = L.flce_vp_workspace_size(ctypes.byref(p), 1, 1, 1)
+    assert bwd > L.flce_vp_workspace_size(ctypes.byref(p), 1, 0, 0) >= 64 * 4
+    # the shard [vocab_offset, vocab_offset + 300) must lie inside [0, vocab_total)
+    for off, tot in ((0, 299), (-1, 600), (301, 600), (0, 1 << 31)):
+        rc = L.flce_vp_forward(ctypes.byref(p), off, tot, fake, fake, fake, fake, fake, 1 << 40, None)
+        assert rc == B.FLCE_ERR_ARG, (off, tot)
+    assert L.flce_vp_forward(ctypes.byref(p), 0, 600, fake, fake, fake, None, fake, 1 << 40, None) == B.FLCE_ERR_ARG
+    pf = _params(L, n_rows=64, hidden=32, vocab=300, dtype=B.FLCE_DTYPE_F32)
+    assert L.flce_vp_forward(ctypes.byref(pf), 0, 600, fake, fake, fake, fake, fake, 1 << 40, None) == \
+        B.FLCE_ERR_UNSUPPORTED
+
+    def bwd_rc(offsets, off=0, tot=600, params=p, ws=1 << 40):
+        arr = (ctypes.c_int64 * len(offsets))(*offsets)
+        return L.flce_vp_backward(ctypes.byref(params), off, tot, len(offsets) - 1, arr, fake, fake, fake, fake,
+                                  fake, None, None, None, fake, fake, fake, ws, None)
+    for bad in ([0, 600], [0, 300, 599], [1, 300, 600], [0, 250, 600], [0, 300, 300, 600]):
+        assert bwd_rc(bad) == B.FLCE_ERR_ARG, bad
+    assert bwd_rc([0, 300, 600], ws=bwd - 256) == B.FLCE_ERR_WORKSPACE
+    assert bwd_rc([0, 300, 600], params=pf) == B.FLCE_ERR_UNSUPPORTED
+    assert bwd_rc(list(range(0, 600, 9)) + [600]) == B.FLCE_ERR_ARG          # 67 shards: more than 64
