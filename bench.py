@@ -322,7 +322,7 @@ def kernel_source_hash() -> str:
 def _traffic_key(args, w):
     """The key of a bench line's recorded traffic: the workload and the variant
     of the path it runs. Lines with overridden sizes have none."""
-    if args.rows or args.vocab or args.chunk_rows or args.vocab_slab:
+    if args.rows or args.vocab or args.chunk_rows or args.vocab_slab or getattr(args, "vocab_shards", 0):
         return None
     if args.ce_logits:
         return w.name + "-ce_logits"
@@ -345,6 +345,47 @@ def recorded_traffic(workload, kernel: str, chunk_rows: int = 8192):
     return e["bytes_per_launch"]
 
 
+GOLDEN_DIR = os.path.join(ROOT, "tests", "golden", "configs")
+GOLDEN_FOR = {"llama": "llama", "muse": "muse", "dsv3": "dsv3", "frozen_ce": "frozen", "frozen_grad_h": "frozen"}
+NEAR_TIE = 1e-3
+
+
+def parity_against_goldens(flce, w, h, W, lab, inputs_cpu, kw):
+    """One flce_forward of the timed workload (outside the timed region)
+    compared row by row with the stored full-size oracle forward of the same
+    inputs (tests/golden/configs, written by the oracle alone): the loss, every
+    row's lse, every predicted token, and the correct count. Rows whose oracle
+    top-2 gap is below 1e-3 relative may predict the other token; they are
+    counted here. None when the workload has no stored oracle forward."""
+    g = GOLDEN_FOR.get(w.name)
+    if g is None or not os.path.exists(os.path.join(GOLDEN_DIR, g + ".json")):
+        return None
+    with open(os.path.join(GOLDEN_DIR, g + ".json")) as f:
+        meta = json.load(f)
+    arr = np.load(os.path.join(GOLDEN_DIR, g + ".npz"))
+    hashes = {k: workloads.tensor_sha256(t) for k, t in zip(("h", "W", "labels"), inputs_cpu)}
+    if hashes != meta["sha256"]:
+        return {"oracle": f"tests/golden/configs/{g}", "skipped": "inputs differ from the stored oracle's"}
+    f = flce.flce_forward(h, W, lab, return_lse=True, **kw)
+    torch.cuda.synchronize()
+    pred = f["predicted"].reshape(-1).cpu().numpy()
+    lse = f["lse"].reshape(-1).cpu().double().numpy()
+    y = inputs_cpu[2].numpy()
+    valid = y != -100
+    pred_o = arr["predicted"].astype(np.int64)
+    near = arr["near_tie"].astype(bool)
+    mism = pred != pred_o
+    correct = int(np.sum((pred == y) & valid))
+    loss = float(f["loss"])
+    return {"oracle": f"tests/golden/configs/{g} (fp64, all {len(y)} rows)",
+            "loss": loss, "loss_oracle": meta["loss"], "loss_rel_err": abs(loss - meta["loss"]) / abs(meta["loss"]),
+            "lse_max_abs_err": float(np.abs(lse - arr["lse"].astype(np.float64)).max()),
+            "near_tie_rows": int(near.sum()), "near_tie_threshold": NEAR_TIE,
+            "predicted_mismatches": int(mism.sum()), "predicted_mismatches_on_near_ties": int((mism & near).sum()),
+            "predicted_mismatches_off_near_ties": int((mism & ~near).sum()),
+            "correct": correct, "correct_oracle": meta["correct"], "n_valid": int(valid.sum())}
+
+
 def run_ours(args, w):
     world, rank, local, dist = _dist()
     torch.cuda.set_device(local)
@@ -354,6 +395,7 @@ def run_ours(args, w):
     if args.ce_logits:
         return run_ce_logits(args, w, world, rank, local, dist, flce)
     h_cpu, W_cpu, lab_cpu = workloads.make_inputs(w)
+    inputs_bf16 = (h_cpu, W_cpu, lab_cpu)
     if args.fp32:  # the same bf16-valued inputs carried in fp32: the tf32 tensor-core path
         h_cpu, W_cpu = h_cpu.float(), W_cpu.float()
     h = h_cpu.to(dev)
@@ -369,6 +411,32 @@ def run_ours(args, w):
             return flce.flce_ce_only(h, W, lab, **kw)
         return flce.flce_forward_backward(h, W, lab, grad_W=gW, need_grad_h=True,
                                           return_predicted=w.return_predicted, **kw, **bkw)
+
+    if args.vocab_shards:
+        # The vocabulary-parallel form, its S shards run one after another on
+        # this GPU: every shard's forward, the gather (a stack in shard order),
+        # every shard's backward into one fp32 grad_h and its rows of grad_W,
+        # then grad_h rounded to bf16. The same work S GPUs would share.
+        S = args.vocab_shards
+        offsets = [round(k * w.vocab / S) for k in range(S + 1)]
+        shards = [W[offsets[k]:offsets[k + 1]] for k in range(S)]
+        gW_sh = [None if gW is None else gW[offsets[k]:offsets[k + 1]] for k in range(S)]
+        gh32 = torch.empty((w.n_rows, w.hidden), dtype=torch.float32, device=dev)
+        vkw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+
+        def step():
+            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, **vkw) for k in range(S)]
+            allp = torch.stack(parts)
+            gh32.zero_()
+            out = None
+            for k in range(S):
+                out = flce.flce_vp_backward(h, shards[k], lab, allp, offsets, offsets[k], w.vocab,
+                                            grad_h_partial=gh32 if w.mode != "ce_only" else None,
+                                            grad_W=gW_sh[k], vocab_slab=args.vocab_slab,
+                                            return_predicted=w.return_predicted, **vkw)
+            if w.mode != "ce_only":
+                flce.flce_scale_gradient(gh32, None, out_dtype=h.dtype)
+            return out
 
     for _ in range(args.warmup):
         step()
@@ -400,21 +468,28 @@ def run_ours(args, w):
         torch.cuda.current_stream(dev).synchronize()
         res[0], res[1] = float(loss), float(acc)
 
-    e2e_step()
-    _barrier(dist)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
+    e2e_value = None
+    if not args.vocab_shards:
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / args.steps
-    e2e_max = _max_over_ranks(dist, e2e_s)
-    e2e_value = rows_total / e2e_max
+        _barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        e2e_max = _max_over_ranks(dist, e2e_s)
+        e2e_value = rows_total / e2e_max
 
     peaks = _peaks()
     flops = w.flops
     tflops = flops / (ms / 1e3) / 1e12
     step_peak = peaks["bf16_sustained"] * (TF32_OVER_BF16 if args.fp32 else 1.0)
     line = None
+    parity = None
+    if rank == 0 and not (args.rows or args.vocab):
+        parity = parity_against_goldens(flce, w, h, W, lab, inputs_bf16,
+                                        dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows,
+                                             flags=kw["flags"]))
     if rank == 0:
         chunk_used = flce.flce_chunk_rows(
             w.n_rows, w.hidden, w.vocab,
@@ -460,16 +535,24 @@ def run_ours(args, w):
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
             "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,
-            "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if args.low_memory and w.mode == "fwd_bwd"
-                                                       else 1.0),
-            "backward": "recompute (low memory)" if args.low_memory else "stored logits",
+            "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if (args.low_memory or args.vocab_shards)
+                                                       and w.mode == "fwd_bwd" else 1.0),
+            "backward": "recompute (low memory)" if (args.low_memory or args.vocab_shards) else "stored logits",
             "gemm_cta_tile": ("128x256, two accumulators" if args.tile128
                               else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"),
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT,
+            **({"vocab_shards": {"shards": args.vocab_shards, "run": "in turn on one GPU",
+                                 "exchange_bytes_per_step": 16 * w.n_rows * args.vocab_shards}}
+               if args.vocab_shards else {}),
+            "e2e": None if e2e_value is None else {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h.numel() * h.element_size() + lab.numel() * 8, "d2h_bytes_per_step": 8,
                     "path": "flce_*_from_host: host h and labels, copied by the library in chunks under its "
-                            "kernels"},
+                            "kernels; the loss and token accuracy come back to host memory",
+                    "resident_outputs": ("none (CE-only)" if w.mode == "ce_only" else
+                                         "grad_h" + (", grad_W" if w.mode == "fwd_bwd" else "")
+                                         + (", predicted" if w.return_predicted else "")
+                                         + " stay in device memory (a training step consumes them there)")},
+            "parity": parity,
             "gpu_launches": launches,
             "clocks": clocks,
             **({"remeasured": remeasured} if remeasured else {}),
@@ -610,6 +693,8 @@ def main():
                     help="128-row GEMM tiles with two accumulators (FLCE_FLAG_TILE128), for comparison")
     ap.add_argument("--ce-logits", action="store_true",
                     help="time the cross-entropy on materialised bf16 logits [N, V] instead")
+    ap.add_argument("--vocab-shards", type=int, default=0,
+                    help="time the vocabulary-parallel form with this many shards, run in turn on one GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]

@@ -142,3 +142,26 @@ def zipf_head_ids(vocab: int, k: int) -> list:
     """The k most frequent ids under the Zipf recipe (ids 0..k-1)."""
     return list(range(min(k, vocab)))
 
+
+def plant_labels(labels: torch.Tensor, predicted, frac: float, seed: int,
+                 ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
+    """Labels with a seeded `frac` of the non-ignored rows replaced by the given
+    predicted ids (ignored rows stay ignored). With the oracle's predictions this
+    makes a batch whose token accuracy is far from the ~1/V of uniform labels."""
+    lab = labels.clone()
+    valid = np.nonzero(lab.numpy() != ignore_index)[0]
+    k = int(round(frac * len(valid)))
+    rng = np.random.default_rng(seed)
+    pick = np.sort(rng.choice(valid, size=k, replace=False)) if k > 0 else np.zeros(0, np.int64)
+    pred = np.asarray(predicted, dtype=np.int64)
+    lab[torch.from_numpy(pick)] = torch.from_numpy(pred[pick])
+    return lab
+
+
+def tensor_sha256(t: torch.Tensor) -> str:
+    """sha256 of a CPU tensor's raw bytes (bf16 as its 16-bit patterns)."""
+    import hashlib
+    x = t.contiguous()
+    if x.dtype == torch.bfloat16:
+        x = x.view(torch.int16)
+    return hashlib.sha256(x.numpy().tobytes()).hexdigest()
