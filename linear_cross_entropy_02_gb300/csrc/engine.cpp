@@ -158,6 +158,19 @@ bool encode_f32_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+// fp16 [outer][inner] with row stride `ld` elements; 64 x 32 boxes (128-byte
+// rows), 128-byte swizzle: the forward epilogue's store of s - gmax.
+bool encode_f16_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ layout
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -168,8 +181,12 @@ struct Layout {
   int64_t merge_blocks;
   int64_t slab;     // recompute mode: vocab columns per slab (0 otherwise)
   bool need_z, need_dz, need_dzt, need_wt, need_ht, need_gh32;
-  size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_dz, off_dzt, off_wt,
-      off_ht, off_gh32, total;
+  // z16: the stored logits are fp16 s - gmax with fp32 gmax per 32 columns
+  // (the bf16 backward on MN-major tiles); otherwise fp32 s
+  bool z16;
+  int64_t ldg;      // gmax row stride (ldz / 32)
+  size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_gmax, off_dz, off_dzt,
+      off_wt, off_ht, off_gh32, total;
   // host inputs (flce_forward_backward_from_host): two chunk buffers of h, all
   // labels, and the two result scalars before they are copied to the host
   bool host_in;
@@ -303,6 +320,8 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
     L->slab = round_up(std::min<int64_t>(want, round_up(p.vocab, kVTile)), kVTile);
   }
   L->need_z = (bwd && !recompute) || simt;
+  L->z16 = bwd && !recompute && !simt && !kmajor && !f32;
+  L->ldg = L->ldz / 32;
   L->need_dz = bwd && (gh || (gw && !kmajor));
   L->need_dzt = bwd && gw && kmajor;
   L->need_wt = bwd && gh && kmajor;
@@ -322,7 +341,8 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_pidx = take(sizeof(int32_t) * L->n_vtiles * L->ldp);
   L->off_tgt = take(sizeof(float) * L->C);
   L->off_lse = take(sizeof(float) * L->C);
-  L->off_z = L->need_z ? take(sizeof(float) * L->C * L->ldz) : 0;
+  L->off_z = L->need_z ? take((L->z16 ? 2 : sizeof(float)) * L->C * L->ldz) : 0;
+  L->off_gmax = L->z16 ? take(sizeof(float) * L->C * L->ldg) : 0;
   L->off_dz = L->need_dz ? take(es * L->C * (recompute ? L->slab : L->ldd)) : 0;
   L->off_dzt = L->need_dzt ? take(es * round_up(p.vocab, kBM) * L->ldt) : 0;
   L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
@@ -609,7 +629,9 @@ int run(const flce_params* params, const Call& c) {
   int32_t* pidx = reinterpret_cast<int32_t*>(ws + L.off_pidx);
   float* tgt = reinterpret_cast<float*>(ws + L.off_tgt);
   float* lse = reinterpret_cast<float*>(ws + L.off_lse);
-  float* zbuf = L.need_z ? reinterpret_cast<float*>(ws + L.off_z) : nullptr;
+  float* zbuf = L.need_z && !L.z16 ? reinterpret_cast<float*>(ws + L.off_z) : nullptr;
+  uint16_t* z16 = L.z16 ? reinterpret_cast<uint16_t*>(ws + L.off_z) : nullptr;
+  float* gmax = L.z16 ? reinterpret_cast<float*>(ws + L.off_gmax) : nullptr;
   uint16_t* dz = L.need_dz ? reinterpret_cast<uint16_t*>(ws + L.off_dz) : nullptr;
   uint16_t* dzt = L.need_dzt ? reinterpret_cast<uint16_t*>(ws + L.off_dzt) : nullptr;
   uint16_t* wt = L.need_wt ? reinterpret_cast<uint16_t*>(ws + L.off_wt) : nullptr;
@@ -701,8 +723,10 @@ int run(const flce_params* params, const Call& c) {
     g.part_idx = pidx;
     g.tgt = tgt;
     g.ldp = static_cast<int>(L.ldp);
-    g.zbuf = zbuf;
+    g.zbuf = L.z16 ? nullptr : zbuf;
     g.ldz = L.ldz;
+    g.gmax = gmax;
+    g.ldg = L.ldg;
     g.status = &hdr->status;
     g.timeout_ns = timeout;
     g.debug_flags = p.flags;
@@ -715,8 +739,10 @@ int run(const flce_params* params, const Call& c) {
     } else {
       const int tiles = g.m_tiles * g.n_tiles;
       CUtensorMap map_z;
-      if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(store ? EPI_STATS_STORE : EPI_STATS, false, false, wide_for(g), &map_hc, &map_w,
+      if (store && L.z16 && !encode_f16_out(&map_z, z16, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
+      if (store && !L.z16 && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
+      const int mode = !store ? EPI_STATS : L.z16 ? EPI_STATS_STORE16 : EPI_STATS_STORE;
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(mode, false, false, wide_for(g), &map_hc, &map_w,
                                              store ? &map_z : nullptr, g, std::min(tiles, sms), stream));
     }
 
@@ -790,6 +816,9 @@ int run(const flce_params* params, const Call& c) {
     dp.vocab = V;
     dp.s = zbuf;
     dp.lds = L.ldz;
+    dp.s16 = z16;
+    dp.gmax = gmax;
+    dp.ldg = L.ldg;
     dp.lse = lse;
     dp.labels = lab_c;
     dp.ignore_index = p.ignore_index;

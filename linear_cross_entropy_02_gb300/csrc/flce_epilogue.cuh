@@ -45,13 +45,14 @@ __device__ __forceinline__ void pair_level(float (&v)[16], int (&ix)[16]) {
   }
 }
 
-// Folds 32 consecutive columns col0 .. col0+31 of one row into `st`.
+// Folds 32 consecutive columns col0 .. col0+31 of one row into `st`, and
+// returns the largest of the 32 values.
 // Argmax over the 32 by a tree of adjacent pairs, so the left operand always
 // holds the lower columns and a strict comparison keeps the lowest index on
 // ties; against earlier columns the running max is also replaced only on a
 // strict increase. exp(s - mx) is computed as 2^(s log2 e - mx log2 e).
-__device__ __forceinline__ void row_stats_update32(RowStats& st, const float (&s)[32], int col0,
-                                                   int64_t label) {
+__device__ __forceinline__ float row_stats_update32(RowStats& st, const float (&s)[32], int col0,
+                                                    int64_t label) {
   float v[16];
   int ix[16];
 #pragma unroll
@@ -95,6 +96,7 @@ __device__ __forceinline__ void row_stats_update32(RowStats& st, const float (&s
     }
     st.tgt = t;
   }
+  return cm;
 }
 
 }  // namespace flce

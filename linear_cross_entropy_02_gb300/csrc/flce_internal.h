@@ -71,6 +71,7 @@ enum EpiMode {
   EPI_ACC_F32 = 3,      // out += alpha * acc (fp32)
   EPI_DZ = 4,           // out = bf16 dlogits formed from z = alpha * acc, lse and labels
   EPI_F32 = 5,          // out = alpha * acc (fp32, bulk store)
+  EPI_STATS_STORE16 = 6,  // statistics partials + s stored as fp16 s - gmax, gmax (fp32) per 32 columns
 };
 
 struct GemmParams {
@@ -92,6 +93,8 @@ struct GemmParams {
   int ldp;
   float* zbuf;  // capped logits [rows][ldz] (STATS_STORE, and the SIMT path)
   int64_t ldz;
+  float* gmax;  // STATS_STORE16: [rows][ldg] maximum of each 32-column group of s
+  int64_t ldg;
   // plain epilogues
   void* out;
   int64_t ldo;
@@ -193,6 +196,9 @@ struct DlogitParams {
   int rows, vocab;
   const float* s;   // capped logits [rows][lds]
   int64_t lds;
+  const uint16_t* s16;  // or: fp16 s - gmax [rows][lds] (the bf16 product path)
+  const float* gmax;    // with s16: [rows][ldg], the reference of each 32-column group
+  int64_t ldg;
   const float* lse; // [rows]
   const int64_t* labels;
   int64_t ignore_index;

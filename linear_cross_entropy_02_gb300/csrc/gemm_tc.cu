@@ -22,6 +22,7 @@
 // Every wait is bounded (FLCE_ERR_TIMEOUT); on the way out the CTA drains the
 // copies and MMAs it issued and frees TMEM.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <atomic>
@@ -93,7 +94,47 @@ __device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* 
   if (es.nbuf == 2) es.next ^= 1;
 }
 
-template <bool STORE>
+// The same staging for two 32-column groups of fp16 values (a 32 x 64 fp16
+// sub-tile, again 128 bytes per row): lo holds columns x .. x+31, hi the next 32.
+__device__ __forceinline__ void stage_and_send16(EpiStage& es, const CUtensorMap* map, int lane,
+                                                 const uint32_t (&lo)[16], const uint32_t (&hi)[16], int32_t x,
+                                                 int32_t y) {
+  uint8_t* buf = es.base + es.next * kStageBufBytes;
+  if (lane == 0) {
+    if (es.nbuf == 2)
+      bulk_wait_group_read<1>();
+    else
+      bulk_wait_group_read<0>();
+  }
+  __syncwarp();
+  uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) row[q ^ (lane & 7)] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    row[(q + 4) ^ (lane & 7)] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (es.hint)
+      tma_store_2d_hint(map, buf, x, y, es.policy);
+    else
+      tma_store_2d(map, buf, x, y);
+    bulk_commit_group();
+  }
+  if (es.nbuf == 2) es.next ^= 1;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Forward statistics of one 256-column tile of 128 rows. STORE: 0 keeps only
+// the statistics; 1 also stores the capped logits s in fp32; 2 stores them
+// relative to the maximum of their 32-column group, s - gmax, in fp16 (halving
+// the stored bytes), with gmax in fp32 beside them.
+template <int STORE>
 __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtensorMap* zmap, EpiStage& es,
                                                uint32_t tcol, int mb, int nb, int quarter, int lane) {
   const int row = quarter * 32 + lane;
@@ -106,6 +147,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
   const bool full_tile = n0 + kBN <= p.N_valid;  // no column past V: skip the mask
   RowStats st;
   row_stats_init(st, n0);
+  uint32_t held[16];  // STORE == 2: the even group's fp16 values, sent with the odd one
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
@@ -125,8 +167,22 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
       for (int j = 0; j < 32; ++j)
         if (col0 + j >= p.N_valid) s[j] = -INFINITY;
     }
-    if (STORE) stage_and_send<false>(es, zmap, lane, s, col0, mb * kBM + quarter * 32);
-    row_stats_update32(st, s, col0, has_label ? ylocal : -1);
+    if (STORE == 1) stage_and_send<false>(es, zmap, lane, s, col0, mb * kBM + quarter * 32);
+    const float cm = row_stats_update32(st, s, col0, has_label ? ylocal : -1);
+    if (STORE == 2) {
+      // A group wholly past V has cm = -inf; its values are never read.
+      const float ref = cm == -INFINITY ? 0.f : cm;
+      uint32_t hv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hv[j] = cm == -INFINITY ? 0u : pack_half2(s[2 * j] - ref, s[2 * j + 1] - ref);
+      if (row_ok) p.gmax[static_cast<int64_t>(grow) * p.ldg + (col0 >> 5)] = ref;
+      if ((c & 1) == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) held[j] = hv[j];
+      } else {
+        stage_and_send16(es, zmap, lane, held, hv, col0 - 32, mb * kBM + quarter * 32);
+      }
+    }
   }
   if (row_ok) {
     const int64_t o = static_cast<int64_t>(nb) * p.ldp + grow;
@@ -284,7 +340,8 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
-    if (MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32 || MODE == EPI_F32) tma_prefetch_desc(&tma_c);
+    if (MODE == EPI_STATS_STORE || MODE == EPI_STATS_STORE16 || MODE == EPI_ACC_F32 || MODE == EPI_F32)
+      tma_prefetch_desc(&tma_c);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -457,9 +514,11 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
         if (mb >= p.m_tiles) break;
         const uint32_t tcol = t_lane + static_cast<uint32_t>((acc + hh) * kBN);
         if (MODE == EPI_STATS) {
-          epilogue_stats<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_STATS_STORE) {
-          epilogue_stats<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_STATS_STORE16) {
+          epilogue_stats<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_BF16) {
           epilogue_bf16(p, tcol, mb, nb, row);
         } else if (MODE == EPI_ACC_F32) {
@@ -480,7 +539,9 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
       }
     }
     // Outstanding bulk stores / reduce-adds must finish before the CTA exits.
-    if ((MODE == EPI_STATS_STORE || MODE == EPI_ACC_F32 || MODE == EPI_F32) && lane == 0) bulk_wait_group<0>();
+    if ((MODE == EPI_STATS_STORE || MODE == EPI_STATS_STORE16 || MODE == EPI_ACC_F32 || MODE == EPI_F32) &&
+        lane == 0)
+      bulk_wait_group<0>();
   }
 
   tc_fence_before_sync();
@@ -519,7 +580,8 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
 
 cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUtensorMap* a, const CUtensorMap* b,
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
-  if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
+  if ((mode == EPI_STATS_STORE || mode == EPI_STATS_STORE16 || mode == EPI_ACC_F32 || mode == EPI_F32) &&
+      c == nullptr)
     return cudaErrorInvalidValue;
   // The combinations the engine uses: the forward GEMM (both K-major), grad_h
   // (dz K-major, W MN-major or its transpose K-major), grad_W (dz and h_c
@@ -531,6 +593,8 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
       switch (mode) {
         case EPI_STATS: return launch_mode<EPI_STATS, false, false, false, 2>(a, b, c, p, grid, s);
         case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false, false, 2>(a, b, c, p, grid, s);
+        case EPI_STATS_STORE16:
+          return launch_mode<EPI_STATS_STORE16, false, false, false, 2>(a, b, c, p, grid, s);
         case EPI_DZ: return launch_mode<EPI_DZ, false, false, false, 2>(a, b, c, p, grid, s);
         default: break;
       }
@@ -544,6 +608,7 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
     switch (mode) {
       case EPI_STATS: return launch_mode<EPI_STATS, false, false>(a, b, c, p, grid, s);
       case EPI_STATS_STORE: return launch_mode<EPI_STATS_STORE, false, false>(a, b, c, p, grid, s);
+      case EPI_STATS_STORE16: return launch_mode<EPI_STATS_STORE16, false, false>(a, b, c, p, grid, s);
       case EPI_BF16: return launch_mode<EPI_BF16, false, false>(a, b, c, p, grid, s);
       case EPI_ACC_F32: return launch_mode<EPI_ACC_F32, false, false>(a, b, c, p, grid, s);
       case EPI_DZ: return launch_mode<EPI_DZ, false, false>(a, b, c, p, grid, s);

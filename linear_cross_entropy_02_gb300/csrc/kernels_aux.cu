@@ -10,6 +10,7 @@
 //   finish        loss and token accuracy scalars
 //   simt gemm     fp32 FMA GEMM + statistics from stored logits (debug path)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "flce_device.cuh"
@@ -380,12 +381,31 @@ __global__ void __launch_bounds__(256) dlogits_kernel(const DlogitParams p) {
 // 2048 i + 8 t (each piece: 32 B of s read, 16 B of dz written, contiguous
 // across the block), so the per-row setup is paid once per 32 columns.
 // exp(s - lse) is 2^(s log2 e - lse log2 e) on the special-function unit.
-template <bool CAP>
-__device__ __forceinline__ void dlogits_piece(const DlogitParams& p, const float* srow, uint16_t* drow, int c,
-                                              float ci, float lse_l2e, int label_local) {
+// HALF: the forward stored s - gmax in fp16 (s16) with gmax per 32-column
+// group; the eight columns of a piece lie in one group.
+template <bool CAP, bool HALF>
+__device__ __forceinline__ void dlogits_piece(const DlogitParams& p, const float* srow, const uint16_t* s16row,
+                                              const float* grow, uint16_t* drow, int c, float ci, float lse_l2e,
+                                              int label_local) {
   float sv[8];
   const bool full = c + 8 <= p.vocab;
-  if (full) {
+  if (HALF) {
+    const float gm = grow[c >> 5];
+    if (full) {
+      const uint4 a = *reinterpret_cast<const uint4*>(s16row + c);
+      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
+        sv[2 * j] = f.x + gm;
+        sv[2 * j + 1] = f.y + gm;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        sv[j] = (c + j < p.vocab) ? __half2float(__ushort_as_half(s16row[c + j])) + gm : 0.f;
+    }
+  } else if (full) {
     const float4 a = *reinterpret_cast<const float4*>(srow + c);
     const float4 b = *reinterpret_cast<const float4*>(srow + c + 4);
     sv[0] = a.x; sv[1] = a.y; sv[2] = a.z; sv[3] = a.w;
@@ -415,6 +435,7 @@ __device__ __forceinline__ void dlogits_piece(const DlogitParams& p, const float
   }
 }
 
+template <bool HALF>
 __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p) {
   const int r = blockIdx.y;
   const int c_base = blockIdx.x * 8192 + threadIdx.x * 8;
@@ -425,7 +446,9 @@ __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p)
   if (y != p.ignore_index && n_valid > 0)
     ci = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(n_valid) : p.grad_scale;
   const float lse_l2e = p.lse[r] * 1.4426950408889634f;
-  const float* srow = p.s + static_cast<int64_t>(r) * p.lds;
+  const float* srow = HALF ? nullptr : p.s + static_cast<int64_t>(r) * p.lds;
+  const uint16_t* s16row = HALF ? p.s16 + static_cast<int64_t>(r) * p.lds : nullptr;
+  const float* grow = HALF ? p.gmax + static_cast<int64_t>(r) * p.ldg : nullptr;
   uint16_t* drow = p.dz + static_cast<int64_t>(r) * p.ldd;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -434,9 +457,9 @@ __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p)
     const int64_t dl = y - c;
     const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
     if (p.softcap > 0.f)
-      dlogits_piece<true>(p, srow, drow, c, ci, lse_l2e, label_local);
+      dlogits_piece<true, HALF>(p, srow, s16row, grow, drow, c, ci, lse_l2e, label_local);
     else
-      dlogits_piece<false>(p, srow, drow, c, ci, lse_l2e, label_local);
+      dlogits_piece<false, HALF>(p, srow, s16row, grow, drow, c, ci, lse_l2e, label_local);
   }
 }
 
@@ -496,7 +519,10 @@ cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s) {
   }
   if (p.dzt == nullptr && p.dz != nullptr) {
     dim3 grid((p.vocab + 8191) / 8192, p.rows);
-    dlogits_rows_kernel<<<grid, 256, 0, s>>>(p);
+    if (p.s16 != nullptr)
+      dlogits_rows_kernel<true><<<grid, 256, 0, s>>>(p);
+    else
+      dlogits_rows_kernel<false><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
   }
   dim3 grid((p.vocab + kDzTile - 1) / kDzTile, (p.rows + kDzTile - 1) / kDzTile);
