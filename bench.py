@@ -327,7 +327,7 @@ def _traffic_key(args, w):
     if args.ce_logits:
         return w.name + "-ce_logits"
     return (w.name + ("-lowmem" if args.low_memory else "") + ("-fp32" if args.fp32 else "")
-            + ("-tile128" if args.tile128 else ""))
+            + ("-tile128" if args.tile128 else "") + ("-pair" if getattr(args, "pair", False) else ""))
 
 
 def recorded_traffic(workload, kernel: str, chunk_rows: int = 8192):
@@ -403,7 +403,7 @@ def run_ours(args, w):
     lab = lab_cpu.to(dev)
     gW = torch.zeros(W.shape, dtype=torch.float32, device=dev) if w.mode == "fwd_bwd" else None
     kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows,
-              flags=flce.FLCE_FLAG_TILE128 if args.tile128 else 0)
+              flags=(flce.FLCE_FLAG_TILE128 if args.tile128 else 0) | (flce.FLCE_FLAG_CTA_PAIR if args.pair else 0))
     bkw = dict(low_memory=args.low_memory, vocab_slab=args.vocab_slab)
 
     def step():
@@ -422,7 +422,7 @@ def run_ours(args, w):
         shards = [W[offsets[k]:offsets[k + 1]] for k in range(S)]
         gW_sh = [None if gW is None else gW[offsets[k]:offsets[k + 1]] for k in range(S)]
         gh32 = torch.empty((w.n_rows, w.hidden), dtype=torch.float32, device=dev)
-        vkw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows)
+        vkw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows, flags=kw["flags"])
 
         def step():
             parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, **vkw) for k in range(S)]
@@ -539,7 +539,9 @@ def run_ours(args, w):
                                                        and w.mode == "fwd_bwd" else 1.0),
             "backward": "recompute (low memory)" if (args.low_memory or args.vocab_shards) else "stored logits",
             "gemm_cta_tile": ("128x256, two accumulators" if args.tile128
-                              else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"),
+                              else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"
+                              + ("; each on a CTA pair (cta_group::2), two accumulators per SM"
+                                 if args.pair else "")),
             "roofline": roof, "cpu_baseline": cpu,
             **({"vocab_shards": {"shards": args.vocab_shards, "run": "in turn on one GPU",
                                  "exchange_bytes_per_step": 16 * w.n_rows * args.vocab_shards}}
@@ -693,6 +695,8 @@ def main():
                     help="128-row GEMM tiles with two accumulators (FLCE_FLAG_TILE128), for comparison")
     ap.add_argument("--ce-logits", action="store_true",
                     help="time the cross-entropy on materialised bf16 logits [N, V] instead")
+    ap.add_argument("--pair", action="store_true",
+                    help="256 x 256 GEMM tiles on CTA pairs (FLCE_FLAG_CTA_PAIR)")
     ap.add_argument("--vocab-shards", type=int, default=0,
                     help="time the vocabulary-parallel form with this many shards, run in turn on one GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true")

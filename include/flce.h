@@ -114,6 +114,10 @@ extern "C" {
                                         fill the SMs evenly */
 #define FLCE_FLAG_TILE256 32         /* cross-check: 256 x 256 CTA tiles for every bf16 GEMM
                                         that has them, whatever the tile count */
+#define FLCE_FLAG_CTA_PAIR 64        /* the bf16 GEMMs that take 256 x 256 tiles compute each on a
+                                        pair of CTAs (a cluster of two SMs, tcgen05 cta_group::2):
+                                        each SM holds 128 rows, so its accumulator is double-
+                                        buffered and the epilogue overlaps the next tile's MMAs */
 
 typedef struct flce_params {
   int64_t n_rows;        /* N >= 0 */

@@ -37,6 +37,7 @@ FLCE_FLAG_KMAJOR_BWD = 4
 FLCE_FLAG_RECOMPUTE = 8
 FLCE_FLAG_TILE128 = 16
 FLCE_FLAG_TILE256 = 32
+FLCE_FLAG_CTA_PAIR = 64
 
 FLCE_NUM_KERNELS = 16
 

@@ -482,6 +482,7 @@ struct SlabArgs {
   int h_row0;                // row of map_hc holding the chunk's first row
   const CUtensorMap* map_hc; // h (K-major A of the recompute GEMM)
   const CUtensorMap* map_w;  // W (K-major B)
+  const CUtensorMap* map_w_pair;  // W with 128-row boxes (CTA-pair tiles), or null
   const uint16_t* h_c;       // the chunk's rows of h, row stride ld_hc
   int64_t ld_hc;
   const uint16_t* W;
@@ -502,6 +503,7 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
   const flce_params& p = *a.p;
   Header* hdr = const_cast<Header*>(a.hdr);
   auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, a.sms); };
+  const bool pair = (p.flags & FLCE_FLAG_CTA_PAIR) != 0 && a.map_w_pair != nullptr;
   const int rows = a.rows, H = a.H, V = a.V, slab = a.slab;
   for (int v0 = 0; v0 < V; v0 += slab) {
     const int vs = std::min(slab, V - v0);
@@ -532,8 +534,10 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
     r.col0 = a.col_base + v0;
     r.status = &hdr->status;
     r.timeout_ns = a.timeout;
-    FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wide_for(r), a.map_hc, a.map_w, nullptr, r,
-                                                 std::min(r.m_tiles * r.n_tiles, a.sms), stream));
+    const bool wr = wide_for(r);
+    FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wr, a.map_hc,
+                                                 wr && pair ? a.map_w_pair : a.map_w, nullptr, r,
+                                                 std::min(r.m_tiles * r.n_tiles, a.sms), stream, pair));
     if (a.gh_acc) {
       // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
       CUtensorMap map_a, map_b;
@@ -559,7 +563,7 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
       CUtensorMap map_o;
       if (!encode_f32_out(&map_o, a.gh_acc, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
       FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream));
+                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream, pair));
     }
     if (a.grad_W) {
       // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
@@ -585,7 +589,7 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
       CUtensorMap map_o;
       if (!encode_f32_out(&map_o, a.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
       FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream));
+                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream, pair));
     }
   }
   return FLCE_OK;
@@ -663,10 +667,12 @@ int run(const flce_params* params, const Call& c) {
   const int64_t vocab_total = c.vocab_total > 0 ? c.vocab_total : p.vocab;
   FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, vocab_total, p.ignore_index, hdr, stream));
 
-  CUtensorMap map_h, map_w, map_wt;
+  CUtensorMap map_h, map_w, map_wt, map_w_pair;
+  const bool pair = (p.flags & FLCE_FLAG_CTA_PAIR) != 0 && !simt;
   if (!simt && N > 0) {
     if (!c.host_in && !encode_bf16(&map_h, c.h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
     if (!encode_bf16(&map_w, c.W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+    if (pair && !encode_bf16(&map_w_pair, c.W, H, V, n.ld_w, kBN / 2)) return FLCE_ERR_UNSUPPORTED;
   }
   if (L.need_wt && N > 0) {  // debug paths only
     FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_bf16(static_cast<const uint16_t*>(c.W), n.ld_w, V, H, wt, L.ldwt,
@@ -742,8 +748,9 @@ int run(const flce_params* params, const Call& c) {
       if (store && L.z16 && !encode_f16_out(&map_z, z16, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
       if (store && !L.z16 && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
       const int mode = !store ? EPI_STATS : L.z16 ? EPI_STATS_STORE16 : EPI_STATS_STORE;
-      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(mode, false, false, wide_for(g), &map_hc, &map_w,
-                                             store ? &map_z : nullptr, g, std::min(tiles, sms), stream));
+      const bool wg = wide_for(g);
+      FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc(mode, false, false, wg, &map_hc, wg && pair ? &map_w_pair : &map_w,
+                                             store ? &map_z : nullptr, g, std::min(tiles, sms), stream, pair));
     }
 
     // ---- merge of the vocab-tile statistics
@@ -787,6 +794,7 @@ int run(const flce_params* params, const Call& c) {
       sa.h_row0 = h_row0;
       sa.map_hc = &map_hc;
       sa.map_w = &map_w;
+      sa.map_w_pair = pair ? &map_w_pair : nullptr;
       sa.h_c = h_c;
       sa.ld_hc = ld_hc;
       sa.W = static_cast<const uint16_t*>(c.W);
@@ -862,7 +870,7 @@ int run(const flce_params* params, const Call& c) {
           return FLCE_ERR_UNSUPPORTED;
         }
         FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_BF16, false, !kmajor, wide_for(b), &map_dz, &map_wb, nullptr, b,
-                                                 std::min(b.m_tiles * b.n_tiles, sms), stream));
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, pair && !kmajor));
       }
     }
 
@@ -907,7 +915,7 @@ int run(const flce_params* params, const Call& c) {
         CUtensorMap map_o;
         if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
         FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, !kmajor, !kmajor, wide_for(b), &map_a, &map_b, &map_o, b,
-                                                 std::min(b.m_tiles * b.n_tiles, sms), stream));
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, pair && !kmajor));
       }
     }
   }
@@ -1024,9 +1032,11 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
   FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, loss, acc, stream));
   if (!grads || N == 0) return FLCE_OK;
 
-  CUtensorMap map_h, map_w;
+  CUtensorMap map_h, map_w, map_w_pair;
+  const bool pair = (p.flags & FLCE_FLAG_CTA_PAIR) != 0;
   if (!encode_bf16(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
   if (!encode_bf16(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+  if (pair && !encode_bf16(&map_w_pair, W, H, V, n.ld_w, kBN / 2)) return FLCE_ERR_UNSUPPORTED;
   const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
   for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
     SlabArgs sa;
@@ -1038,6 +1048,7 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
     sa.h_row0 = static_cast<int>(r0);
     sa.map_hc = &map_h;
     sa.map_w = &map_w;
+    sa.map_w_pair = pair ? &map_w_pair : nullptr;
     sa.h_c = static_cast<const uint16_t*>(h) + r0 * n.ld_h;
     sa.ld_hc = n.ld_h;
     sa.W = static_cast<const uint16_t*>(W);

@@ -127,8 +127,13 @@ struct GemmParams {
 // one 512-column accumulator) instead of 128 x 256 tiles with two accumulators;
 // the all-K-major backward combinations always use 128-row tiles. grid is the
 // largest number of CTAs to launch (at most one per tile).
+// pair (with wide): the 256 x 256 tile is computed by a cluster of two CTAs on
+// two SMs with tcgen05 cta_group::2 (M = 256): each CTA loads 128 rows of A
+// and 128 of the 256 rows of B, and keeps its 128 rows of the tile in two
+// 256-column TMEM accumulators, so the epilogue overlaps the next tile's MMAs.
+// A K-major B operand then needs a tensor map with 128-row boxes.
 cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUtensorMap* a, const CUtensorMap* b,
-                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s, bool pair = false);
 // The same GEMM on fp32 operands (tcgen05 kind::tf32), both K-major; modes
 // EPI_STATS, EPI_STATS_STORE, EPI_F32, EPI_ACC_F32.
 cudaError_t launch_gemm_tc_tf32(int mode, bool wide, const CUtensorMap* a, const CUtensorMap* b,

@@ -552,6 +552,256 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant: 256 x 256 tiles over a cluster of two CTAs on two SMs.
+// Each CTA holds 128 rows of A and 128 of the 256 rows of B per K step (32 KB,
+// a 6-stage ring), and one lane of the leader (cluster rank 0) issues
+// tcgen05.mma.cta_group::2 with M = 256, N = 256, which reads both CTAs'
+// shared memory and accumulates each CTA's 128 rows in its own TMEM. Each
+// SM thus pulls the same operand bytes per flop as a single-CTA 256 x 256
+// tile, while its accumulator is only 256 columns: two of them fit in TMEM,
+// and the epilogue of one tile overlaps the MMAs of the next.
+// Protocol: both CTAs wait on their own `empty` slot (the leader's MMA commit
+// is multicast to both), load into their own ring, and count the bytes on the
+// leader's `full` barrier, which the leader arms for both CTAs' bytes. The
+// leader's accumulator commits are multicast to both CTAs' `tfull`; both
+// CTAs' epilogue threads arrive on the leader's `tempty`. A cluster barrier
+// after set-up and before teardown keeps either CTA from signalling a peer
+// that is not there. Every mbarrier wait is bounded as in the kernel above.
+constexpr int kPairStages = 6;
+
+template <int MODE, bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                        const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
+  constexpr int S = kPairStages;
+  constexpr int ABytes = kAStageBytes;      // 128 rows x 64 K
+  constexpr int BBytes = kBStageBytes / 2;  // 128 of the tile's 256 B rows x 64 K
+  static_assert(S * (ABytes + BBytes) <= kStages * (kAStageBytes + kBStageBytes), "ring exceeds the budget");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * ABytes;
+  uint8_t* sStage = smem + kStages * (kAStageBytes + kBStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kEpiStagingBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * 128);  // every epilogue thread of both CTAs arrives (on the leader's)
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+    if (MODE == EPI_STATS_STORE || MODE == EPI_STATS_STORE16 || MODE == EPI_ACC_F32 || MODE == EPI_F32)
+      tma_prefetch_desc(&tma_c);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);  // one warp of each CTA, together
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+  const int units_m = (p.m_tiles + 1) / 2;
+  const int group = p.group_m / 2 > 0 ? p.group_m / 2 : 1;
+  const int total = units_m * p.n_tiles;
+  const int cluster = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // the leader's full[0]
+      int stage = 0;
+      uint32_t phase = 0;
+      bool aborted = false;
+      if (!(p.debug_flags & FLCE_FLAG_TEST_STALL)) {
+        for (int t = cluster; t < total && !aborted; t += n_clusters) {
+          int mu, nb;
+          tile_coords(p, units_m, group, t, mu, nb);
+          const int row_a = p.a_row0 + (mu * 2 + static_cast<int>(rank)) * kBM;
+          const int row_b = p.b_row0 + nb * kBN + static_cast<int>(rank) * (kBN / 2);
+          for (int k = 0; k < p.k_iters; ++k) {
+            if (!wait_bounded(&empty[stage], phase ^ 1u, wc)) {
+              aborted = true;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (ABytes + BBytes));
+            const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
+            if (A_MN) {
+#pragma unroll
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d_pair(sA + stage * ABytes + j * 8192, &tma_a, bar, row_a + j * 64, k * kBK);
+            } else {
+              tma_load_2d_pair(sA + stage * ABytes, &tma_a, bar, k * kBK, row_a);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < (kBN / 2) / 64; ++j)
+                tma_load_2d_pair(sB + stage * BBytes + j * 8192, &tma_b, bar, row_b + j * 64, k * kBK);
+            } else {
+              tma_load_2d_pair(sB + stage * BBytes, &tma_b, bar, k * kBK, row_b);
+            }
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool aborted = false;
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, A_MN, B_MN);
+      const uint32_t a_base = smem_u32(sA);
+      const uint32_t b_base = smem_u32(sB);
+      for (int t = cluster; t < total && !aborted; t += n_clusters) {
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int k = 0; k < p.k_iters; ++k) {
+          if (!wait_bounded(&full[stage], phase, wc)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = a_base + stage * ABytes;
+          const uint32_t b0 = b_base + stage * BBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(a0 + kk * 2048) : sdesc_kmajor_sw128(a0 + kk * 32);
+            const uint64_t bd = B_MN ? sdesc_mnmajor_sw128(b0 + kk * 2048) : sdesc_kmajor_sw128(b0 + kk * 32);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair(&empty[stage], 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        tc_commit_pair(&tfull[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All issued tensor-core work must finish before either CTA frees TMEM.
+      tc_commit_pair(mma_done, 0x1);
+      wait_drain(mma_done, 0, p.timeout_ns, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    float coef = 0.f;
+    if (MODE == EPI_DZ) {
+      const int64_t nv = p.hdr->n_valid;
+      if (nv > 0) coef = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(nv) : p.grad_scale;
+    }
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    EpiStage es{sStage + (warp - 2) * 2 * kStageBufBytes, 0, 2, 0, p.store_hint != 0};
+    if (es.hint) es.policy = l2_policy_evict_first();
+    const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);  // the leader's tempty[0]
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cluster; t < total; t += n_clusters) {
+      int mu, nb;
+      tile_coords(p, units_m, group, t, mu, nb);
+      bool ok = wait_bounded(&tfull[acc], acc_phase, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int mb = mu * 2 + static_cast<int>(rank);
+      if (mb < p.m_tiles) {
+        const uint32_t tcol = t_lane + static_cast<uint32_t>(acc * kBN);
+        if (MODE == EPI_STATS) {
+          epilogue_stats<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_STATS_STORE) {
+          epilogue_stats<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_STATS_STORE16) {
+          epilogue_stats<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_BF16) {
+          epilogue_bf16(p, tcol, mb, nb, row);
+        } else if (MODE == EPI_ACC_F32) {
+          epilogue_out_f32<true>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else if (MODE == EPI_F32) {
+          epilogue_out_f32<false>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+        } else {
+          epilogue_dz(p, tcol, mb, nb, row, coef);
+        }
+      }
+      tc_fence_before_sync();
+      if (rank == 0)
+        mbar_arrive(&tempty[acc]);
+      else
+        mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if ((MODE == EPI_STATS_STORE || MODE == EPI_STATS_STORE16 || MODE == EPI_ACC_F32 || MODE == EPI_F32) &&
+        lane == 0)
+      bulk_wait_group<0>();
+  }
+
+  tc_fence_before_sync();
+  cluster_sync_all();  // neither CTA leaves while the other may still signal it
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+template <int MODE, bool A_MN, bool B_MN>
+static cudaError_t launch_mode_pair(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
+                                    const GemmParams& p, int grid, cudaStream_t s) {
+  static std::atomic<bool> configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(gemm_tc_pair_kernel<MODE, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev].store(true, std::memory_order_release);
+  }
+  // one cluster of two CTAs per 256 x 256 tile at most, and an even grid
+  const int units = ((p.m_tiles + 1) / 2) * p.n_tiles;
+  int clusters = grid / 2;
+  if (clusters > units) clusters = units;
+  if (clusters < 1) clusters = 1;
+  gemm_tc_pair_kernel<MODE, A_MN, B_MN><<<2 * clusters, kGemmThreads, kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a, p);
+  return cudaGetLastError();
+}
+
 template <int MODE, bool A_MN, bool B_MN, bool TF32 = false, int TMH = 1>
 static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                                const GemmParams& p, int grid, cudaStream_t s) {
@@ -579,10 +829,27 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
 }
 
 cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUtensorMap* a, const CUtensorMap* b,
-                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
+                           const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s, bool pair) {
   if ((mode == EPI_STATS_STORE || mode == EPI_STATS_STORE16 || mode == EPI_ACC_F32 || mode == EPI_F32) &&
       c == nullptr)
     return cudaErrorInvalidValue;
+  // pair: 256 x 256 tiles over CTA pairs (cta_group::2); a K-major B map must
+  // then have 128-row boxes (each CTA loads half of the tile's B rows).
+  if (wide && pair) {
+    if (!a_mn && !b_mn) {
+      switch (mode) {
+        case EPI_STATS: return launch_mode_pair<EPI_STATS, false, false>(a, b, c, p, grid, s);
+        case EPI_STATS_STORE: return launch_mode_pair<EPI_STATS_STORE, false, false>(a, b, c, p, grid, s);
+        case EPI_STATS_STORE16: return launch_mode_pair<EPI_STATS_STORE16, false, false>(a, b, c, p, grid, s);
+        case EPI_DZ: return launch_mode_pair<EPI_DZ, false, false>(a, b, c, p, grid, s);
+        default: break;
+      }
+    }
+    if (!a_mn && b_mn && mode == EPI_BF16) return launch_mode_pair<EPI_BF16, false, true>(a, b, c, p, grid, s);
+    if (!a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode_pair<EPI_ACC_F32, false, true>(a, b, c, p, grid, s);
+    if (a_mn && b_mn && mode == EPI_ACC_F32) return launch_mode_pair<EPI_ACC_F32, true, true>(a, b, c, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
   // The combinations the engine uses: the forward GEMM (both K-major), grad_h
   // (dz K-major, W MN-major or its transpose K-major), grad_W (dz and h_c
   // MN-major, or their transposes K-major).
