@@ -385,6 +385,21 @@ def test_workload_recipe_is_deterministic_and_shaped():
     assert abs(float((zv == 0).float().mean()) - 1 / hz) < 0.02
 
 
+def test_input_generator_is_splitmix64():
+    """The input streams are SplitMix64: its published first outputs for seed
+    1234567 (the test vector of the reference C implementation)."""
+    got = workloads.draws(np.uint64(1234567), 0, 5)
+    assert [int(x) for x in got] == [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                                     4593380528125082431, 16408922859458223821]
+    # draws are addressed by index: a window equals the same slice of a longer run
+    key = np.uint64(99)
+    assert np.array_equal(workloads.draws(key, 1000, 7), workloads.draws(key, 0, 1007)[1000:])
+    # normals: mean 0, variance 1, and a block boundary does not change them
+    h = workloads.make_hidden(2048, 4096, 5).float()
+    assert abs(h.mean().item()) < 5e-3 and abs(h.std().item() - 1.0) < 5e-3
+    assert torch.equal(workloads.make_hidden(3, 4096, 5), workloads.make_hidden(2048, 4096, 5)[:3])
+
+
 # --- cross-entropy on materialised logits -------------------------------------------
 def test_ce_logits_matches_torch_and_autograd():
     from oracle import oracle_ce_logits

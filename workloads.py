@@ -11,19 +11,34 @@ head (hidden 4096, vocab 128256), and the SpecForge DSpine page's flattened
 frozen draft-proposal projection (section Changes: proposal rows flattened,
 the frozen vocabulary projection applied, the shape restored).
 
-Recipe (fixed so results are reproducible bit for bit):
-  * h ~ N(0, 1) drawn in fp32, rounded to bf16 (round to nearest even);
-  * W ~ N(0, 0.02^2) drawn in fp32, rounded to bf16;
-  * labels uniform in [0, V), or Zipf(s) with p(k) ~ (k+1)^-s sampled by
-    inverse CDF (token id = rank);
-  * exactly round(frac * N) rows set to the ignore index, picked by a seeded
-    permutation;
-  * one torch CPU generator per tensor, seeded seed*16 + {1: h, 2: W, 3: labels,
-    4: ignore mask}.
+Recipe (fixed so that results are reproducible bit for bit, on any machine):
+  * every random number comes from a counter-based generator: SplitMix64
+    (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+    OOPSLA 2014) applied to key + (i + 1) * 0x9E3779B97F4A7C15 for the i-th
+    draw of a tensor. Only 64-bit integer arithmetic, so the same bits come out
+    on x86 and Arm (torch's own normal sampler does not: its vectorised paths
+    differ between the two);
+  * h ~ N(0, 1): Box-Muller in fp64 on pairs of 53-bit uniforms (element 2k
+    takes the cosine, 2k + 1 the sine), rounded to fp32, then to bf16 (round to
+    nearest even);
+  * W ~ N(0, 0.02^2): the same normals times 0.02 in fp64, then fp32, then bf16;
+  * labels uniform in [0, V) (the top 32 bits of a draw times V, shifted down
+    32), or Zipf(s) with p(k) ~ (k+1)^-s sampled by inverse CDF (token id =
+    rank);
+  * exactly round(frac * N) rows set to the ignore index: the rows with the
+    smallest draws of their own stream;
+  * one stream per tensor, keyed seed*16 + {1: h, 2: W, 3: labels, 4: ignore
+    mask}.
+The fp64 log, sqrt, cos and sin of Box-Muller may differ by an ulp between
+math libraries; a bf16 result changes only when the fp64 value lies within
+that ulp of a bf16 rounding midpoint (about 1e-13 per element). The tests that
+compare with stored oracle results check a hash of the inputs first.
 """
 from __future__ import annotations
 
 import dataclasses
+import functools
+import os
 from typing import Optional, Tuple
 
 import numpy as np
@@ -68,56 +83,105 @@ WORKLOADS = {
 }
 
 
-def _gen(seed: int, slot: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
-    g.manual_seed(seed * 16 + slot)
-    return g
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_MIX1 = np.uint64(0xBF58476D1CE4E5B9)
+_MIX2 = np.uint64(0x94D049BB133111EB)
+_BLOCK = 1 << 22            # elements per generation task
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    """SplitMix64's output function on uint64 (wrapping arithmetic)."""
+    z = z ^ (z >> np.uint64(30))
+    z = z * _MIX1
+    z = z ^ (z >> np.uint64(27))
+    z = z * _MIX2
+    return z ^ (z >> np.uint64(31))
+
+
+def _key(seed: int, slot: int) -> np.uint64:
+    return _mix(np.asarray([seed * 16 + slot], dtype=np.uint64) * _GAMMA)[0]
+
+
+def draws(key: np.uint64, i0: int, n: int) -> np.ndarray:
+    """Draws i0 .. i0+n-1 of the stream `key`: uint64 [n]."""
+    i = np.arange(i0 + 1, i0 + n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix(key + i * _GAMMA)
+
+
+def _normals_block(key: np.uint64, i0: int, n: int, scale: float) -> np.ndarray:
+    """Normals i0 .. i0+n-1 of the stream (Box-Muller on draw pairs), times
+    scale, as fp32."""
+    k0, k1 = i0 // 2, (i0 + n + 1) // 2
+    d = draws(key, 2 * k0, 2 * (k1 - k0))
+    u1 = ((d[0::2] >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * 2.0 ** -53   # (0, 1]
+    u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53                    # [0, 1)
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = (2.0 * np.pi) * u2
+    z = np.empty(2 * (k1 - k0))
+    z[0::2] = r * np.cos(t)
+    z[1::2] = r * np.sin(t)
+    z = z[i0 - 2 * k0:i0 - 2 * k0 + n]
+    if scale != 1.0:
+        z = z * scale
+    return z.astype(np.float32)
+
+
+def _normal_bf16(shape, key: np.uint64, scale: float) -> torch.Tensor:
+    """A bf16 tensor of normals (row-major element index = draw index),
+    generated in blocks on a thread pool (numpy releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+
+    def job(i0):
+        m = min(_BLOCK, n - i0)
+        out[i0:i0 + m] = _normals_block(key, i0, m, scale)
+
+    with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+        list(ex.map(job, range(0, n, _BLOCK)))
+    return torch.from_numpy(out).view(*shape).to(torch.bfloat16)
+
+
+@functools.lru_cache(maxsize=4)
+def _cached_normal_bf16(shape, seed: int, slot: int, scale: float) -> torch.Tensor:
+    return _normal_bf16(shape, _key(seed, slot), scale)
 
 
 def make_hidden(n_rows: int, hidden: int, seed: int) -> torch.Tensor:
-    """h [N, H] bf16, N(0,1) rounded to bf16. Drawn in row blocks to bound host memory."""
-    g = _gen(seed, 1)
-    out = torch.empty((n_rows, hidden), dtype=torch.bfloat16)
-    step = max(1, (1 << 26) // max(hidden, 1))
-    for r0 in range(0, n_rows, step):
-        r1 = min(n_rows, r0 + step)
-        out[r0:r1] = torch.randn((r1 - r0, hidden), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    return out
+    """h [N, H] bf16, N(0,1) rounded to bf16. Row i of a smaller N equals row i
+    of a larger one. (A fresh copy of a small per-process cache: a full-size
+    head takes seconds to draw.)"""
+    return _cached_normal_bf16((n_rows, hidden), seed, 1, 1.0).clone()
 
 
 def make_weight(vocab: int, hidden: int, seed: int, std: float = 0.02) -> torch.Tensor:
-    """W [V, H] bf16, N(0, std^2) rounded to bf16. Drawn in row blocks."""
-    g = _gen(seed, 2)
-    out = torch.empty((vocab, hidden), dtype=torch.bfloat16)
-    step = max(1, (1 << 26) // max(hidden, 1))
-    for r0 in range(0, vocab, step):
-        r1 = min(vocab, r0 + step)
-        out[r0:r1] = (torch.randn((r1 - r0, hidden), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
-    return out
+    """W [V, H] bf16, N(0, std^2) rounded to bf16 (a fresh copy, as make_hidden)."""
+    return _cached_normal_bf16((vocab, hidden), seed, 2, float(std)).clone()
 
 
 def make_labels(n_rows: int, vocab: int, seed: int, ignore_frac: float,
                 kind: str = "uniform", zipf_s: float = 1.1,
                 ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
     """labels [N] int64: uniform or Zipf ids, with exactly round(frac*N) ignored rows."""
-    g = _gen(seed, 3)
+    d = draws(_key(seed, 3), 0, n_rows)
     if kind == "uniform":
-        lab = torch.randint(0, vocab, (n_rows,), generator=g, dtype=torch.int64)
+        lab = (((d >> np.uint64(32)) * np.uint64(vocab)) >> np.uint64(32)).astype(np.int64)
     elif kind == "zipf":
         ranks = np.arange(1, vocab + 1, dtype=np.float64)
         p = ranks ** (-zipf_s)
         cdf = np.cumsum(p)
         cdf /= cdf[-1]
-        u = torch.rand((n_rows,), generator=g, dtype=torch.float64).numpy()
+        u = (d >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
         idx = np.searchsorted(cdf, u, side="right")
-        lab = torch.from_numpy(np.minimum(idx, vocab - 1).astype(np.int64))
+        lab = np.minimum(idx, vocab - 1).astype(np.int64)
     else:
         raise ValueError(f"unknown label distribution {kind!r}")
     n_ign = int(round(ignore_frac * n_rows))
     if n_ign > 0:
-        perm = torch.randperm(n_rows, generator=_gen(seed, 4))[:n_ign]
-        lab[perm] = ignore_index
-    return lab
+        order = np.argsort(draws(_key(seed, 4), 0, n_rows), kind="stable")
+        lab[order[:n_ign]] = ignore_index
+    return torch.from_numpy(lab)
 
 
 def make_inputs(w: Workload, n_rows: Optional[int] = None):
