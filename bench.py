@@ -327,7 +327,8 @@ def _traffic_key(args, w):
     if args.ce_logits:
         return w.name + "-ce_logits"
     return (w.name + ("-lowmem" if args.low_memory else "") + ("-fp32" if args.fp32 else "")
-            + ("-tile128" if args.tile128 else "") + ("-pair" if getattr(args, "pair", False) else ""))
+            + ("-tile128" if args.tile128 else "") + ("-pair" if getattr(args, "pair", False) else "")
+            + ("-3pass" if getattr(args, "fp32_3pass", False) else ""))
 
 
 def recorded_traffic(workload, kernel: str, chunk_rows: int = 8192):
@@ -403,7 +404,8 @@ def run_ours(args, w):
     lab = lab_cpu.to(dev)
     gW = torch.zeros(W.shape, dtype=torch.float32, device=dev) if w.mode == "fwd_bwd" else None
     kw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows,
-              flags=(flce.FLCE_FLAG_TILE128 if args.tile128 else 0) | (flce.FLCE_FLAG_CTA_PAIR if args.pair else 0))
+              flags=(flce.FLCE_FLAG_TILE128 if args.tile128 else 0) | (flce.FLCE_FLAG_CTA_PAIR if args.pair else 0)
+              | (flce.FLCE_FLAG_F32_3PASS if args.fp32_3pass else 0))
     bkw = dict(low_memory=args.low_memory, vocab_slab=args.vocab_slab)
 
     def step():
@@ -530,13 +532,16 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "ms_per_step_median": statistics.median(per_step), "ms_per_step_min": min(per_step),
-            "vs_baseline": None, "dtype": "f32 (tf32 tensor cores)" if args.fp32 else "bf16", "data": "synthetic",
+            "vs_baseline": None,
+            "dtype": ("f32 (three-pass tf32 products, fp32 accuracy)" if args.fp32_3pass else
+                      "f32 inputs, tf32 products" if args.fp32 else "bf16"), "data": "synthetic",
             "config": _config(w, args.chunk_rows, chunk_used),
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
             "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,
             "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if (args.low_memory or args.vocab_shards)
-                                                       and w.mode == "fwd_bwd" else 1.0),
+                                                       and w.mode == "fwd_bwd" else 1.0)
+                                                    * (3.0 if args.fp32_3pass else 1.0),
             "backward": "recompute (low memory)" if (args.low_memory or args.vocab_shards) else "stored logits",
             "gemm_cta_tile": ("128x256, two accumulators" if args.tile128
                               else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"
@@ -691,6 +696,8 @@ def main():
                     help="recompute backward: no stored logits, dlogits per vocab slab")
     ap.add_argument("--vocab-slab", type=int, default=0)
     ap.add_argument("--fp32", action="store_true", help="fp32 h and W: the tf32 tensor-core path")
+    ap.add_argument("--fp32-3pass", action="store_true",
+                    help="with --fp32: three-pass tf32 products for fp32 accuracy (FLCE_FLAG_F32_3PASS)")
     ap.add_argument("--tile128", action="store_true",
                     help="128-row GEMM tiles with two accumulators (FLCE_FLAG_TILE128), for comparison")
     ap.add_argument("--ce-logits", action="store_true",
@@ -707,6 +714,8 @@ def main():
         import dataclasses
         w = dataclasses.replace(w, name=f"{w.name}-small", n_rows=args.rows or w.n_rows,
                                 vocab=args.vocab or w.vocab)
+    if args.fp32_3pass:
+        args.fp32 = True
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -114,6 +114,12 @@ extern "C" {
                                         fill the SMs evenly */
 #define FLCE_FLAG_TILE256 32         /* cross-check: 256 x 256 CTA tiles for every bf16 GEMM
                                         that has them, whatever the tile count */
+#define FLCE_FLAG_F32_3PASS 128     /* fp32 operands (FLCE_DTYPE_F32): every product as three tf32
+                                        products, hi*hi + hi*lo + lo*hi with hi = x rounded to tf32
+                                        and lo = x - hi, for about fp32 accuracy (the default fp32
+                                        path multiplies in tf32, a 10-bit mantissa); 3x the tensor
+                                        work, 128 x 256 tiles, and hi / lo copies of W, W^T, h_c,
+                                        h_c^T, dz and dz^T in the workspace */
 #define FLCE_FLAG_CTA_PAIR 64        /* the bf16 GEMMs that take 256 x 256 tiles compute each on a
                                         pair of CTAs (a cluster of two SMs, tcgen05 cta_group::2):
                                         each SM holds 128 rows, so its accumulator is double-
@@ -136,8 +142,10 @@ typedef struct flce_params {
   int64_t vocab_slab;    /* FLCE_FLAG_RECOMPUTE: vocab columns per slab (0 => 16384);
                             rounded up to 256 */
   int32_t dtype;         /* element type of h, W and grad_h: FLCE_DTYPE_BF16 (default) or
-                            FLCE_DTYPE_F32 (fp32 operands on the tf32 tensor cores; fp32
-                            grad_h; not with FLCE_FLAG_RECOMPUTE or FLCE_FLAG_SIMT_GEMM) */
+                            FLCE_DTYPE_F32 (fp32 operands and fp32 grad_h; the products are
+                            tf32 products - 10-bit mantissas, fp32 accumulation - unless
+                            FLCE_FLAG_F32_3PASS asks for fp32 accuracy; not with
+                            FLCE_FLAG_RECOMPUTE or FLCE_FLAG_SIMT_GEMM) */
 } flce_params;
 
 /* Fills the defaults: softcap 0, out_mult 1, ignore_index -100, MEAN,
@@ -325,7 +333,7 @@ int64_t flce_launch_count(void);
  * flce_profile_begin(0) stops. flce_profile_read synchronises the recorded
  * events and fills, for kernel ids 0..n-1, the launch count and the summed
  * milliseconds; it returns the number of kernel ids (FLCE_NUM_KERNELS). */
-#define FLCE_NUM_KERNELS 16
+#define FLCE_NUM_KERNELS 17
 int flce_profile_begin(int enable);
 int flce_profile_read(int64_t* launches, double* total_ms, int n);
 const char* flce_kernel_name(int id);

@@ -23,7 +23,7 @@ import torch
 
 from . import _lib
 from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL,  # noqa: F401
-                   FLCE_FLAG_TILE128, FLCE_FLAG_TILE256, FLCE_FLAG_CTA_PAIR, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,
+                   FLCE_FLAG_TILE128, FLCE_FLAG_TILE256, FLCE_FLAG_CTA_PAIR, FLCE_FLAG_F32_3PASS, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,
                    FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
 
 __all__ = [

@@ -38,8 +38,9 @@ FLCE_FLAG_RECOMPUTE = 8
 FLCE_FLAG_TILE128 = 16
 FLCE_FLAG_TILE256 = 32
 FLCE_FLAG_CTA_PAIR = 64
+FLCE_FLAG_F32_3PASS = 128
 
-FLCE_NUM_KERNELS = 16
+FLCE_NUM_KERNELS = 17
 
 EXPORTED = [
     "flce_default_params", "flce_workspace_size", "flce_chunk_rows", "flce_ce_only", "flce_ce_only_noalloc", "flce_forward",

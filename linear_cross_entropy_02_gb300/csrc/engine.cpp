@@ -77,7 +77,8 @@ struct LaunchScope {
 const char* const kKernelNames[FLCE_NUM_KERNELS] = {
     "prologue", "fwd_gemm_stats", "merge", "dlogits", "grad_h_gemm",
     "grad_W_gemm", "transpose_W", "transpose_h", "finish", "simt_stats",
-    "ce_stats", "ce_grad", "recompute_dz_gemm", "convert_grad_h", "scale_gradient", "vp_merge"};
+    "ce_stats", "ce_grad", "recompute_dz_gemm", "convert_grad_h", "scale_gradient", "vp_merge",
+    "split_tf32"};
 
 // ------------------------------------------------------------ device info
 // Per-device cache of the SM count and compute capability, packed into one
@@ -187,6 +188,11 @@ struct Layout {
   int64_t ldg;      // gmax row stride (ldz / 32)
   size_t off_hdr, off_bl, off_bc, off_pmax, off_psum, off_pidx, off_tgt, off_lse, off_z, off_gmax, off_dz, off_dzt,
       off_wt, off_ht, off_gh32, total;
+  // three-pass tf32 (fp32 operands with FLCE_FLAG_F32_3PASS): hi / lo copies
+  // of W and h_c for the forward GEMM, and lo halves beside W^T, h_c^T, dz
+  // and dz^T (which then hold the hi halves)
+  bool split;
+  size_t off_whi, off_wlo, off_hhi, off_hlo, off_wtlo, off_htlo, off_dzlo, off_dztlo;
   // host inputs (flce_forward_backward_from_host): two chunk buffers of h, all
   // labels, and the two result scalars before they are copied to the host
   bool host_in;
@@ -348,6 +354,15 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
   L->off_ht = L->need_ht ? take(es * p.hidden * L->ldht) : 0;
   L->off_gh32 = L->need_gh32 ? take(sizeof(float) * L->C * p.hidden) : 0;
+  L->split = f32 && !ce && (p.flags & FLCE_FLAG_F32_3PASS) != 0;
+  L->off_whi = L->split ? take(sizeof(float) * p.vocab * p.hidden) : 0;
+  L->off_wlo = L->split ? take(sizeof(float) * p.vocab * p.hidden) : 0;
+  L->off_hhi = L->split ? take(sizeof(float) * L->C * p.hidden) : 0;
+  L->off_hlo = L->split ? take(sizeof(float) * L->C * p.hidden) : 0;
+  L->off_wtlo = L->split && L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
+  L->off_htlo = L->split && L->need_ht ? take(es * p.hidden * L->ldht) : 0;
+  L->off_dzlo = L->split && L->need_dz ? take(es * L->C * L->ldd) : 0;
+  L->off_dztlo = L->split && L->need_dzt ? take(es * round_up(p.vocab, kBM) * L->ldt) : 0;
   const size_t h_es = p.dtype == FLCE_DTYPE_F32 ? 4 : 2;
   L->hstage_bytes = L->host_in ? (static_cast<size_t>(L->C) * p.hidden * h_es + 255) / 256 * 256 : 0;
   L->off_hstage = L->host_in ? take(2 * L->hstage_bytes) : 0;
@@ -1130,14 +1145,32 @@ int run_f32(const Norm& n, const Call& c) {
   }
 
   FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, p.vocab, p.ignore_index, hdr, stream));
-  CUtensorMap map_h, map_w, map_wt;
+  // Three-pass tf32: every GEMM operand as hi = tf32(x) and lo = x - hi.
+  const bool split = L.split;
+  float* w_hi = split ? reinterpret_cast<float*>(ws + L.off_whi) : nullptr;
+  float* w_lo = split ? reinterpret_cast<float*>(ws + L.off_wlo) : nullptr;
+  float* h_hi = split ? reinterpret_cast<float*>(ws + L.off_hhi) : nullptr;
+  float* h_lo = split ? reinterpret_cast<float*>(ws + L.off_hlo) : nullptr;
+  float* wt_lo = split && L.need_wt ? reinterpret_cast<float*>(ws + L.off_wtlo) : nullptr;
+  float* ht_lo = split && L.need_ht ? reinterpret_cast<float*>(ws + L.off_htlo) : nullptr;
+  float* dz_lo = split && L.need_dz ? reinterpret_cast<float*>(ws + L.off_dzlo) : nullptr;
+  float* dzt_lo = split && L.need_dzt ? reinterpret_cast<float*>(ws + L.off_dztlo) : nullptr;
+  const bool wide_ok = !split;  // the split runs on 128-row tiles
+  CUtensorMap map_h, map_w, map_wt, map_w_lo, map_wt_lo;
   if (N > 0) {
-    if (!c.host_in && !encode_f32_in(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
-    if (!encode_f32_in(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
+    if (!c.host_in && !split && !encode_f32_in(&map_h, h, H, N, n.ld_h, kBM)) return FLCE_ERR_UNSUPPORTED;
+    if (split) {
+      FLCE_LAUNCH(K_SPLIT, launch_split_f32(W, n.ld_w, V, H, w_hi, w_lo, H, stream));
+      if (!encode_f32_in(&map_w, w_hi, H, V, H, kBN)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_f32_in(&map_w_lo, w_lo, H, V, H, kBN)) return FLCE_ERR_UNSUPPORTED;
+    } else if (!encode_f32_in(&map_w, W, H, V, n.ld_w, kBN)) {
+      return FLCE_ERR_UNSUPPORTED;
+    }
   }
   if (L.need_wt && N > 0) {
-    FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_f32(W, n.ld_w, V, H, wt, L.ldwt, stream));
+    FLCE_LAUNCH(K_TRANSPOSE_W, launch_transpose_f32(W, n.ld_w, V, H, wt, L.ldwt, stream, wt_lo));
     if (!encode_f32_in(&map_wt, wt, V, H, L.ldwt, kBN)) return FLCE_ERR_UNSUPPORTED;
+    if (split && !encode_f32_in(&map_wt_lo, wt_lo, V, H, L.ldwt, kBN)) return FLCE_ERR_UNSUPPORTED;
   }
   for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
     const int rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
@@ -1146,13 +1179,19 @@ int run_f32(const Norm& n, const Call& c) {
     const float* h_c = h + r0 * n.ld_h;
     int64_t ld_hc = n.ld_h;
     int h_row0 = static_cast<int>(r0);
-    CUtensorMap map_hc = map_h;
+    CUtensorMap map_hc = map_h, map_hc_lo;
     if (c.host_in) {
       h_c = static_cast<const float*>(hs.wait_chunk(r0 / L.C));
       if (!h_c) return FLCE_ERR_CUDA;
       ld_hc = H;
       h_row0 = 0;
-      if (!encode_f32_in(&map_hc, h_c, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (!split && !encode_f32_in(&map_hc, h_c, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+    }
+    if (split) {  // this chunk's rows as hi / lo
+      FLCE_LAUNCH(K_SPLIT, launch_split_f32(h_c, ld_hc, rows, H, h_hi, h_lo, H, stream));
+      if (!encode_f32_in(&map_hc, h_hi, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (!encode_f32_in(&map_hc_lo, h_lo, H, rows, H, kBM)) return FLCE_ERR_UNSUPPORTED;
+      h_row0 = 0;
     }
     GemmParams g{};
     std::memset(&g, 0, sizeof(g));
@@ -1185,9 +1224,10 @@ int run_f32(const Norm& n, const Call& c) {
     g.store_hint = store ? 1 : 0;
     CUtensorMap map_z;
     if (store && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
-    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS, pick_wide(p.flags, g, sms), &map_hc, &map_w,
-                                                store ? &map_z : nullptr, g,
-                                                std::min(g.m_tiles * g.n_tiles, sms), stream));
+    FLCE_LAUNCH(K_FWD_GEMM, launch_gemm_tc_tf32(store ? EPI_STATS_STORE : EPI_STATS,
+                                                wide_ok && pick_wide(p.flags, g, sms), &map_hc, &map_w,
+                                                store ? &map_z : nullptr, g, std::min(g.m_tiles * g.n_tiles, sms),
+                                                stream, split ? &map_hc_lo : nullptr, split ? &map_w_lo : nullptr));
     MergeParams mp{};
     mp.rows = rows;
     mp.n_vtiles = static_cast<int>(L.n_vtiles);
@@ -1224,6 +1264,8 @@ int run_f32(const Norm& n, const Call& c) {
     dp.ldd = L.ldd;
     dp.dzt32 = gw ? dzt : nullptr;
     dp.ldt = L.ldt;
+    dp.dz32_lo = gh ? dz_lo : nullptr;
+    dp.dzt32_lo = gw ? dzt_lo : nullptr;
     FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
 
     if (gh) {  // grad_h_c = m dz W: A = dz [C][V], B = W^T [H][V], fp32 output
@@ -1241,14 +1283,16 @@ int run_f32(const Norm& n, const Call& c) {
       b.N_valid = H;
       b.status = &hdr->status;
       b.timeout_ns = timeout;
-      CUtensorMap map_a, map_o;
+      CUtensorMap map_a, map_o, map_a_lo;
       if (!encode_f32_in(&map_a, dz, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (split && !encode_f32_in(&map_a_lo, dz_lo, V, rows, L.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_out(&map_o, static_cast<float*>(c.grad_h) + r0 * H, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc_tf32(EPI_F32, pick_wide(p.flags, b, sms), &map_a, &map_wt, &map_o, b,
-                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
+      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc_tf32(EPI_F32, wide_ok && pick_wide(p.flags, b, sms), &map_a, &map_wt,
+                                                    &map_o, b, std::min(b.m_tiles * b.n_tiles, sms), stream,
+                                                    split ? &map_a_lo : nullptr, split ? &map_wt_lo : nullptr));
     }
     if (gw) {  // grad_W += m dz^T h_c: A = dz^T [V][C], B = h_c^T [H][C]
-      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_f32(h_c, ld_hc, rows, H, ht, L.ldht, stream));
+      FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_f32(h_c, ld_hc, rows, H, ht, L.ldht, stream, ht_lo));
       GemmParams b{};
       std::memset(&b, 0, sizeof(b));
       b.M = V;
@@ -1263,12 +1307,15 @@ int run_f32(const Norm& n, const Call& c) {
       b.N_valid = H;
       b.status = &hdr->status;
       b.timeout_ns = timeout;
-      CUtensorMap map_a, map_b, map_o;
+      CUtensorMap map_a, map_b, map_o, map_a_lo, map_b_lo;
       if (!encode_f32_in(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_in(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
+      if (split && !encode_f32_in(&map_a_lo, dzt_lo, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
+      if (split && !encode_f32_in(&map_b_lo, ht_lo, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
       if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc_tf32(EPI_ACC_F32, pick_wide(p.flags, b, sms), &map_a, &map_b, &map_o, b,
-                                                    std::min(b.m_tiles * b.n_tiles, sms), stream));
+      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc_tf32(EPI_ACC_F32, wide_ok && pick_wide(p.flags, b, sms), &map_a, &map_b,
+                                                    &map_o, b, std::min(b.m_tiles * b.n_tiles, sms), stream,
+                                                    split ? &map_a_lo : nullptr, split ? &map_b_lo : nullptr));
     }
   }
   FLCE_LAUNCH(K_FINISH, launch_finish(hdr, p.reduction, out_loss, out_acc, stream));

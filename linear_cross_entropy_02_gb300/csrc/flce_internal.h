@@ -62,6 +62,7 @@ enum KernelId {
   K_CONVERT = 13,
   K_SCALE = 14,
   K_VP_MERGE = 15,
+  K_SPLIT = 16,
 };
 
 enum EpiMode {
@@ -136,8 +137,11 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
                            const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s, bool pair = false);
 // The same GEMM on fp32 operands (tcgen05 kind::tf32), both K-major; modes
 // EPI_STATS, EPI_STATS_STORE, EPI_F32, EPI_ACC_F32.
+// a_lo / b_lo (both or neither): the three-pass split for fp32 accuracy; a and
+// b then hold hi = tf32(x), a_lo and b_lo lo = x - hi (128-row tiles).
 cudaError_t launch_gemm_tc_tf32(int mode, bool wide, const CUtensorMap* a, const CUtensorMap* b,
-                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s);
+                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s,
+                                const CUtensorMap* a_lo = nullptr, const CUtensorMap* b_lo = nullptr);
 // Debug GEMM on the fp32 FMA pipes; writes alpha*acc to zbuf for the statistics
 // modes (then run launch_stats_from_z) and behaves like the tensor-core GEMM
 // for the plain modes.
@@ -217,14 +221,20 @@ struct DlogitParams {
   int64_t ldt;
   float* dz32;      // fp32-operand path: dz [rows][ldd] and dz^T [vocab][ldt] in fp32
   float* dzt32;
+  float* dz32_lo;   // three-pass tf32: dz32 / dzt32 then get tf32(dz), these dz - tf32(dz)
+  float* dzt32_lo;
 };
 cudaError_t launch_dlogits(const DlogitParams& p, cudaStream_t s);
 
 // out [cols][ldo] = in [rows][ldi]^T, bf16 / fp32.
 cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int cols, uint16_t* out,
                                   int64_t ldo, cudaStream_t s);
+// out_lo non-null: out receives tf32(x) and out_lo x - tf32(x) (the split).
 cudaError_t launch_transpose_f32(const float* in, int64_t ldi, int rows, int cols, float* out, int64_t ldo,
-                                 cudaStream_t s);
+                                 cudaStream_t s, float* out_lo = nullptr);
+// hi / lo [rows][ldo] = the tf32 split of in [rows][ldi] (cols columns).
+cudaError_t launch_split_f32(const float* in, int64_t ldi, int rows, int cols, float* hi, float* lo, int64_t ldo,
+                             cudaStream_t s);
 
 // Columns per warp task of the cross-entropy-on-logits statistics.
 constexpr int kCeTile = 8192;

@@ -297,14 +297,24 @@ __device__ __forceinline__ void epilogue_dz(const GemmParams& p, uint32_t tcol, 
 // epilogue warps, two per TMEM lane quarter (warps 2-5 rows 0-127, warps 6-9
 // rows 128-255, one staging buffer each), so the tensor cores wait for half
 // as long between tiles as four warps would make them.
-template <int MODE, bool A_MN, bool B_MN, bool TF32, int TMH>
+// SPLIT (tf32 only, 128-row tiles): three-pass tf32 for fp32 accuracy. Each
+// fp32 operand comes as two arrays, hi = x rounded to tf32 and lo = x - hi
+// (tma_a / tma_b and tma_a2 / tma_b2), and every K step issues
+// hi*hi + hi*lo + lo*hi into the same accumulator; the dropped lo*lo term
+// and the tf32 rounding of lo are about 2^-21 of each product. A stage then
+// holds both halves of A and B (96 KB), so the ring has two stages.
+template <int MODE, bool A_MN, bool B_MN, bool TF32, int TMH, bool SPLIT = false>
 __global__ void __launch_bounds__(gemm_threads(TMH), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                   const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
-  constexpr int S = TMH == 2 ? 3 : kStages;
-  constexpr int ABytes = kAStageBytes * TMH;
+                   const __grid_constant__ CUtensorMap tma_c, const __grid_constant__ CUtensorMap tma_a2,
+                   const __grid_constant__ CUtensorMap tma_b2, const GemmParams p) {
+  static_assert(!SPLIT || (TF32 && TMH == 1), "the three-pass split is for tf32 on 128-row tiles");
+  constexpr int S = SPLIT ? 2 : TMH == 2 ? 3 : kStages;
+  constexpr int AHalf = kAStageBytes * TMH;          // one copy of A's slice
+  constexpr int ABytes = AHalf * (SPLIT ? 2 : 1);    // hi then lo
+  constexpr int BBytes = kBStageBytes * (SPLIT ? 2 : 1);
   constexpr int NBUF = TMH == 2 ? 1 : 2;
-  static_assert(S * (ABytes + kBStageBytes) <= kStages * (kAStageBytes + kBStageBytes), "ring exceeds the budget");
+  static_assert(S * (ABytes + BBytes) <= kStages * (kAStageBytes + kBStageBytes), "ring exceeds the budget");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -374,7 +384,7 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
               aborted = true;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], ABytes + kBStageBytes);
+            mbar_arrive_expect_tx(&full[stage], ABytes + BBytes);
             // K-major operand: boxes of 64 K x 128 (A) or 256 (B) rows.
             // MN-major operand: boxes of 64 MN x 64 K, one per 64 rows of the
             // tile, 8 KB apart.
@@ -391,10 +401,15 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
             if (B_MN) {
 #pragma unroll
               for (int j = 0; j < kBN / 64; ++j)
-                tma_load_2d(sB + stage * kBStageBytes + j * 8192, &tma_b, &full[stage], p.b_row0 + nb * kBN + j * 64,
+                tma_load_2d(sB + stage * BBytes + j * 8192, &tma_b, &full[stage], p.b_row0 + nb * kBN + j * 64,
                             k * kSliceK);
             } else {
-              tma_load_2d(sB + stage * kBStageBytes, &tma_b, &full[stage], k * kSliceK, p.b_row0 + nb * kBN);
+              tma_load_2d(sB + stage * BBytes, &tma_b, &full[stage], k * kSliceK, p.b_row0 + nb * kBN);
+            }
+            if (SPLIT) {
+              tma_load_2d(sA + stage * ABytes + AHalf, &tma_a2, &full[stage], k * kSliceK, row0);
+              tma_load_2d(sB + stage * BBytes + kBStageBytes, &tma_b2, &full[stage], k * kSliceK,
+                          p.b_row0 + nb * kBN);
             }
             ++issued;
             if (++stage == S) {
@@ -443,9 +458,21 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
           }
           tc_fence_after_sync();
           const uint32_t a0 = a_base + stage * ABytes;
-          const uint32_t b0 = b_base + stage * kBStageBytes;
+          const uint32_t b0 = b_base + stage * BBytes;
+          if (SPLIT) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ah = sdesc_kmajor_sw128(a0 + kk * 32);
+              const uint64_t al = sdesc_kmajor_sw128(a0 + AHalf + kk * 32);
+              const uint64_t bh = sdesc_kmajor_sw128(b0 + kk * 32);
+              const uint64_t bl = sdesc_kmajor_sw128(b0 + kBStageBytes + kk * 32);
+              tc_mma_tf32(d_tmem, ah, bh, idesc, (k | kk) != 0 ? 1u : 0u);
+              tc_mma_tf32(d_tmem, ah, bl, idesc, 1u);
+              tc_mma_tf32(d_tmem, al, bh, idesc, 1u);
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < (SPLIT ? 0 : 4); ++kk) {
             // One MMA per 32 B of K (16 bf16 or 8 tf32 elements): 32 B along a
             // K-major row, or two 8-row K groups (2048 B) of an MN-major tile.
             // With TMH = 2 the second M half of A starts 16 KB further on (128
@@ -802,9 +829,10 @@ static cudaError_t launch_mode_pair(const CUtensorMap* a, const CUtensorMap* b, 
   return cudaGetLastError();
 }
 
-template <int MODE, bool A_MN, bool B_MN, bool TF32 = false, int TMH = 1>
+template <int MODE, bool A_MN, bool B_MN, bool TF32 = false, int TMH = 1, bool SPLIT = false>
 static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
-                               const GemmParams& p, int grid, cudaStream_t s) {
+                               const GemmParams& p, int grid, cudaStream_t s, const CUtensorMap* a2 = nullptr,
+                               const CUtensorMap* b2 = nullptr) {
   // The shared-memory opt-in is a per-device function attribute: set it on the
   // first launch on each device (outside any stream capture that follows).
   // Two host threads may both set it on a first call; that is harmless, and
@@ -815,7 +843,7 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH>,
+    e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH, SPLIT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev].store(true, std::memory_order_release);
@@ -823,8 +851,8 @@ static cudaError_t launch_mode(const CUtensorMap* a, const CUtensorMap* b, const
   const int units = ((p.m_tiles + TMH - 1) / TMH) * p.n_tiles;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH><<<grid, gemm_threads(TMH), kGemmSmemBytes, s>>>(*a, *b, c ? *c : *a,
-                                                                                           p);
+  gemm_tc_kernel<MODE, A_MN, B_MN, TF32, TMH, SPLIT><<<grid, gemm_threads(TMH), kGemmSmemBytes, s>>>(
+      *a, *b, c ? *c : *a, a2 ? *a2 : *a, b2 ? *b2 : *b, p);
   return cudaGetLastError();
 }
 
@@ -889,9 +917,22 @@ cudaError_t launch_gemm_tc(int mode, bool a_mn, bool b_mn, bool wide, const CUte
 }
 
 cudaError_t launch_gemm_tc_tf32(int mode, bool wide, const CUtensorMap* a, const CUtensorMap* b,
-                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s) {
+                                const CUtensorMap* c, const GemmParams& p, int grid, cudaStream_t s,
+                                const CUtensorMap* a_lo, const CUtensorMap* b_lo) {
   if ((mode == EPI_STATS_STORE || mode == EPI_ACC_F32 || mode == EPI_F32) && c == nullptr)
     return cudaErrorInvalidValue;
+  if (a_lo != nullptr || b_lo != nullptr) {  // three-pass tf32, 128-row tiles
+    if (a_lo == nullptr || b_lo == nullptr) return cudaErrorInvalidValue;
+    switch (mode) {
+      case EPI_STATS: return launch_mode<EPI_STATS, false, false, true, 1, true>(a, b, c, p, grid, s, a_lo, b_lo);
+      case EPI_STATS_STORE:
+        return launch_mode<EPI_STATS_STORE, false, false, true, 1, true>(a, b, c, p, grid, s, a_lo, b_lo);
+      case EPI_F32: return launch_mode<EPI_F32, false, false, true, 1, true>(a, b, c, p, grid, s, a_lo, b_lo);
+      case EPI_ACC_F32:
+        return launch_mode<EPI_ACC_F32, false, false, true, 1, true>(a, b, c, p, grid, s, a_lo, b_lo);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (wide) {
     switch (mode) {
       case EPI_STATS: return launch_mode<EPI_STATS, false, false, true, 2>(a, b, c, p, grid, s);

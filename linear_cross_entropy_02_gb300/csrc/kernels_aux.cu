@@ -28,6 +28,16 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return *reinterpret_cast<const uint16_t*>(&v);
 }
 
+// x = hi + lo with hi = x rounded to tf32 (10 mantissa bits, nearest, ties
+// away from zero: cvt.rna.tf32.f32) and lo = x - hi, exact in fp32: the two
+// operands of the three-pass tf32 products.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  uint32_t h;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+  hi = __uint_as_float(h);
+  lo = x - hi;
+}
+
 // ------------------------------------------------------------------ prologue
 // One block: counts rows whose label is not ignore_index, flags labels outside
 // [0, V), and resets the batch sums. Deterministic (no atomics).
@@ -490,7 +500,16 @@ __global__ void __launch_bounds__(256) dlogits_f32_kernel(const DlogitParams p) 
           const float u = sv * p.inv_softcap;
           q *= (1.f - u * u);
         }
-        if (p.dz32) p.dz32[static_cast<int64_t>(r) * p.ldd + c] = q;
+        if (p.dz32) {
+          if (p.dz32_lo) {
+            float hi, lo;
+            split_tf32(q, hi, lo);
+            p.dz32[static_cast<int64_t>(r) * p.ldd + c] = hi;
+            p.dz32_lo[static_cast<int64_t>(r) * p.ldd + c] = lo;
+          } else {
+            p.dz32[static_cast<int64_t>(r) * p.ldd + c] = q;
+          }
+        }
       }
       tile[lr][tx * 4 + j] = q;
     }
@@ -505,7 +524,16 @@ __global__ void __launch_bounds__(256) dlogits_f32_kernel(const DlogitParams p) 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = r0 + tx * 4 + j;
-      if (r < p.rows) p.dzt32[static_cast<int64_t>(c) * p.ldt + r] = tile[tx * 4 + j][lc];
+      if (r >= p.rows) continue;
+      const float q = tile[tx * 4 + j][lc];
+      if (p.dzt32_lo) {
+        float hi, lo;
+        split_tf32(q, hi, lo);
+        p.dzt32[static_cast<int64_t>(c) * p.ldt + r] = hi;
+        p.dzt32_lo[static_cast<int64_t>(c) * p.ldt + r] = lo;
+      } else {
+        p.dzt32[static_cast<int64_t>(c) * p.ldt + r] = q;
+      }
     }
   }
 }
@@ -570,7 +598,8 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t ldi, int rows, int
 }
 
 __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ in, int64_t ldi, int rows,
-                                                            int cols, float* __restrict__ out, int64_t ldo) {
+                                                            int cols, float* __restrict__ out, int64_t ldo,
+                                                            float* __restrict__ out_lo) {
   __shared__ float tile[64][65];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
@@ -593,17 +622,53 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restr
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = r0 + tx * 4 + j;
-      if (r < rows) out[static_cast<int64_t>(c) * ldo + r] = tile[tx * 4 + j][lc];
+      if (r >= rows) continue;
+      const float v = tile[tx * 4 + j][lc];
+      if (out_lo) {
+        float hi, lo;
+        split_tf32(v, hi, lo);
+        out[static_cast<int64_t>(c) * ldo + r] = hi;
+        out_lo[static_cast<int64_t>(c) * ldo + r] = lo;
+      } else {
+        out[static_cast<int64_t>(c) * ldo + r] = v;
+      }
     }
   }
 }
 
 cudaError_t launch_transpose_f32(const float* in, int64_t ldi, int rows, int cols, float* out, int64_t ldo,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, float* out_lo) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   dim3 grid((cols + 63) / 64, (rows + 63) / 64);
-  transpose_f32_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo);
+  transpose_f32_kernel<<<grid, 256, 0, s>>>(in, ldi, rows, cols, out, ldo, out_lo);
   return cudaGetLastError();
+}
+
+// hi [rows][ldo], lo [rows][ldo] = the tf32 split of in [rows][ldi] (cols columns).
+__global__ void __launch_bounds__(256) split_f32_kernel(const float* __restrict__ in, int64_t ldi, int rows, int cols,
+                                                        float* __restrict__ hi, float* __restrict__ lo, int64_t ldo) {
+  const int r = blockIdx.y;
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+    float h, l;
+    split_tf32(in[static_cast<int64_t>(r) * ldi + c], h, l);
+    hi[static_cast<int64_t>(r) * ldo + c] = h;
+    lo[static_cast<int64_t>(r) * ldo + c] = l;
+  }
+}
+
+cudaError_t launch_split_f32(const float* in, int64_t ldi, int rows, int cols, float* hi, float* lo, int64_t ldo,
+                             cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  for (int r0 = 0; r0 < rows; r0 += 65535) {  // grid.y per launch stays within its limit
+    const int nr = rows - r0 < 65535 ? rows - r0 : 65535;
+    dim3 grid((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8, nr);
+    split_f32_kernel<<<grid, 256, 0, s>>>(in + static_cast<int64_t>(r0) * ldi, ldi, nr, cols,
+                                           hi + static_cast<int64_t>(r0) * ldo, lo + static_cast<int64_t>(r0) * ldo,
+                                           ldo);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ convert

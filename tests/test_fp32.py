@@ -111,3 +111,67 @@ def test_fp32_fuzzed_shapes(flce, case):
     assert flce.flce_get_status() == 0
     ref = flce_oracle(h, W, y, softcap=c["softcap"], out_mult=c["out_mult"])
     check_against_oracle(out, ref, y, what=f"fp32 fuzz {case}")
+
+
+def _rel_errs(out, ref, G0=None):
+    loss = abs(float(out["loss"]) - ref["loss"]) / abs(ref["loss"])
+    gh = out["grad_h"].double().cpu().numpy()
+    e_h = np.abs(gh - ref["grad_h"]).max() / np.abs(ref["grad_h"]).max()
+    e_w = None
+    if out.get("grad_W") is not None:
+        d = ref["grad_W"] - (0.0 if G0 is None else G0)
+        e_w = np.abs(out["grad_W"].double().cpu().numpy() - ref["grad_W"]).max() / np.abs(d).max()
+    return loss, e_h, e_w
+
+
+@pytest.mark.parametrize("case", [
+    dict(N=256, H=512, V=4096),
+    dict(N=513, H=136, V=777, chunk_rows=256, softcap=30.0, out_mult=0.5),
+    dict(N=700, H=1024, V=5000, softcap=2.0, out_mult=-1.5, reduction="sum", grad_scale=0.75),
+])
+def test_fp32_three_pass_reaches_fp32_accuracy(flce, case):
+    """FLCE_FLAG_F32_3PASS: each product as hi*hi + hi*lo + lo*hi in tf32. The
+    loss and both gradients come within fp32 rounding of the fp64 oracle on the
+    exact fp32 inputs (errors of about 1e-6), two orders of magnitude closer
+    than the single-pass tf32 products, whose 10-bit mantissas limit them to
+    about 1e-3."""
+    c = dict(case)
+    N, H, V = c.pop("N"), c.pop("H"), c.pop("V")
+    h, W, y = _inputs_f32(N, H, V, seed=N + H + V + 1)
+    G0 = (np.random.default_rng(3).standard_normal((V, H)) * 1e-3).astype(np.float32).astype(np.float64)
+    ref = flce_oracle(h, W, y, grad_W0=G0, softcap=c.get("softcap", 0.0), out_mult=c.get("out_mult", 1.0),
+                      reduction=c.get("reduction", "mean"), grad_scale=c.get("grad_scale", 1.0))
+    errs = {}
+    for flags in (0, flce.FLCE_FLAG_F32_3PASS):
+        gW = torch.from_numpy(G0).float().to(DEV)
+        out = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, return_predicted=True,
+                                         flags=flags, **c)
+        torch.cuda.synchronize()
+        assert flce.flce_get_status() == 0
+        check_against_oracle(out, ref, y, grad_W0=G0, what=f"fp32 {case} flags={flags}")
+        errs[flags] = _rel_errs(out, ref, G0)
+    l3, h3, w3 = errs[flce.FLCE_FLAG_F32_3PASS]
+    l1, h1, w1 = errs[0]
+    print(case, "tf32", errs[0], "3-pass", errs[flce.FLCE_FLAG_F32_3PASS])
+    assert l3 <= 1e-5 and h3 <= 1e-4 and w3 <= 1e-4, errs
+    assert h3 * 20 <= h1 and w3 * 20 <= w1, errs
+
+
+def test_fp32_three_pass_forward_llama_width_and_host_inputs(flce):
+    """The three-pass forward at H = 4096 (the lse of every row), and the same
+    call with host inputs, which splits each staged chunk."""
+    N, H, V = 600, 4096, 20000
+    h, W, y = _inputs_f32(N, H, V, seed=11, w_std=0.02)
+    f = flce.flce_forward(h.to(DEV), W.to(DEV), y.to(DEV), return_lse=True, flags=flce.FLCE_FLAG_F32_3PASS)
+    torch.cuda.synchronize()
+    ref = flce_oracle(h, W, y, need_grad_h=False, need_grad_W=False)
+    assert np.abs(f["lse"].cpu().double().numpy() - ref["lse"]).max() <= 1e-5 * np.abs(ref["lse"]).max()
+    gW = torch.zeros(W.shape, dtype=torch.float32, device=DEV)
+    a = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW, chunk_rows=256,
+                                   flags=flce.FLCE_FLAG_F32_3PASS)
+    gW2 = torch.zeros(W.shape, dtype=torch.float32, device=DEV)
+    b = flce.flce_forward_backward_from_host(h.pin_memory(), W.to(DEV), y.pin_memory(), grad_W=gW2, chunk_rows=256,
+                                             flags=flce.FLCE_FLAG_F32_3PASS)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    assert float(a["loss"]) == float(b["loss"]) and torch.equal(a["grad_h"], b["grad_h"]) and torch.equal(gW, gW2)
