@@ -351,13 +351,15 @@ GOLDEN_FOR = {"llama": "llama", "muse": "muse", "dsv3": "dsv3", "frozen_ce": "fr
 NEAR_TIE = 1e-3
 
 
-def parity_against_goldens(flce, w, h, W, lab, inputs_cpu, kw):
+def parity_against_goldens(flce, w, h, W, lab, inputs_cpu, kw, forward=None):
     """One flce_forward of the timed workload (outside the timed region)
     compared row by row with the stored full-size oracle forward of the same
     inputs (tests/golden/configs, written by the oracle alone): the loss, every
     row's lse, every predicted token, and the correct count. Rows whose oracle
     top-2 gap is below 1e-3 relative may predict the other token; they are
-    counted here. None when the workload has no stored oracle forward."""
+    counted here. `forward` (optional) runs the line's own path and returns
+    loss, lse and predicted; by default flce_forward with the line's flags.
+    None when the workload has no stored oracle forward."""
     g = GOLDEN_FOR.get(w.name)
     if g is None or not os.path.exists(os.path.join(GOLDEN_DIR, g + ".json")):
         return None
@@ -367,7 +369,7 @@ def parity_against_goldens(flce, w, h, W, lab, inputs_cpu, kw):
     hashes = {k: workloads.tensor_sha256(t) for k, t in zip(("h", "W", "labels"), inputs_cpu)}
     if hashes != meta["sha256"]:
         return {"oracle": f"tests/golden/configs/{g}", "skipped": "inputs differ from the stored oracle's"}
-    f = flce.flce_forward(h, W, lab, return_lse=True, **kw)
+    f = forward() if forward is not None else flce.flce_forward(h, W, lab, return_lse=True, **kw)
     torch.cuda.synchronize()
     pred = f["predicted"].reshape(-1).cpu().numpy()
     lse = f["lse"].reshape(-1).cpu().double().numpy()
@@ -414,6 +416,7 @@ def run_ours(args, w):
         return flce.flce_forward_backward(h, W, lab, grad_W=gW, need_grad_h=True,
                                           return_predicted=w.return_predicted, **kw, **bkw)
 
+    vp_forward = None
     if args.vocab_shards:
         # The vocabulary-parallel form, its S shards run one after another on
         # this GPU: every shard's forward, the gather (a stack in shard order),
@@ -439,6 +442,11 @@ def run_ours(args, w):
             if w.mode != "ce_only":
                 flce.flce_scale_gradient(gh32, None, out_dtype=h.dtype)
             return out
+
+        def vp_forward():
+            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, **vkw) for k in range(S)]
+            return flce.flce_vp_backward(h, shards[0], lab, torch.stack(parts), offsets, 0, w.vocab,
+                                         return_predicted=True, return_lse=True, **vkw)
 
     for _ in range(args.warmup):
         step()
@@ -491,7 +499,8 @@ def run_ours(args, w):
     if rank == 0 and not (args.rows or args.vocab):
         parity = parity_against_goldens(flce, w, h, W, lab, inputs_bf16,
                                         dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows,
-                                             flags=kw["flags"]))
+                                             flags=kw["flags"]),
+                                        forward=vp_forward if args.vocab_shards else None)
     if rank == 0:
         chunk_used = flce.flce_chunk_rows(
             w.n_rows, w.hidden, w.vocab,
