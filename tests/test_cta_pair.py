@@ -104,3 +104,21 @@ def test_pair_ce_only_and_vocab_shards(flce):
     assert abs(float(o["loss"]) - ref["loss"]) <= 2e-3 * abs(ref["loss"])
     g = gh.double().cpu().numpy()
     assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * np.abs(ref["grad_h"]).max()
+
+
+def test_pair_bounded_waits_time_out_and_context_survives(flce):
+    """The test hook makes both CTAs' loaders issue nothing: the leader's MMA
+    waits and both CTAs' epilogue waits give up after the limit, each CTA on
+    its own clock, and both reach the closing cluster barrier, free TMEM and
+    return with FLCE_ERR_TIMEOUT; the next call on the context is correct."""
+    N, H, V = 256, 128, 1024
+    h, W, y = _inputs(N, H, V, 73)
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    flce.flce_ce_only(hd, Wd, yd, flags=flce.FLCE_FLAG_TEST_STALL | TILE256 | PAIR, timeout_ns=50_000_000)
+    st = flce.flce_get_status()
+    assert st & 32, st
+    loss, acc = flce.flce_ce_only(hd, Wd, yd, flags=TILE256 | PAIR)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = flce_oracle(h, W, y, need_grad_h=False, need_grad_W=False)
+    assert abs(float(loss) - ref["loss"]) <= 2e-3 * ref["loss"]

@@ -37,7 +37,7 @@ def _run_shards(flce, h, W, y, offsets, grad_h=True, grad_W=True, **kw):
     summed grad_h (bf16, rounded by the library) and the full grad_W."""
     V = offsets[-1]
     hd, yd = h.to(DEV), y.to(DEV)
-    fwd_kw = {k: v for k, v in kw.items() if k in ("softcap", "out_mult", "chunk_rows")}
+    fwd_kw = {k: v for k, v in kw.items() if k in ("softcap", "out_mult", "chunk_rows", "flags")}
     shards = [W[offsets[k]:offsets[k + 1]].to(DEV) for k in range(len(offsets) - 1)]
     parts = [flce.flce_vp_forward(hd, Wk, yd, offsets[k], V, **fwd_kw) for k, Wk in enumerate(shards)]
     allp = torch.stack(parts)
@@ -170,3 +170,38 @@ def test_bad_labels_and_shard_tables(flce):
                                   allp[:1].expand(len(bad) - 1, 4, N).contiguous(), bad, 0, V)
         assert e.value.code == _lib.FLCE_ERR_ARG
     flce.flce_release_workspaces()
+
+
+def _fuzz(n=10, seed=90):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        V = int(rng.integers(300, 6000))
+        S = int(rng.integers(1, 5))
+        cuts = sorted(set(int(x) for x in rng.integers(1, V, S - 1))) if S > 1 else []
+        out.append(dict(N=int(rng.integers(1, 900)), H=int(8 * rng.integers(1, 40)), V=V, offsets=[0] + cuts + [V],
+                        softcap=float(rng.choice([0.0, 2.0, 30.0])), out_mult=float(rng.choice([1.0, 0.5, -1.5])),
+                        chunk_rows=int(rng.choice([0, 128, 384])), vocab_slab=int(rng.choice([0, 256, 1024])),
+                        seed=100 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", _fuzz(), ids=lambda c: f"N{c['N']}-H{c['H']}-V{c['V']}-S{len(c['offsets']) - 1}")
+def test_fuzzed_shard_tables(flce, case):
+    """Seeded random shapes, options and shard boundaries (none aligned to the
+    256-column tiles), against the fp64 oracle and the unsharded call."""
+    kw = {k: case[k] for k in ("softcap", "out_mult", "chunk_rows")}
+    okw = {k: case[k] for k in ("softcap", "out_mult")}
+    h, W, y = _inputs(case["N"], case["H"], case["V"], case["seed"])
+    _, outs, gh, gW = _run_shards(flce, h, W, y, case["offsets"], vocab_slab=case["vocab_slab"], **kw)
+    f = flce.flce_forward(h.to(DEV), W.to(DEV), y.to(DEV), **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0]["predicted"], f["predicted"])
+    assert float(outs[0]["token_accuracy"]) == float(f["token_accuracy"])
+    ref = flce_oracle(h, W, y, **okw)
+    if ref["n_valid"]:
+        assert abs(float(outs[0]["loss"]) - ref["loss"]) <= 2e-3 * abs(ref["loss"])
+    g = gh.float().cpu().numpy()
+    assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * max(np.abs(ref["grad_h"]).max(), 1e-30)
+    gw = gW.double().cpu().numpy()
+    assert np.abs(gw - ref["grad_W"]).max() <= 1e-2 * max(np.abs(ref["grad_W"]).max(), 1e-30)
