@@ -418,6 +418,7 @@ struct Call {
   int64_t vocab_offset = 0;
   int64_t vocab_total = 0;
   float* shard_partials = nullptr;
+  bool shard_call = false;
 };
 
 int run_f32(const Norm& n, const Call& c);
@@ -618,7 +619,7 @@ int run(const flce_params* params, const Call& c) {
   const flce_params& p = n.p;
   const bool gh = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_h != nullptr;
   const bool gw = c.mode == FLCE_MODE_FORWARD_BACKWARD && c.grad_W != nullptr;
-  const bool shard = c.shard_partials != nullptr;
+  const bool shard = c.shard_call;
   if ((!c.loss && !shard) || !c.ws || !c.W) return FLCE_ERR_ARG;
   if (p.n_rows > 0 && (!c.h || !c.labels)) return FLCE_ERR_ARG;
   if (!aligned16(c.ws) || (!c.host_in && c.h && !aligned16(c.h)) || !aligned16(c.W)) return FLCE_ERR_ALIGN;
@@ -1502,7 +1503,7 @@ size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_
 int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, const void* h,
                     const void* W_shard, const int64_t* labels, float* partials, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  if (!p || !partials) return FLCE_ERR_ARG;
+  if (!p || (!partials && p->n_rows > 0)) return FLCE_ERR_ARG;
   const int rc = check_shards(vocab_offset, p->vocab, vocab_total, 0, nullptr);
   if (rc != FLCE_OK) return rc;
   if (p->dtype != FLCE_DTYPE_BF16 || (p->flags & FLCE_FLAG_SIMT_GEMM)) return FLCE_ERR_UNSUPPORTED;
@@ -1510,7 +1511,8 @@ int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_to
          workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.vocab_offset = vocab_offset;
   c.vocab_total = vocab_total;
-  c.shard_partials = partials;
+  c.shard_partials = partials;  // NULL only with no rows, which write none
+  c.shard_call = true;
   return run(p, c);
 }
 

@@ -61,6 +61,24 @@ struct EpiStage {
   bool hint;
 };
 
+// Walks the 256 accumulator columns of this thread's row in chunks of 32,
+// calling f(r, c) for chunk c, with the TMEM load of chunk c + 1 in flight
+// while chunk c is processed (two register buffers).
+template <typename F>
+__device__ __forceinline__ void tmem_row_chunks(uint32_t tcol, F&& f) {
+  uint32_t ra[32], rb[32];
+  tmem_load_32cols(tcol, ra);
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; c += 2) {
+    tmem_load_wait_regs(ra);
+    tmem_load_32cols(tcol + (c + 1) * 32, rb);
+    f(ra, c);
+    tmem_load_wait_regs(rb);
+    if (c + 2 < kBN / 32) tmem_load_32cols(tcol + (c + 2) * 32, ra);
+    f(rb, c + 1);
+  }
+}
+
 template <bool REDUCE>
 __device__ __forceinline__ void stage_and_send(EpiStage& es, const CUtensorMap* map, int lane, const float (&v)[32],
                                                int32_t x, int32_t y) {
@@ -148,11 +166,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
   RowStats st;
   row_stats_init(st, n0);
   uint32_t held[16];  // STORE == 2: the even group's fp16 values, sent with the odd one
-#pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_load_32cols(tcol + c * 32, r);
-    tmem_load_wait();
+  tmem_row_chunks(tcol, [&](const uint32_t(&r)[32], int c) {
     float s[32];
     const int col0 = n0 + c * 32;
     if (p.softcap > 0.f) {
@@ -183,7 +197,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
         stage_and_send16(es, zmap, lane, held, hv, col0 - 32, mb * kBM + quarter * 32);
       }
     }
-  }
+  });
   if (row_ok) {
     const int64_t o = static_cast<int64_t>(nb) * p.ldp + grow;
     p.part_max[o] = st.mx;
@@ -203,11 +217,7 @@ __device__ __forceinline__ void epilogue_bf16(const GemmParams& p, uint32_t tcol
   const bool row_ok = grow < p.M_valid;
   const int n0 = nb * kBN;
   uint16_t* orow = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(grow) * p.ldo + n0;
-#pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_load_32cols(tcol + c * 32, r);
-    tmem_load_wait();
+  tmem_row_chunks(tcol, [&](const uint32_t(&r)[32], int c) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int col = n0 + c * 32 + g * 8;
@@ -220,7 +230,7 @@ __device__ __forceinline__ void epilogue_bf16(const GemmParams& p, uint32_t tcol
         *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = v;
       }
     }
-  }
+  });
 }
 
 // grad_W (or the recompute path's fp32 grad_h) += alpha * acc: the sub-tile is
@@ -230,16 +240,12 @@ template <bool REDUCE>
 __device__ __forceinline__ void epilogue_out_f32(const GemmParams& p, const CUtensorMap* omap, EpiStage& es,
                                                  uint32_t tcol, int mb, int nb, int quarter, int lane) {
   const int n0 = nb * kBN;
-#pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_load_32cols(tcol + c * 32, r);
-    tmem_load_wait();
+  tmem_row_chunks(tcol, [&](const uint32_t(&r)[32], int c) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.alpha;
     if (n0 + c * 32 < p.N_valid) stage_and_send<REDUCE>(es, omap, lane, v, n0 + c * 32, mb * kBM + quarter * 32);
-  }
+  });
 }
 
 // Recompute pass of the low-memory backward: z = alpha * acc is capped, turned

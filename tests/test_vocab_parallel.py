@@ -205,3 +205,17 @@ def test_fuzzed_shard_tables(flce, case):
     assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * max(np.abs(ref["grad_h"]).max(), 1e-30)
     gw = gW.double().cpu().numpy()
     assert np.abs(gw - ref["grad_W"]).max() <= 1e-2 * max(np.abs(ref["grad_W"]).max(), 1e-30)
+
+
+def test_empty_and_all_ignored_batches(flce):
+    """No rows, and rows that are all ignored: the loss and accuracy are 0, the
+    gradients stay 0 and nothing reads outside the (empty) inputs."""
+    H, V = 64, 1000
+    offsets = [0, 400, V]
+    W = workloads.make_weight(V, H, 57)
+    for N, ign in ((0, 0.0), (70, 1.0)):
+        h = workloads.make_hidden(max(N, 1), H, 57)[:N]
+        y = workloads.make_labels(max(N, 1), V, 57, ign)[:N]
+        _, outs, gh, gW = _run_shards(flce, h, W, y, offsets)
+        assert float(outs[0]["loss"]) == 0.0 and float(outs[0]["token_accuracy"]) == 0.0
+        assert torch.count_nonzero(gh).item() == 0 and torch.count_nonzero(gW).item() == 0
