@@ -372,6 +372,8 @@ def vp_shard_table(vocab_offset: int, vocab_shard: int, group=None):
     if _world(group) == 1:
         table = [mine]
     else:
+        if dist.get_backend(group) == "nccl":  # NCCL exchanges device tensors only
+            mine = mine.to(torch.device("cuda", torch.cuda.current_device()))
         table = [torch.empty_like(mine) for _ in range(_world(group))]
         dist.all_gather(table, mine, group=group)
     rows = sorted((int(t[0]), int(t[1]), r) for r, t in enumerate(table))
