@@ -7,15 +7,17 @@
 //   prologue                               labels -> n_valid, status, sums = 0
 //   [W^T transpose]                        when grad_h is wanted
 //   for each chunk of C rows:
-//     forward GEMM + statistics epilogue   z = m h_c W^T, s = cap(z) stored
+//     forward GEMM + statistics epilogue   z = m h_c W^T, s = cap(z) stored (fp16
+//                                          s - gmax per 32 columns on the bf16 path)
 //     merge                                lse, argmax, row loss, chunk sums
-//     dlogits                              dz (bf16), and dz^T when grad_W
+//     dlogits                              dz (bf16); dz^T on the K-major paths
 //     grad_h GEMM                          grad_h_c = m dz W
 //     [h_c^T transpose] + grad_W GEMM      grad_W += m dz^T h_c
 //   finish                                 loss, token accuracy
 // The logits of a chunk are the only O(C * V) transient (the Liger-Kernel
 // DeepSeek-V3 page, section Memory: chunked transients instead of the full
-// logits).
+// logits). FLCE_FLAG_RECOMPUTE and the vocabulary-parallel backward keep none:
+// they rebuild the logits per vocab slab (recompute_slabs).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

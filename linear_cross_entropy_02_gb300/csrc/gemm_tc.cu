@@ -17,8 +17,12 @@
 //   accumulator is drained by eight epilogue warps.
 // Epilogue modes: forward statistics of the linear cross-entropy (softcap,
 // running max / sum of exponentials, argmax, label logit) with or without
-// storing the capped logits; bf16 store of alpha*acc (grad_h); fp32
-// accumulate-in-place of alpha*acc (grad_W += ...).
+// storing the capped logits (fp32, or fp16 relative to each 32-column group's
+// maximum); bf16 store of alpha*acc (grad_h); fp32 accumulate-in-place of
+// alpha*acc (grad_W += ...); bf16 dlogits from recomputed logits (EPI_DZ).
+// A CTA-pair variant (gemm_tc_pair_kernel, below) computes 256 x 256 tiles on
+// two SMs with cta_group::2, and a three-pass split (SPLIT) gives fp32
+// operands fp32 accuracy on the tf32 tensor cores.
 // Every wait is bounded (FLCE_ERR_TIMEOUT); on the way out the CTA drains the
 // copies and MMAs it issued and frees TMEM.
 #include <cuda_bf16.h>

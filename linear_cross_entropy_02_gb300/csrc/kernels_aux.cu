@@ -2,12 +2,18 @@
 // path, plus the debug fp32-FMA GEMM:
 //   prologue      label check, n_valid, reset of the device scalars
 //   merge         per-row merge of the vocab-tile statistics: lse, argmax,
-//                 row loss; fixed-order reduction into the batch sums
-//   dlogits       dz = c (softmax - onehot) (1 - (s/T)^2) in bf16, written
-//                 row-major (A operand of grad_h) and transposed (A operand of
-//                 grad_W)
-//   transpose     bf16 transposes that give the backward GEMMs K-major operands
+//                 row loss; fixed-order reduction into the batch sums; or one
+//                 vocab shard's per-row partials
+//   vp merge      the merge of every vocab shard's partials, in shard order
+//   dlogits       dz = c (softmax - onehot) (1 - (s/T)^2) in bf16 from the
+//                 stored logits (fp16 s - gmax, or fp32), row-major (A operand
+//                 of grad_h, and MN-major A of grad_W), and on the K-major
+//                 paths also transposed; fp32 (and its tf32 split) on the
+//                 fp32-operand path
+//   transpose     bf16 / fp32 transposes that give the backward GEMMs K-major
+//                 operands; split: the hi / lo halves of the three-pass tf32
 //   finish        loss and token accuracy scalars
+//   scale         y = scale * x with a dtype conversion (autograd's backward)
 //   simt gemm     fp32 FMA GEMM + statistics from stored logits (debug path)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
