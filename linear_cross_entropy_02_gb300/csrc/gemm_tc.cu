@@ -640,7 +640,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * 128);  // every epilogue thread of both CTAs arrives (on the leader's)
+      mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of both CTAs (on the leader's)
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -795,11 +795,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           epilogue_dz(p, tcol, mb, nb, row, coef);
         }
       }
+      // The warp's TMEM reads are complete (each thread waited for its loads);
+      // one lane then arrives for the warp, which keeps the cross-SM arrivals
+      // on the leader's barrier to four per CTA and tile.
       tc_fence_before_sync();
-      if (rank == 0)
-        mbar_arrive(&tempty[acc]);
-      else
-        mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
