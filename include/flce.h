@@ -46,8 +46,9 @@
  *    cudaStream_t; NULL = legacy default stream).
  *  - The return value is FLCE_OK or a host-detected error, returned before
  *    any launch. Errors found on the device (bad labels, a bounded wait that
- *    gave up) are OR-ed into a status word in the workspace; read it with
- *    flce_get_status. On any error the outputs are unspecified.
+ *    gave up, a non-finite row) are OR-ed into a status word in the
+ *    workspace; read it with flce_get_status. On a bad label or a timeout the
+ *    outputs are unspecified.
  *  - Nothing traps, prints or throws across this boundary.
  *  - The current CUDA device (cudaSetDevice) must be the device that owns
  *    `stream` and every device pointer of the call: the library takes the SM
@@ -79,6 +80,10 @@ extern "C" {
 /* Device-detected bits of the status word (flce_get_status). */
 #define FLCE_ERR_LABEL 16       /* a label is neither ignore_index nor in [0, V) */
 #define FLCE_ERR_TIMEOUT 32     /* a bounded pipeline wait gave up; the kernel returned early */
+#define FLCE_ERR_NONFINITE 64   /* a row's log-sum-exp is not finite (inf or NaN in h or W, or
+                                   logits beyond fp32 range); that row's predicted token is -1
+                                   and its loss and gradients are not meaningful; the other rows
+                                   are unaffected */
 
 /* Modes for flce_workspace_size. */
 #define FLCE_MODE_CE_ONLY 0
@@ -318,7 +323,8 @@ int flce_vp_backward(const flce_params* p, int64_t vocab_offset, int64_t vocab_t
                      size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream` and returns (in *status) the device status word of the
- * last call that used this workspace: 0 or FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT.
+ * last call that used this workspace: 0, or an OR of FLCE_ERR_LABEL,
+ * FLCE_ERR_TIMEOUT and FLCE_ERR_NONFINITE.
  * Return value: FLCE_OK or FLCE_ERR_ARG / FLCE_ERR_CUDA. */
 int flce_get_status(const void* workspace, void* stream, int32_t* status);
 

@@ -16,6 +16,7 @@ FLCE_ERR_UNSUPPORTED = 4
 FLCE_ERR_CUDA = 5
 FLCE_ERR_LABEL = 16
 FLCE_ERR_TIMEOUT = 32
+FLCE_ERR_NONFINITE = 64
 
 FLCE_MODE_CE_ONLY = 0
 FLCE_MODE_FORWARD = 1

@@ -1579,6 +1579,7 @@ const char* flce_status_string(int code) {
     case FLCE_ERR_LABEL: return "label outside [0, V) that is not ignore_index";
     case FLCE_ERR_TIMEOUT: return "bounded device wait timed out";
     case FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT: return "bad label and device wait timed out";
+    case FLCE_ERR_NONFINITE: return "non-finite log-sum-exp in some row (inf or NaN inputs)";
     default: return "unknown status";
   }
 }

@@ -38,7 +38,7 @@ constexpr int kMergeRows = 32;
 
 // Workspace header (offset 0 of every workspace).
 struct Header {
-  int32_t status;    // FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT bits
+  int32_t status;    // FLCE_ERR_LABEL | FLCE_ERR_TIMEOUT | FLCE_ERR_NONFINITE bits
   uint32_t ticket;   // last-block election in the merge kernel
   int64_t n_valid;   // rows whose label is not ignore_index
   double loss_sum;   // sum of row losses over finished chunks (fixed order)

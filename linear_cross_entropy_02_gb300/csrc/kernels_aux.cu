@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kMergeRows * kMergeWarps) merge_kernel(const M
           if (m2 == M && a2 < A) A = a2;
         }
       }
+      if (!isfinite(M) || !isfinite(S)) atomicOr(&p.hdr->status, FLCE_ERR_NONFINITE);
       const int64_t y = p.labels[row];
       const int64_t yl = y - p.vocab_offset;
       const bool here = y != p.ignore_index && yl >= 0 && yl < p.vocab_shard;
@@ -176,6 +177,10 @@ __global__ void __launch_bounds__(kMergeRows * kMergeWarps) merge_kernel(const M
       }
       const float lse = M + logf(S);
       p.lse[row] = lse;
+      if (!isfinite(lse)) {  // inf / NaN inputs: no meaningful argmax
+        atomicOr(&p.hdr->status, FLCE_ERR_NONFINITE);
+        A = -1;
+      }
       const int64_t y = p.labels[row];
       if (y != p.ignore_index) {
         loss_i = static_cast<double>(lse) - static_cast<double>(p.tgt[row]);
@@ -250,6 +255,10 @@ __global__ void __launch_bounds__(32) vp_merge_kernel(const VpMergeParams p) {
     }
     const float lse = M + logf(S);
     p.lse[row] = lse;
+    if (!isfinite(lse)) {
+      atomicOr(&p.hdr->status, FLCE_ERR_NONFINITE);
+      A = -1;
+    }
     const int64_t y = p.labels[row];
     if (y != p.ignore_index) {
       int k = 0;

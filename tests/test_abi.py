@@ -146,10 +146,11 @@ def test_host_errors_before_any_device_work(L):
 
 
 def test_status_strings(L):
-    for code in (0, 1, 2, 3, 4, 5, 16, 32, 48, 999):
+    for code in (0, 1, 2, 3, 4, 5, 16, 32, 48, 64, 999):
         s = L.flce_status_string(code)
         assert isinstance(s, bytes) and len(s) > 0
     assert L.flce_status_string(32) == b"bounded device wait timed out"
+    assert b"non-finite" in L.flce_status_string(64)
 
 
 def test_kernel_names(L):

@@ -501,3 +501,37 @@ def test_fuzzed_shapes_and_options(flce, case):
     out = run_fwd_bwd(flce, h, W, y, grad_W0=G0, flags=flags, **c)
     ref = flce_oracle(h, W, y, grad_W0=G0, softcap=c["softcap"], out_mult=c["out_mult"], reduction=c["reduction"])
     check_against_oracle(out, ref, y, grad_W0=G0, what=f"fuzz {case}")
+
+
+def test_non_finite_rows_are_flagged_without_fault(flce):
+    """A NaN in one row of h and an inf in another: those rows' log-sum-exp is
+    not finite and the status word gets FLCE_ERR_NONFINITE; with both rows
+    ignored the loss over the other rows is still the oracle's. A NaN in one
+    vocabulary row of W reaches every row's sum of exponentials, in a vocab
+    shard too. The next clean call reports 0."""
+    N, H, V = 300, 64, 2000
+    h, W, y = _inputs(N, H, V, seed=77)
+    h[7, 3] = float("nan")
+    h[200, 5] = float("inf")
+    y[7] = -100
+    y[200] = -100
+    f = flce.flce_forward(h.to(DEV), W.to(DEV), y.to(DEV), return_lse=True)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() & flce._lib.FLCE_ERR_NONFINITE
+    lse = f["lse"].cpu()
+    assert not torch.isfinite(lse[7]) and torch.isfinite(lse[[0, 8, 199, 201]]).all()
+    pred = f["predicted"].cpu()
+    assert pred[7] == -1 and pred[200] == -1 and (pred[[0, 8, 199, 201]] >= 0).all()
+    keep = torch.ones(N, dtype=torch.bool)
+    keep[[7, 200]] = False
+    ref = flce_oracle(h[keep], W, y[keep], need_grad_h=False, need_grad_W=False)
+    assert abs(float(f["loss"]) - ref["loss"]) <= LOSS_RTOL * ref["loss"]
+    W2 = W.clone()
+    W2[1500, 0] = float("nan")
+    part = flce.flce_vp_forward(h.to(DEV), W2[1024:].to(DEV), y.to(DEV), 1024, V)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() & flce._lib.FLCE_ERR_NONFINITE
+    h2, _, _ = _inputs(N, H, V, seed=78)
+    flce.flce_forward(h2.to(DEV), W.to(DEV), y.to(DEV))
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
