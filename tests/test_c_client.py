@@ -106,3 +106,46 @@ def test_forward_backward_from_c(client, tmp_path):
     assert abs(float(sc[0]) - orc["loss"]) <= 2e-3 * abs(orc["loss"])
     gwd = gw.reshape(V, H).astype(np.float64)
     assert np.abs(gwd - orc["grad_W"]).max() <= 1e-2 * np.abs(orc["grad_W"] - G0).max()
+
+
+@pytest.mark.gpu
+def test_vocab_parallel_from_c(client, tmp_path):
+    """The vocabulary-parallel entry points driven from C alone: three shards
+    run in turn on buffers the C program allocates. Predictions and accuracy
+    equal the unsharded call's, the loss agrees to the fp32 merge order, and
+    grad_h (summed in fp32 over the shards) and grad_W match the oracle."""
+    import linear_cross_entropy_02_gb300 as flce
+    N, H, V, C, T, m, S = 300, 136, 777, 128, 30.0, 0.5, 3
+    h = workloads.make_hidden(N, H, 82)
+    W = workloads.make_weight(V, H, 82, std=0.05)
+    y = workloads.make_labels(N, V, 82, 0.1)
+    G0 = (np.random.default_rng(82).standard_normal((V, H)) * 1e-3).astype(np.float32)
+    inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
+    with open(inp, "wb") as f:
+        f.write(np.array([N, H, V, C], dtype="<i8").tobytes())
+        f.write(np.array([T, m], dtype="<f4").tobytes())
+        f.write(h.view(torch.int16).numpy().astype("<i2").tobytes())
+        f.write(W.view(torch.int16).numpy().astype("<i2").tobytes())
+        f.write(y.numpy().astype("<i8").tobytes())
+        f.write(G0.astype("<f4").tobytes())
+    r = subprocess.run([client, "vp", str(inp), str(out), str(S)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    raw = open(out, "rb").read()
+    o = 0
+    sc = np.frombuffer(raw, "<f4", 2, o); o += 8
+    codes = np.frombuffer(raw, "<i4", 2, o); o += 8
+    pred = np.frombuffer(raw, "<i8", N, o); o += 8 * N
+    gh = np.frombuffer(raw, "<f4", N * H, o); o += 4 * N * H
+    gw = np.frombuffer(raw, "<f4", V * H, o); o += 4 * V * H
+    assert o == len(raw) and list(codes) == [0, 0]
+
+    dev = torch.device("cuda", 0)
+    ref = flce.flce_forward(h.to(dev), W.to(dev), y.to(dev), softcap=T, out_mult=m, chunk_rows=C)
+    torch.cuda.synchronize()
+    assert np.array_equal(pred, ref["predicted"].cpu().numpy())
+    assert float(sc[1]) == float(ref["token_accuracy"])
+    assert abs(float(sc[0]) - float(ref["loss"])) <= 1e-6 * abs(float(ref["loss"]))
+    orc = flce_oracle(h, W, y, softcap=T, out_mult=m, grad_W0=G0.astype(np.float64))
+    assert np.abs(gh.reshape(N, H) - orc["grad_h"]).max() <= 1e-2 * np.abs(orc["grad_h"]).max()
+    gwd = gw.reshape(V, H).astype(np.float64)
+    assert np.abs(gwd - orc["grad_W"]).max() <= 1e-2 * np.abs(orc["grad_W"] - G0).max()
