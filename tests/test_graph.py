@@ -105,3 +105,50 @@ def test_vocab_parallel_step_on_cta_pairs_captured_and_replayed(flce):
         torch.cuda.synchronize()
         assert float(out["loss"]) == float(ref["loss"]) and torch.equal(out["predicted"], ref["predicted"])
         assert torch.equal(gh, ref_gh) and torch.equal(gW, ref_gW)
+
+
+def test_two_host_threads_on_two_streams(flce):
+    """Two host threads, each on its own stream (and so its own cached
+    workspace), call the library at once: every result equals the serial one
+    bit for bit, and the status stays 0."""
+    import threading
+    N, H, V = 600, 192, 7000
+    ins = []
+    for i in range(2):
+        ins.append((workloads.make_hidden(N, H, 40 + i).to(DEV), workloads.make_weight(V, H, 40 + i).to(DEV),
+                    workloads.make_labels(N, V, 40 + i, 0.05).to(DEV)))
+    refs = []
+    for h, W, y in ins:
+        o = flce.flce_forward_backward(h, W, y, return_predicted=True, softcap=30.0)
+        torch.cuda.synchronize()
+        refs.append((float(o["loss"]), o["predicted"].clone(), o["grad_h"].clone()))
+    results = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(DEV)
+            st = torch.cuda.Stream(DEV)
+            h, W, y = ins[i]
+            st.wait_stream(torch.cuda.default_stream(DEV))
+            outs = []
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    o = flce.flce_forward_backward(h, W, y, return_predicted=True, softcap=30.0)
+                    outs.append((o["loss"], o["predicted"], o["grad_h"]))
+                st.synchronize()
+                assert flce.flce_get_status() == 0
+            results[i] = outs
+        except Exception as e:  # surfaced below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    for i in range(2):
+        for loss, pred, gh in results[i]:
+            assert float(loss) == refs[i][0]
+            assert torch.equal(pred, refs[i][1]) and torch.equal(gh, refs[i][2])
