@@ -755,6 +755,9 @@ int run(const flce_params* params, const Call& c) {
     g.timeout_ns = timeout;
     g.debug_flags = p.flags;
     g.col0 = static_cast<int>(c.vocab_offset);
+    // without predicted tokens to return, the epilogue keeps only what the
+    // token accuracy needs (a shard's partials always carry the argmax)
+    g.no_argmax = (c.predicted == nullptr && !shard) ? 1 : 0;
     const bool store = L.need_z;
     g.store_hint = store ? 1 : 0;
     if (simt) {
@@ -1223,6 +1226,7 @@ int run_f32(const Norm& n, const Call& c) {
     g.status = &hdr->status;
     g.timeout_ns = timeout;
     g.debug_flags = p.flags;
+    g.no_argmax = c.predicted == nullptr ? 1 : 0;
     const bool store = L.need_z;
     g.store_hint = store ? 1 : 0;
     CUtensorMap map_z;

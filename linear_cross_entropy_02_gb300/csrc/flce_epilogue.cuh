@@ -24,6 +24,7 @@ struct RowStats {
   float sum;   // sum of exp(s - mx)
   int arg;     // vocab index of the first maximum
   float tgt;   // s at the label column, when the label falls in this tile
+  bool first;  // (no-argmax form) s at the label is above every earlier column of the tile
 };
 
 __device__ __forceinline__ void row_stats_init(RowStats& st, int col0) {
@@ -31,6 +32,7 @@ __device__ __forceinline__ void row_stats_init(RowStats& st, int col0) {
   st.sum = 0.f;
   st.arg = col0;
   st.tgt = 0.f;
+  st.first = false;
 }
 
 // One level of the adjacent-pairs argmax tree: slot j takes the larger of slots
@@ -43,6 +45,41 @@ __device__ __forceinline__ void pair_level(float (&v)[16], int (&ix)[16]) {
     v[j] = right ? v[2 * j + 1] : v[2 * j];
     ix[j] = right ? ix[2 * j + 1] : ix[2 * j];
   }
+}
+
+// The running sum of exponentials over 32 columns, after the running max has
+// taken in this group: 2^(s log2 e - mx log2 e), one packed FMA per two columns
+// and four running sums (two packed) in the order of four scalar ones.
+__device__ __forceinline__ void row_sum_exp32(RowStats& st, const float (&s)[32]) {
+  const float mx_l2e = st.mx * 1.4426950408889634f;
+  const uint64_t l2e2 = f2_pack(1.4426950408889634f, 1.4426950408889634f);
+  const uint64_t nmx2 = f2_pack(-mx_l2e, -mx_l2e);
+  uint64_t a01 = f2_pack(0.f, 0.f), a23 = a01;
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(s[j], s[j + 1]), l2e2, nmx2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(s[j + 2], s[j + 3]), l2e2, nmx2), x2, x3);
+    a01 = f2_add(a01, f2_pack(ex2_approx(x0), ex2_approx(x1)));
+    a23 = f2_add(a23, f2_pack(ex2_approx(x2), ex2_approx(x3)));
+  }
+  float a0, a1, a2, a3;
+  f2_unpack(a01, a0, a1);
+  f2_unpack(a23, a2, a3);
+  st.sum += (a0 + a1) + (a2 + a3);
+}
+
+// s at column d of the group, without a dynamically indexed (local-memory)
+// array: a predicated select per column.
+__device__ __forceinline__ float select_col32(const float (&s)[32], int d, float t) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool hit = (j == d);
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q mov.f32 %0, %1;\n\t}\n"
+        : "+f"(t)
+        : "f"(s[j]), "r"(static_cast<uint32_t>(hit)));
+  }
+  return t;
 }
 
 // Folds 32 consecutive columns col0 .. col0+31 of one row into `st`, and
@@ -71,30 +108,40 @@ __device__ __forceinline__ float row_stats_update32(RowStats& st, const float (&
     st.mx = cm;
     st.arg = col0 + ix[0];
   }
-  const float mx_l2e = st.mx * 1.4426950408889634f;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    a0 += ex2_approx(fmaf(s[j + 0], 1.4426950408889634f, -mx_l2e));
-    a1 += ex2_approx(fmaf(s[j + 1], 1.4426950408889634f, -mx_l2e));
-    a2 += ex2_approx(fmaf(s[j + 2], 1.4426950408889634f, -mx_l2e));
-    a3 += ex2_approx(fmaf(s[j + 3], 1.4426950408889634f, -mx_l2e));
-  }
-  st.sum += (a0 + a1) + (a2 + a3);
-  // Label gather without a dynamically indexed (local-memory) array: a
-  // predicated select per column, taken only by rows whose label is here.
+  row_sum_exp32(st, s);
+  // the label's logit, taken only by rows whose label is in this group
   const int64_t d64 = label - col0;
-  if (d64 >= 0 && d64 < 32) {
-    const int d = static_cast<int>(d64);
-    float t = st.tgt;
+  if (d64 >= 0 && d64 < 32) st.tgt = select_col32(s, static_cast<int>(d64), st.tgt);
+  return cm;
+}
+
+// The same fold without the argmax, for calls that return token accuracy but
+// not the predicted tokens: the group's max by a tree of three-input maxima,
+// and, in the group holding the row's label (column d of the group, else d
+// outside 0..31), whether the label's logit lies strictly above every earlier
+// column of the tile. The label is the row's first maximum exactly when that
+// holds, the logit equals the tile's max, and no earlier tile reaches it.
+// The sums and the running max take the same steps as row_stats_update32.
+__device__ __forceinline__ float row_stats_update32_noarg(RowStats& st, const float (&s)[32], int d) {
+  float m[11];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const bool hit = (j == d);
-      asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q mov.f32 %0, %1;\n\t}\n"
-          : "+f"(t)
-          : "f"(s[j]), "r"(static_cast<uint32_t>(hit)));
-    }
+  for (int k = 0; k < 10; ++k) m[k] = max3f(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
+  m[10] = fmaxf(s[30], s[31]);
+  const float cm = fmaxf(max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), max3f(m[6], m[7], m[8])),
+                         fmaxf(m[9], m[10]));
+  const float prev = st.mx;  // max of the tile's earlier columns
+  if (cm > st.mx) {
+    st.sum *= ex2_approx((st.mx - cm) * 1.4426950408889634f);
+    st.mx = cm;
+  }
+  row_sum_exp32(st, s);
+  if (d >= 0 && d < 32) {
+    const float t = select_col32(s, d, st.tgt);
+    bool first = prev < t;
+#pragma unroll
+    for (int j = 0; j < 31; ++j) first = first && !(j < d && !(s[j] < t));
     st.tgt = t;
+    st.first = first;
   }
   return cm;
 }

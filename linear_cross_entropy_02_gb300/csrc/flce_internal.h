@@ -90,6 +90,11 @@ struct GemmParams {
   float* part_max;  // [n_tiles][ldp]
   float* part_sum;  // [n_tiles][ldp]
   int32_t* part_idx;  // [n_tiles][ldp]
+  // 1: the call returns no predicted tokens, so part_idx carries only what the
+  // token accuracy needs (the label's column where the label is the tile's
+  // first maximum, else another column of the tile) and the epilogue skips
+  // the argmax; 0 (the default): part_idx is the tile's first maximum
+  int no_argmax;
   float* tgt;       // [ldp]  capped logit at the label
   int ldp;
   float* zbuf;  // capped logits [rows][ldz] (STATS_STORE, and the SIMT path)

@@ -156,7 +156,13 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 // the statistics; 1 also stores the capped logits s in fp32; 2 stores them
 // relative to the maximum of their 32-column group, s - gmax, in fp16 (halving
 // the stored bytes), with gmax in fp32 beside them.
-template <int STORE>
+// ARGMAX: the partial index is the tile's first maximum; without it (calls that
+// need the token accuracy but not the predicted tokens) the index is the
+// label's column when the label is the tile's first maximum, and otherwise a
+// column of the tile other than the label's. The merge then takes the index of
+// the first tile that holds the row's maximum, as before, and it equals the
+// label exactly when the label is the row's first maximum.
+template <int STORE, bool ARGMAX>
 __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtensorMap* zmap, EpiStage& es,
                                                uint32_t tcol, int mb, int nb, int quarter, int lane) {
   const int row = quarter * 32 + lane;
@@ -167,6 +173,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
   const int64_t ylocal = label - p.col0;  // the label as a column of D
   const bool has_label = label != p.ignore_index && ylocal >= n0 && ylocal < n0 + kBN;
   const bool full_tile = n0 + kBN <= p.N_valid;  // no column past V: skip the mask
+  const int ycol = has_label ? static_cast<int>(ylocal) : -1;  // the label's column in this tile, or -1
   RowStats st;
   row_stats_init(st, n0);
   uint32_t held[16];  // STORE == 2: the even group's fp16 values, sent with the odd one
@@ -176,9 +183,14 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
     if (p.softcap > 0.f) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) s[j] = p.softcap * tanhf(__uint_as_float(r[j]) * p.alpha * p.inv_softcap);
+    } else if (p.alpha != 1.f) {
+      const uint64_t al2 = f2_pack(p.alpha, p.alpha);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2)
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), al2), s[j], s[j + 1]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]) * p.alpha;
+      for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
     }
     if (!full_tile) {
 #pragma unroll
@@ -186,13 +198,19 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
         if (col0 + j >= p.N_valid) s[j] = -INFINITY;
     }
     if (STORE == 1) stage_and_send<false>(es, zmap, lane, s, col0, mb * kBM + quarter * 32);
-    const float cm = row_stats_update32(st, s, col0, has_label ? ylocal : -1);
+    const float cm = ARGMAX ? row_stats_update32(st, s, col0, ycol) : row_stats_update32_noarg(st, s, ycol - col0);
     if (STORE == 2) {
-      // A group wholly past V has cm = -inf; its values are never read.
+      // A group wholly past V has cm = -inf: its values are stored as -inf
+      // (never read) and its gmax as 0.
       const float ref = cm == -INFINITY ? 0.f : cm;
+      const uint64_t nref2 = f2_pack(-ref, -ref);
       uint32_t hv[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) hv[j] = cm == -INFINITY ? 0u : pack_half2(s[2 * j] - ref, s[2 * j + 1] - ref);
+      for (int j = 0; j < 16; ++j) {
+        float d0, d1;
+        f2_unpack(f2_add(f2_pack(s[2 * j], s[2 * j + 1]), nref2), d0, d1);
+        hv[j] = pack_half2(d0, d1);
+      }
       if (row_ok) p.gmax[static_cast<int64_t>(grow) * p.ldg + (col0 >> 5)] = ref;
       if ((c & 1) == 0) {
 #pragma unroll
@@ -206,9 +224,22 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
     const int64_t o = static_cast<int64_t>(nb) * p.ldp + grow;
     p.part_max[o] = st.mx;
     p.part_sum[o] = st.sum;
-    p.part_idx[o] = st.arg;
+    if (ARGMAX)
+      p.part_idx[o] = st.arg;
+    else
+      p.part_idx[o] = (has_label && st.first && st.tgt == st.mx) ? ycol : (ycol == n0 ? n0 + 1 : n0);
     if (has_label) p.tgt[grow] = st.tgt;
   }
+}
+
+// The statistics epilogue in the form the call asks for (GemmParams::no_argmax).
+template <int STORE>
+__device__ __forceinline__ void epilogue_stats_any(const GemmParams& p, const CUtensorMap* zmap, EpiStage& es,
+                                                   uint32_t tcol, int mb, int nb, int quarter, int lane) {
+  if (p.no_argmax)
+    epilogue_stats<STORE, false>(p, zmap, es, tcol, mb, nb, quarter, lane);
+  else
+    epilogue_stats<STORE, true>(p, zmap, es, tcol, mb, nb, quarter, lane);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -551,11 +582,11 @@ __global__ void __launch_bounds__(gemm_threads(TMH), 1)
         if (mb >= p.m_tiles) break;
         const uint32_t tcol = t_lane + static_cast<uint32_t>((acc + hh) * kBN);
         if (MODE == EPI_STATS) {
-          epilogue_stats<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_STATS_STORE) {
-          epilogue_stats<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_STATS_STORE16) {
-          epilogue_stats<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_BF16) {
           epilogue_bf16(p, tcol, mb, nb, row);
         } else if (MODE == EPI_ACC_F32) {
@@ -780,11 +811,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (mb < p.m_tiles) {
         const uint32_t tcol = t_lane + static_cast<uint32_t>(acc * kBN);
         if (MODE == EPI_STATS) {
-          epilogue_stats<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<0>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_STATS_STORE) {
-          epilogue_stats<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<1>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_STATS_STORE16) {
-          epilogue_stats<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
+          epilogue_stats_any<2>(p, &tma_c, es, tcol, mb, nb, quarter, lane);
         } else if (MODE == EPI_BF16) {
           epilogue_bf16(p, tcol, mb, nb, row);
         } else if (MODE == EPI_ACC_F32) {
