@@ -61,6 +61,10 @@ def _config(w: workloads.Workload, chunk_rows: int, chunk_used: int = 0):
                         f"mode={w.mode}",
             "n_rows": w.n_rows, "hidden": w.hidden, "vocab": w.vocab, "softcap": w.softcap,
             "out_mult": w.out_mult, "mode": w.mode, "chunk_rows": chunk_rows,
+            "outputs": {"fwd_bwd": "loss, token_accuracy, grad_h, grad_W",
+                        "fwd_grad_h": "loss, token_accuracy, grad_h",
+                        "ce_only": "loss, token_accuracy"}[w.mode]
+                       + (", predicted_tokens" if w.return_predicted and w.mode != "ce_only" else ""),
             **({"chunk_rows_used": chunk_used} if chunk_used else {}),
             "l2": "inputs larger than L2 (no flush needed)"}
 
@@ -715,14 +719,18 @@ def main():
                     help="256 x 256 GEMM tiles on CTA pairs (FLCE_FLAG_CTA_PAIR)")
     ap.add_argument("--vocab-shards", type=int, default=0,
                     help="time the vocabulary-parallel form with this many shards, run in turn on one GPU")
+    ap.add_argument("--predicted", action="store_true",
+                    help="also return the predicted tokens (the epilogue then computes the argmax)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
+    import dataclasses
     if args.rows or args.vocab:
         # a smaller case of the same head (used for profiler captures, never for the bench line)
-        import dataclasses
         w = dataclasses.replace(w, name=f"{w.name}-small", n_rows=args.rows or w.n_rows,
                                 vocab=args.vocab or w.vocab)
+    if args.predicted and w.mode != "ce_only":
+        w = dataclasses.replace(w, return_predicted=True)
     if args.fp32_3pass:
         args.fp32 = True
     if args.impl == "reference":

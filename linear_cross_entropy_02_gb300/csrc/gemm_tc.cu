@@ -181,8 +181,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
     float s[32];
     const int col0 = n0 + c * 32;
     if (p.softcap > 0.f) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) s[j] = p.softcap * tanhf(__uint_as_float(r[j]) * p.alpha * p.inv_softcap);
+      softcap32(s, r, p.alpha, p.softcap, p.inv_softcap);
     } else if (p.alpha != 1.f) {
       const uint64_t al2 = f2_pack(p.alpha, p.alpha);
 #pragma unroll
@@ -301,14 +300,19 @@ __device__ __forceinline__ void epilogue_dz(const GemmParams& p, uint32_t tcol, 
     uint32_t r[32];
     tmem_load_32cols(tcol + c * 32, r);
     tmem_load_wait();
+    float sv[32];  // the capped logits, as the forward statistics computed them
+    if (p.softcap > 0.f) {
+      softcap32(sv, r, p.alpha, p.softcap, p.inv_softcap);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(r[j]) * p.alpha;
+    }
     float d[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      const float z = __uint_as_float(r[j]) * p.alpha;
-      const float sv = p.softcap > 0.f ? p.softcap * tanhf(z * p.inv_softcap) : z;
-      float q = __expf(sv - lse) - (static_cast<int64_t>(n0 + c * 32 + j) == ylocal ? 1.f : 0.f);
+      float q = __expf(sv[j] - lse) - (static_cast<int64_t>(n0 + c * 32 + j) == ylocal ? 1.f : 0.f);
       if (p.softcap > 0.f) {
-        const float u = sv * p.inv_softcap;
+        const float u = sv[j] * p.inv_softcap;
         q *= (1.f - u * u);
       }
       d[j] = ci * q;
