@@ -177,6 +177,7 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
   RowStats st;
   row_stats_init(st, n0);
   uint32_t held[16];  // STORE == 2: the even group's fp16 values, sent with the odd one
+  float gm0 = 0.f, gm1 = 0.f, gm2 = 0.f;  // STORE == 2: gmax of groups 4k .. 4k+2, stored with 4k+3
   tmem_row_chunks(tcol, [&](const uint32_t(&r)[32], int c) {
     float s[32];
     const int col0 = n0 + c * 32;
@@ -210,7 +211,19 @@ __device__ __forceinline__ void epilogue_stats(const GemmParams& p, const CUtens
         f2_unpack(f2_add(f2_pack(s[2 * j], s[2 * j + 1]), nref2), d0, d1);
         hv[j] = pack_half2(d0, d1);
       }
-      if (row_ok) p.gmax[static_cast<int64_t>(grow) * p.ldg + (col0 >> 5)] = ref;
+      // four groups' maxima in one 16-byte store (ldg and the tile's first
+      // group are multiples of 8)
+      const int q = c & 3;
+      if (q == 0) {
+        gm0 = ref;
+      } else if (q == 1) {
+        gm1 = ref;
+      } else if (q == 2) {
+        gm2 = ref;
+      } else if (row_ok) {
+        *reinterpret_cast<float4*>(p.gmax + static_cast<int64_t>(grow) * p.ldg + (col0 >> 5) - 3) =
+            make_float4(gm0, gm1, gm2, ref);
+      }
       if ((c & 1) == 0) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) held[j] = hv[j];
