@@ -156,3 +156,37 @@ def test_fp32_inputs_accuracy_without_argmax(flce):
     assert c1 == _count(f2["token_accuracy"], planted.cpu()) == _count(acc_c, planted.cpu())
     assert c1 == int(((f1["predicted"].cpu() == planted.cpu()) & (planted.cpu() != -100)).sum())
     assert c1 >= int((planted.cpu() != -100).sum()) // 2 - 1
+
+
+@pytest.mark.parametrize("V", [1, 7, 300, 513])
+def test_all_logits_tied(flce, V):
+    """W = 0: every logit of every row is 0, so the first maximum is column 0.
+    A row is correct exactly when its label is 0, on every entry point; with
+    V = 1, 7 the whole vocabulary is one partial group, with 300 and 513 the
+    last tile is masked."""
+    N, H = 80, 64
+    h = workloads.make_hidden(N, H, 44)
+    W = torch.zeros((V, H), dtype=torch.bfloat16)
+    y = workloads.make_labels(N, V, 44, 0.1)
+    y[:7] = 0
+    counts, from_pred, pred = _all_paths(flce, h, W, y)
+    assert torch.all(pred == 0)
+    expect = int(((y == 0) & (y != -100)).sum())
+    assert from_pred == expect >= 7
+    assert set(counts.values()) == {expect}, counts
+
+
+def test_zero_rows_among_random_rows(flce):
+    """Rows of h that are all zero have all-tied logits (first maximum 0);
+    the other rows keep their own argmax; labels planted on both kinds."""
+    N, H, V = 120, 96, 1100
+    h = workloads.make_hidden(N, H, 45)
+    W = workloads.make_weight(V, H, 45, std=0.1)
+    h[::4] = 0
+    y = workloads.make_labels(N, V, 45, 0.0)
+    y[::8] = 0                       # zero rows labelled 0: correct
+    y[4::8] = 5                      # zero rows labelled 5: wrong
+    counts, from_pred, pred = _all_paths(flce, h, W, y)
+    assert torch.all(pred[::4] == 0)
+    assert set(counts.values()) == {from_pred}, counts
+    assert from_pred >= N // 8
