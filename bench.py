@@ -721,6 +721,8 @@ def main():
                     help="time the vocabulary-parallel form with this many shards, run in turn on one GPU")
     ap.add_argument("--predicted", action="store_true",
                     help="also return the predicted tokens (the epilogue then computes the argmax)")
+    ap.add_argument("--no-predicted", action="store_true",
+                    help="return no predicted tokens (the epilogue keeps only what the accuracy needs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
@@ -731,6 +733,8 @@ def main():
                                 vocab=args.vocab or w.vocab)
     if args.predicted and w.mode != "ce_only":
         w = dataclasses.replace(w, return_predicted=True)
+    if args.no_predicted:
+        w = dataclasses.replace(w, return_predicted=False)
     if args.fp32_3pass:
         args.fp32 = True
     if args.impl == "reference":

@@ -75,7 +75,9 @@ WORKLOADS = {
     "llama": Workload("llama", 8192, 4096, 128256, 0.05, seed=1),
     "muse": Workload("muse", 8192, 6656, 202048, 0.05, softcap=30.0, out_mult=0.5,
                      return_predicted=True, seed=2),
-    "dsv3": Workload("dsv3", 32768, 7168, 129280, 0.03, labels="zipf", zipf_s=1.1, seed=3),
+    # the DeepSeek-V3 training head returns the predicted tokens beside the token
+    # accuracy (Liger-Kernel DeepSeek-V3 support, Summary: lce_forward's output)
+    "dsv3": Workload("dsv3", 32768, 7168, 129280, 0.03, labels="zipf", zipf_s=1.1, return_predicted=True, seed=3),
     "frozen_ce": Workload("frozen_ce", 131072, 4096, 151936, 0.10, mode="ce_only",
                           row_shape=(16, 4, 2048), seed=4),
     "frozen_grad_h": Workload("frozen_grad_h", 131072, 4096, 151936, 0.10, mode="fwd_grad_h",
