@@ -11,6 +11,7 @@ import os
 import re
 
 import numpy as np
+import pytest
 
 SRC = os.path.join(os.path.dirname(__file__), "..", "linear_cross_entropy_02_gb300", "csrc", "flce_epilogue.cuh")
 
@@ -83,3 +84,33 @@ def test_error_bound_against_fp64_tanh():
         assert np.array_equal(_kernel_form(-u, T, c), -s)
     z = _kernel_form(np.array([0.0, -0.0], dtype=np.float32), 30.0, c)
     assert z[0] == 0 and not np.signbit(z[0]) and np.signbit(z[1])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("softcap", [0.5, 5.5, 30.0])
+def test_capped_row_lse_against_fp64(softcap):
+    """Every row's lse on the GPU against the fp64 oracle, to 2e-6 relative.
+    The logits z have a standard deviation of 0.8: with T = 30 every 32 x 32
+    group of a warp takes the polynomial form, with T = 0.5 every group falls
+    back to tanhf, and with T = 5.5 (|z| > T/2 at 3.4 sigma) about half the
+    groups take each, within the same rows."""
+    import torch
+
+    import __graft_entry__
+    import workloads
+    from oracle import flce_oracle
+    __graft_entry__.build()
+    import linear_cross_entropy_02_gb300 as flce
+
+    N, H, V = 256, 256, 3000
+    h = workloads.make_hidden(N, H, 61)
+    W = workloads.make_weight(V, H, 61, std=0.1)
+    y = workloads.make_labels(N, V, 61, 0.1)
+    dev = torch.device("cuda", 0)
+    f = flce.flce_forward(h.to(dev), W.to(dev), y.to(dev), softcap=softcap, out_mult=0.5, return_lse=True)
+    torch.cuda.synchronize()
+    assert flce.flce_get_status() == 0
+    ref = flce_oracle(h, W, y, softcap=softcap, out_mult=0.5, need_grad_h=False, need_grad_W=False)
+    lse = f["lse"].double().cpu().numpy()
+    rel = np.abs(lse - ref["lse"]) / np.abs(ref["lse"])
+    assert rel.max() <= 2e-6, rel.max()
