@@ -195,7 +195,11 @@ int flce_ce_only_noalloc(const flce_params* p, const void* h, const void* W, con
                          float* loss, float* token_accuracy, int32_t* device_status, void* stream);
 
 /* Forward: as flce_ce_only, plus optional per-row outputs predicted [N]
- * (int64, argmax for every row) and row_lse [N] (fp32 log-sum-exp of s_i). */
+ * (int64, argmax for every row) and row_lse [N] (fp32 log-sum-exp of s_i).
+ * With predicted NULL (here, in flce_forward_backward and in flce_ce_only) the
+ * forward epilogue skips the argmax and keeps only what token_accuracy needs:
+ * whether each row's label is its first maximum. The accuracy is the same,
+ * bit for bit. */
 int flce_forward(const flce_params* p, const void* h, const void* W, const int64_t* labels,
                  float* loss, float* token_accuracy, int64_t* predicted, float* row_lse,
                  void* workspace, size_t workspace_bytes, void* stream);
