@@ -78,18 +78,6 @@ __device__ __forceinline__ void row_stats_init(RowStats& st, int col0) {
   st.first = false;
 }
 
-// One level of the adjacent-pairs argmax tree: slot j takes the larger of slots
-// 2j and 2j+1 (which cover lower and higher columns); equal values keep the left.
-template <int W>
-__device__ __forceinline__ void pair_level(float (&v)[16], int (&ix)[16]) {
-#pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const bool right = v[2 * j + 1] > v[2 * j];
-    v[j] = right ? v[2 * j + 1] : v[2 * j];
-    ix[j] = right ? ix[2 * j + 1] : ix[2 * j];
-  }
-}
-
 // The running sum of exponentials over 32 columns, after the running max has
 // taken in this group: 2^(s log2 e - mx log2 e), one packed FMA per two columns
 // and four running sums (two packed) in the order of four scalar ones.
@@ -127,29 +115,32 @@ __device__ __forceinline__ float select_col32(const float (&s)[32], int d, float
 
 // Folds 32 consecutive columns col0 .. col0+31 of one row into `st`, and
 // returns the largest of the 32 values.
-// Argmax over the 32 by a tree of adjacent pairs, so the left operand always
-// holds the lower columns and a strict comparison keeps the lowest index on
-// ties; against earlier columns the running max is also replaced only on a
-// strict increase. exp(s - mx) is computed as 2^(s log2 e - mx log2 e).
+// The group's max comes from the maxima of its four 8-column quarters (trees
+// of three-input maxima). Only where it raises the running max, that is where
+// the tile gets a new first maximum, is its column looked up: the first
+// quarter whose max equals it, then the first column of that quarter that
+// does. Earlier columns win every tie, and against earlier groups the running
+// max is replaced only on a strict increase, so the index is the lowest one
+// holding the tile's maximum. exp(s - mx) is computed as 2^(s log2 e - mx log2 e).
 __device__ __forceinline__ float row_stats_update32(RowStats& st, const float (&s)[32], int col0,
                                                     int64_t label) {
-  float v[16];
-  int ix[16];
+  float q[4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const bool right = s[2 * j + 1] > s[2 * j];
-    v[j] = right ? s[2 * j + 1] : s[2 * j];
-    ix[j] = right ? 2 * j + 1 : 2 * j;
-  }
-  pair_level<8>(v, ix);
-  pair_level<4>(v, ix);
-  pair_level<2>(v, ix);
-  pair_level<1>(v, ix);
-  const float cm = v[0];
+  for (int k = 0; k < 4; ++k)
+    q[k] = max3f(max3f(s[8 * k], s[8 * k + 1], s[8 * k + 2]), max3f(s[8 * k + 3], s[8 * k + 4], s[8 * k + 5]),
+                 fmaxf(s[8 * k + 6], s[8 * k + 7]));
+  const float cm = max3f(q[0], q[1], fmaxf(q[2], q[3]));
   if (cm > st.mx) {
     st.sum *= ex2_approx((st.mx - cm) * 1.4426950408889634f);
     st.mx = cm;
-    st.arg = col0 + ix[0];
+    const bool in0 = q[0] == cm, in1 = q[1] == cm, in2 = q[2] == cm;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = in0 ? s[j] : in1 ? s[8 + j] : in2 ? s[16 + j] : s[24 + j];
+    int jj = 7;
+#pragma unroll
+    for (int j = 6; j >= 0; --j) jj = v[j] == cm ? j : jj;
+    st.arg = col0 + (in0 ? 0 : in1 ? 8 : in2 ? 16 : 24) + jj;
   }
   row_sum_exp32(st, s);
   // the label's logit, taken only by rows whose label is in this group
