@@ -421,6 +421,7 @@ def run_ours(args, w):
                                           return_predicted=w.return_predicted, **kw, **bkw)
 
     vp_forward = None
+    status_workspaces = []  # explicit workspaces whose status words are checked too
     if args.vocab_shards:
         # The vocabulary-parallel form, its S shards run one after another on
         # this GPU: every shard's forward, the gather (a stack in shard order),
@@ -432,9 +433,18 @@ def run_ours(args, w):
         gW_sh = [None if gW is None else gW[offsets[k]:offsets[k + 1]] for k in range(S)]
         gh32 = torch.empty((w.n_rows, w.hidden), dtype=torch.float32, device=dev)
         vkw = dict(softcap=w.softcap, out_mult=w.out_mult, chunk_rows=args.chunk_rows, flags=kw["flags"])
+        # --vp-stored: each shard keeps its logits between its two calls, in a
+        # workspace of its own (FLCE_FLAG_VP_STORED)
+        vp_ws = [None] * S
+        if args.vp_stored:
+            vkw["flags"] |= flce.FLCE_FLAG_VP_STORED
+            vp_ws = [flce.flce_vp_workspace(h, shards[k], keep_logits=True, chunk_rows=args.chunk_rows)
+                     for k in range(S)]
+            status_workspaces.extend(vp_ws)
 
         def step():
-            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, **vkw) for k in range(S)]
+            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, workspace=vp_ws[k], **vkw)
+                     for k in range(S)]
             allp = torch.stack(parts)
             gh32.zero_()
             out = None
@@ -442,24 +452,25 @@ def run_ours(args, w):
                 out = flce.flce_vp_backward(h, shards[k], lab, allp, offsets, offsets[k], w.vocab,
                                             grad_h_partial=gh32 if w.mode != "ce_only" else None,
                                             grad_W=gW_sh[k], vocab_slab=args.vocab_slab,
-                                            return_predicted=w.return_predicted, **vkw)
+                                            return_predicted=w.return_predicted, workspace=vp_ws[k], **vkw)
             if w.mode != "ce_only":
                 flce.flce_scale_gradient(gh32, None, out_dtype=h.dtype)
             return out
 
         def vp_forward():
-            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, **vkw) for k in range(S)]
+            parts = [flce.flce_vp_forward(h, shards[k], lab, offsets[k], w.vocab, workspace=vp_ws[k], **vkw)
+                     for k in range(S)]
             return flce.flce_vp_backward(h, shards[0], lab, torch.stack(parts), offsets, 0, w.vocab,
-                                         return_predicted=True, return_lse=True, **vkw)
+                                         return_predicted=True, return_lse=True, workspace=vp_ws[0], **vkw)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if flce.flce_get_status() != 0:
+    if flce.flce_get_status() != 0 or any(flce.flce_get_status(workspace=x) for x in status_workspaces):
         raise RuntimeError(f"device status {flce.flce_get_status()} after warm-up")
 
     (ms, per_step, kernels, launches, clocks), remeasured = timed_steps_checked(flce, step, args.steps, local, dist)
-    if flce.flce_get_status() != 0:
+    if flce.flce_get_status() != 0 or any(flce.flce_get_status(workspace=x) for x in status_workspaces):
         raise RuntimeError(f"device status {flce.flce_get_status()} after timed steps")
     ms_max = _max_over_ranks(dist, ms)
     rows_total = _sum_over_ranks(dist, float(w.n_rows))
@@ -552,16 +563,19 @@ def run_ours(args, w):
             "tflops": tflops, "pct_of_peak": 100.0 * tflops / step_peak,
             "peak_tflops": step_peak, "peak_source": peaks["source"] + (" x tf32/bf16 nominal" if args.fp32 else ""),
             "flops_per_step": flops,
-            "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if (args.low_memory or args.vocab_shards)
+            "executed_tensor_flops_per_step": flops * (4.0 / 3.0 if (args.low_memory or (args.vocab_shards and
+                                                                                       not args.vp_stored))
                                                        and w.mode == "fwd_bwd" else 1.0)
                                                     * (3.0 if args.fp32_3pass else 1.0),
-            "backward": "recompute (low memory)" if (args.low_memory or args.vocab_shards) else "stored logits",
+            "backward": ("recompute (low memory)" if (args.low_memory or (args.vocab_shards and not args.vp_stored))
+                         else "stored logits"),
             "gemm_cta_tile": ("128x256, two accumulators" if args.tile128
                               else "per GEMM: 256x256 unless too few tiles to fill the SMs evenly"
                               + ("; each on a CTA pair (cta_group::2), two accumulators per SM"
                                  if args.pair else "")),
             "roofline": roof, "cpu_baseline": cpu,
             **({"vocab_shards": {"shards": args.vocab_shards, "run": "in turn on one GPU",
+                                 "logits": "kept between the shard calls" if args.vp_stored else "recomputed",
                                  "exchange_bytes_per_step": 16 * w.n_rows * args.vocab_shards}}
                if args.vocab_shards else {}),
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": UNIT,
@@ -717,6 +731,9 @@ def main():
                     help="time the cross-entropy on materialised bf16 logits [N, V] instead")
     ap.add_argument("--pair", action="store_true",
                     help="256 x 256 GEMM tiles on CTA pairs (FLCE_FLAG_CTA_PAIR)")
+    ap.add_argument("--vp-stored", action="store_true",
+                    help="with --vocab-shards: each shard keeps its logits between its two calls "
+                         "(FLCE_FLAG_VP_STORED; 6NHV instead of 8NHV)")
     ap.add_argument("--vocab-shards", type=int, default=0,
                     help="time the vocabulary-parallel form with this many shards, run in turn on one GPU")
     ap.add_argument("--predicted", action="store_true",

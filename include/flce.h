@@ -129,6 +129,15 @@ extern "C" {
                                         pair of CTAs (a cluster of two SMs, tcgen05 cta_group::2):
                                         each SM holds 128 rows, so its accumulator is double-
                                         buffered and the epilogue overlaps the next tile's MMAs */
+#define FLCE_FLAG_VP_STORED 256      /* vocab shards (flce_vp_forward / flce_vp_backward): the
+                                        forward keeps the shard's capped logits in the workspace
+                                        (fp16, relative to each 32-column group's max, as the
+                                        fused backward stores them) and the backward forms
+                                        dlogits from them instead of recomputing the logits:
+                                        6 N H V_k tensor flops per shard instead of 8, and
+                                        O(N * V_k) workspace. N <= 32768 per call pair; the two
+                                        calls take the same params and the same workspace, which
+                                        nothing else may use in between */
 
 typedef struct flce_params {
   int64_t n_rows;        /* N >= 0 */
@@ -292,7 +301,9 @@ int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_
  * The backward recomputes the shard's logits per vocab slab, as
  * FLCE_FLAG_RECOMPUTE does, so only the partials cross shards and no logits
  * are kept between the calls: 8 N H V_k tensor flops per shard, transient
- * memory O(C * vocab_slab + N). bf16 operands only (FLCE_ERR_UNSUPPORTED for
+ * memory O(C * vocab_slab + N). With FLCE_FLAG_VP_STORED the forward keeps
+ * them in the workspace instead (6 N H V_k flops, O(N * V_k) memory; a caller
+ * with more rows makes one call pair per block of rows). bf16 operands only (FLCE_ERR_UNSUPPORTED for
  * fp32, FLCE_FLAG_SIMT_GEMM and FLCE_FLAG_KMAJOR_BWD).
  * In both calls p->vocab is V_k, the shard's row count, and W_shard is
  * [V_k, ld_w]; labels are checked against [0, vocab_total) (FLCE_ERR_LABEL).
@@ -303,11 +314,15 @@ int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_
 
 /* Workspace bytes of flce_vp_forward (backward = 0) or flce_vp_backward
  * (backward = 1; need_grad_h / need_grad_W as that call will have them). The
- * backward's includes 4 bytes of lse per row (all N rows). 0 if invalid. */
+ * backward's includes 4 bytes of lse per row (all N rows). With
+ * FLCE_FLAG_VP_STORED both calls need the same size, which holds the kept
+ * logits (about N * V_k * 4.1 bytes with their dlogits). 0 if invalid. */
 size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_h, int need_grad_W);
 
 /* Forward of one shard: writes partials [4][N] (device). FLCE_ERR_ARG when
- * [vocab_offset, vocab_offset + V_k) is not inside [0, vocab_total). */
+ * [vocab_offset, vocab_offset + V_k) is not inside [0, vocab_total), and with
+ * FLCE_FLAG_VP_STORED when N > 32768 or with FLCE_FLAG_RECOMPUTE or
+ * FLCE_FLAG_KMAJOR_BWD. */
 int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, const void* h,
                     const void* W_shard, const int64_t* labels, float* partials, void* workspace,
                     size_t workspace_bytes, void* stream);

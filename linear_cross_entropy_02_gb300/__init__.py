@@ -23,7 +23,8 @@ import torch
 
 from . import _lib
 from ._lib import (FLCE_FLAG_KMAJOR_BWD, FLCE_FLAG_RECOMPUTE, FLCE_FLAG_SIMT_GEMM, FLCE_FLAG_TEST_STALL,  # noqa: F401
-                   FLCE_FLAG_TILE128, FLCE_FLAG_TILE256, FLCE_FLAG_CTA_PAIR, FLCE_FLAG_F32_3PASS, FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,
+                   FLCE_FLAG_TILE128, FLCE_FLAG_TILE256, FLCE_FLAG_CTA_PAIR, FLCE_FLAG_F32_3PASS, FLCE_FLAG_VP_STORED,
+                   FLCE_MODE_CE_ONLY, FLCE_MODE_FORWARD,
                    FLCE_MODE_FORWARD_BACKWARD, FLCE_REDUCTION_MEAN, FLCE_REDUCTION_SUM, FlceError, FlceParams)
 
 __all__ = [
@@ -32,7 +33,7 @@ __all__ = [
     "flce_scale_gradient", "flce_workspace_size", "flce_chunk_rows", "flce_chunk_rows_for_budget", "flce_release_workspaces", "flce_get_status", "flce_launch_count",
     "flce_profile_begin",
     "flce_profile_read", "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "FlceError",
-    "flce_vp_forward", "flce_vp_backward", "vocab_parallel_linear_cross_entropy", "vp_shard_table",
+    "flce_vp_forward", "flce_vp_backward", "flce_vp_workspace", "vocab_parallel_linear_cross_entropy", "vp_shard_table",
     "vp_gather_partials", "vp_reduce_grad_h",
 ]
 
@@ -283,12 +284,42 @@ def _vp_params(h2, W, softcap, out_mult, ignore_index, reduction, grad_scale, ch
                    reduction, grad_scale, chunk_rows, flags, timeout_ns, vocab_slab, _dtype_code(h2))
 
 
+def _vp_workspace(dev, nbytes: int, workspace: Optional[torch.Tensor], flags: int) -> torch.Tensor:
+    if workspace is None:
+        if flags & FLCE_FLAG_VP_STORED:
+            raise ValueError("FLCE_FLAG_VP_STORED keeps the logits in the workspace between the two calls: "
+                             "pass the same workspace= (from flce_vp_workspace) to both")
+        return _workspace(dev, nbytes)
+    if workspace.dtype != torch.uint8 or workspace.device != dev or workspace.numel() < nbytes:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {nbytes} bytes on {dev}")
+    return workspace
+
+
+def flce_vp_workspace(h, W_shard, *, keep_logits=False, backward=True, need_grad_h=True, need_grad_W=True,
+                      chunk_rows=0, vocab_slab=0, flags=0) -> torch.Tensor:
+    """A device workspace (uint8) for flce_vp_forward / flce_vp_backward on
+    these shapes. With keep_logits (FLCE_FLAG_VP_STORED) one workspace serves
+    both calls and holds the shard's logits between them."""
+    H = W_shard.shape[1]
+    h2 = _rows2d(h, H)
+    if keep_logits:
+        flags |= FLCE_FLAG_VP_STORED
+    p = _vp_params(h2, W_shard, 0.0, 1.0, -100, "mean", 1.0, chunk_rows, flags, 0, vocab_slab)
+    nbytes = _native(h.device, "flce_vp_workspace_size", ctypes.byref(p), int(backward), int(need_grad_h),
+                     int(need_grad_W))
+    if nbytes == 0:
+        raise FlceError(_lib.FLCE_ERR_ARG, "flce_vp_workspace_size")
+    return torch.empty(nbytes, dtype=torch.uint8, device=h.device)
+
+
 def flce_vp_forward(h, W_shard, labels, vocab_offset: int, vocab_total: int, *, softcap=0.0, out_mult=1.0,
-                    ignore_index=-100, chunk_rows=0, flags=0, timeout_ns=0) -> torch.Tensor:
+                    ignore_index=-100, chunk_rows=0, flags=0, timeout_ns=0,
+                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Forward of one vocab shard (W_shard holds the rows of vocab ids
     [vocab_offset, vocab_offset + V_k) of vocab_total): returns this shard's
     per-row partials, an fp32 [4, N] CUDA tensor (max, sum of exp, argmax id
-    as int32 bits, label logit or 0)."""
+    as int32 bits, label logit or 0). With FLCE_FLAG_VP_STORED in flags the
+    shard's logits stay in `workspace` for flce_vp_backward."""
     _check(h, W_shard, labels)
     H = W_shard.shape[1]
     h2 = _rows2d(h, H)
@@ -299,7 +330,7 @@ def flce_vp_forward(h, W_shard, labels, vocab_offset: int, vocab_total: int, *, 
     nbytes = _native(h.device, "flce_vp_workspace_size", ctypes.byref(p), 0, 0, 0)
     if nbytes == 0:
         raise FlceError(_lib.FLCE_ERR_ARG, "flce_vp_workspace_size")
-    ws = _workspace(h.device, nbytes)
+    ws = _vp_workspace(h.device, nbytes, workspace, flags)
     part = torch.empty((4, h2.shape[0]), dtype=torch.float32, device=h.device)
     rc = _native(h.device, "flce_vp_forward", ctypes.byref(p), int(vocab_offset), int(vocab_total), _ptr(h2),
                  _ptr(W_shard), _ptr(lab), _ptr(part), _ptr(ws), nbytes, _stream_handle(h.device))
@@ -311,11 +342,13 @@ def flce_vp_backward(h, W_shard, labels, all_partials: torch.Tensor, shard_offse
                      vocab_total: int, *, grad_h_partial: Optional[torch.Tensor] = None,
                      grad_W: Optional[torch.Tensor] = None, softcap=0.0, out_mult=1.0, ignore_index=-100,
                      reduction="mean", grad_scale=1.0, return_predicted=True, return_lse=False, chunk_rows=0,
-                     vocab_slab=0, flags=0, timeout_ns=0) -> dict:
+                     vocab_slab=0, flags=0, timeout_ns=0, workspace: Optional[torch.Tensor] = None) -> dict:
     """Backward of one vocab shard given every shard's partials ([S, 4, N], in
     shard order) and the shard table (S + 1 vocab offsets). grad_h_partial
     (fp32 [N, H]) and grad_W (this shard's fp32 [V_k, H]) are ACCUMULATED in
-    place when given. Returns dict(loss, token_accuracy, predicted, lse)."""
+    place when given. Returns dict(loss, token_accuracy, predicted, lse).
+    With FLCE_FLAG_VP_STORED it reads the logits that flce_vp_forward kept in
+    `workspace` (the same params and workspace as that call)."""
     _check(h, W_shard, labels)
     H = W_shard.shape[1]
     h2 = _rows2d(h, H)
@@ -338,7 +371,7 @@ def flce_vp_backward(h, W_shard, labels, all_partials: torch.Tensor, shard_offse
                      int(grad_W is not None))
     if nbytes == 0:
         raise FlceError(_lib.FLCE_ERR_ARG, "flce_vp_workspace_size")
-    ws = _workspace(h.device, nbytes)
+    ws = _vp_workspace(h.device, nbytes, workspace, flags)
     dev = h.device
     loss = torch.empty((), dtype=torch.float32, device=dev)
     acc = torch.empty((), dtype=torch.float32, device=dev)
@@ -408,24 +441,30 @@ def vp_reduce_grad_h(grad_h_partial: torch.Tensor, group=None) -> torch.Tensor:
 def vocab_parallel_linear_cross_entropy(h, W_shard, labels, vocab_offset: int, *, group=None,
                                         grad_W: Optional[torch.Tensor] = None, need_grad_h=True, softcap=0.0,
                                         out_mult=1.0, ignore_index=-100, reduction="mean", grad_scale=1.0,
-                                        chunk_rows=0, vocab_slab=0) -> dict:
+                                        chunk_rows=0, vocab_slab=0, keep_logits=False) -> dict:
     """The fused head with W split by vocabulary rows over the ranks of
     `group` (one shard per rank, any order): shard forward, all-gather of the
     per-row partials (16 bytes per row and rank), shard backward, all-reduce of
     the fp32 grad_h parts, rounded to h's dtype by the library's kernel. Every
     rank gets the same loss, token accuracy and predictions; grad_W (this
-    rank's fp32 [V_k, H], optional) is accumulated in place."""
+    rank's fp32 [V_k, H], optional) is accumulated in place. keep_logits keeps
+    each shard's logits between its forward and backward
+    (FLCE_FLAG_VP_STORED: 6 N H V_k flops instead of 8, O(N V_k) memory; at
+    most 32768 rows)."""
     offsets, order = vp_shard_table(vocab_offset, W_shard.shape[0], group)
     V = offsets[-1]
+    flags = FLCE_FLAG_VP_STORED if keep_logits else 0
+    ws = flce_vp_workspace(h, W_shard, keep_logits=True, chunk_rows=chunk_rows) if keep_logits else None
     part = flce_vp_forward(h, W_shard, labels, vocab_offset, V, softcap=softcap, out_mult=out_mult,
-                           ignore_index=ignore_index, chunk_rows=chunk_rows)
+                           ignore_index=ignore_index, chunk_rows=chunk_rows, flags=flags, workspace=ws)
     allp = vp_gather_partials(part, order, group)
     gh32 = None
     if need_grad_h:
         gh32 = torch.zeros((h.reshape(-1, h.shape[-1]).shape[0], h.shape[-1]), dtype=torch.float32, device=h.device)
     out = flce_vp_backward(h, W_shard, labels, allp, offsets, vocab_offset, V, grad_h_partial=gh32, grad_W=grad_W,
                            softcap=softcap, out_mult=out_mult, ignore_index=ignore_index, reduction=reduction,
-                           grad_scale=grad_scale, chunk_rows=chunk_rows, vocab_slab=vocab_slab)
+                           grad_scale=grad_scale, chunk_rows=chunk_rows, vocab_slab=vocab_slab, flags=flags,
+                           workspace=ws)
     gh = None
     if gh32 is not None:
         vp_reduce_grad_h(gh32, group)
@@ -685,12 +724,16 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         return (loss, acc) if self.return_token_accuracy else loss
 
 
-def flce_get_status(device=None) -> int:
+def flce_get_status(device=None, workspace: Optional[torch.Tensor] = None) -> int:
     """Synchronises the current stream and returns the device status word of
-    the last call on the cached workspace of this device and stream (0 = no
-    device error)."""
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    ws = _workspaces.get((dev.index, torch.cuda.current_stream(dev).cuda_stream))
+    the last call on the cached workspace of this device and stream, or on
+    `workspace` when given (0 = no device error)."""
+    if workspace is not None:
+        dev = workspace.device
+        ws = workspace
+    else:
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        ws = _workspaces.get((dev.index, torch.cuda.current_stream(dev).cuda_stream))
     if ws is None:
         return 0
     st = ctypes.c_int32(0)

@@ -40,6 +40,7 @@ FLCE_FLAG_TILE128 = 16
 FLCE_FLAG_TILE256 = 32
 FLCE_FLAG_CTA_PAIR = 64
 FLCE_FLAG_F32_3PASS = 128
+FLCE_FLAG_VP_STORED = 256
 
 FLCE_NUM_KERNELS = 17
 

@@ -421,6 +421,9 @@ struct Call {
   int64_t vocab_total = 0;
   float* shard_partials = nullptr;
   bool shard_call = false;
+  // FLCE_FLAG_VP_STORED: the shard forward stores its logits in the layout
+  // that the shard backward will read them from (make_vp_stored_layout)
+  bool vp_stored = false;
 };
 
 int run_f32(const Norm& n, const Call& c);
@@ -613,6 +616,22 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
   return FLCE_OK;
 }
 
+// The workspace layout that FLCE_FLAG_VP_STORED shares between a shard's
+// forward and backward: the fused forward + backward layout with one chunk of
+// all N rows, so the fp16 logits, their group maxima and the dlogits buffer
+// sit at the same offsets in both calls.
+void make_vp_stored_layout(const Norm& n, Layout* L) {
+  Norm ns = n;
+  ns.p.chunk_rows = std::max<int64_t>(ns.p.n_rows, 1);
+  make_layout(ns, FLCE_MODE_FORWARD_BACKWARD, true, true, L);
+}
+
+int check_vp_stored(const flce_params& p) {
+  if (p.flags & (FLCE_FLAG_RECOMPUTE | FLCE_FLAG_KMAJOR_BWD | FLCE_FLAG_SIMT_GEMM)) return FLCE_ERR_ARG;
+  if (p.n_rows > 32768) return FLCE_ERR_ARG;
+  return FLCE_OK;
+}
+
 int run(const flce_params* params, const Call& c) {
   Norm n;
   int rc = normalise(params, &n);
@@ -632,6 +651,7 @@ int run(const flce_params* params, const Call& c) {
   make_layout(n, !c.host_in ? c.mode
                              : c.mode == FLCE_MODE_CE_ONLY ? FLCE_MODE_CE_ONLY_HOST : FLCE_MODE_FORWARD_BACKWARD_HOST,
               gh, gw, &L);
+  if (c.vp_stored) make_vp_stored_layout(n, &L);  // one chunk; the logits are stored for the backward
   if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   rc = device_info(&sms, &cc);
@@ -1021,17 +1041,27 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
   if (!aligned16(wsv) || (h && !aligned16(h)) || !aligned16(W)) return FLCE_ERR_ALIGN;
   if ((gh_acc && !aligned16(gh_acc)) || (grad_W && !aligned16(grad_W))) return FLCE_ERR_ALIGN;
   const bool grads = gh_acc != nullptr || grad_W != nullptr;
+  // FLCE_FLAG_VP_STORED: the forward's stored logits come first in the
+  // workspace (the layout both calls compute), this call's own part after them
+  const bool stored = (p.flags & FLCE_FLAG_VP_STORED) != 0;
+  if (stored && (rc = check_vp_stored(p)) != FLCE_OK) return rc;
+  Layout Ls{};
+  if (stored) make_vp_stored_layout(n, &Ls);
+  const size_t base = stored ? Ls.total : 0;
   VpLayout L;
-  make_vp_layout(n, grads, &L);
-  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  make_vp_layout(n, grads && !stored, &L);
+  if (ws_bytes < base + L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   rc = device_info(&sms, &cc);
   if (rc != FLCE_OK) return rc;
   if (cc != 103) return FLCE_ERR_UNSUPPORTED;
   if (!load_encoder()) return FLCE_ERR_UNSUPPORTED;
 
-  uint8_t* ws = static_cast<uint8_t*>(wsv);
-  Header* hdr = reinterpret_cast<Header*>(ws + L.off_hdr);
+  uint8_t* ws_all = static_cast<uint8_t*>(wsv);
+  uint8_t* ws = ws_all + base;
+  // the status word stays at the start of the workspace (flce_get_status):
+  // with stored logits this call takes over the forward's header there
+  Header* hdr = reinterpret_cast<Header*>(stored ? ws_all + Ls.off_hdr : ws + L.off_hdr);
   float* lse_all = reinterpret_cast<float*>(ws + L.off_lse);
   const int N = static_cast<int>(p.n_rows), H = static_cast<int>(p.hidden), V = static_cast<int>(p.vocab);
   FLCE_LAUNCH(K_PROLOGUE, launch_prologue(labels, p.n_rows, vocab_total, p.ignore_index, hdr, stream));
@@ -1059,6 +1089,82 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
   if (!encode_bf16(&map_w, W, H, V, n.ld_w, kBN)) return FLCE_ERR_UNSUPPORTED;
   if (pair && !encode_bf16(&map_w_pair, W, H, V, n.ld_w, kBN / 2)) return FLCE_ERR_UNSUPPORTED;
   const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
+  if (stored) {
+    // dlogits from the stored logits (labels relative to the shard), then
+    // grad_h_partial += m dz W_k and grad_W_k += m dz^T h, as the fused path
+    uint16_t* z16 = reinterpret_cast<uint16_t*>(ws_all + Ls.off_z);
+    float* gmax = reinterpret_cast<float*>(ws_all + Ls.off_gmax);
+    uint16_t* dz = reinterpret_cast<uint16_t*>(ws_all + Ls.off_dz);
+    auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, sms); };
+    DlogitParams dp{};
+    dp.rows = N;
+    dp.vocab = V;
+    dp.s16 = z16;
+    dp.lds = Ls.ldz;
+    dp.gmax = gmax;
+    dp.ldg = Ls.ldg;
+    dp.lse = lse_all;
+    dp.labels = labels;
+    dp.label_offset = vocab_offset;
+    dp.ignore_index = p.ignore_index;
+    dp.softcap = p.softcap;
+    dp.inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    dp.grad_scale = p.grad_scale;
+    dp.reduction = p.reduction;
+    dp.hdr = hdr;
+    dp.dz = dz;
+    dp.ldd = Ls.ldd;
+    FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
+    if (gh_acc) {
+      CUtensorMap map_a, map_b, map_o;
+      if (!encode_bf16(&map_a, dz, V, N, Ls.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;   // dz K-major
+      if (!encode_bf16(&map_b, W, H, V, n.ld_w, 64)) return FLCE_ERR_UNSUPPORTED;     // W MN-major
+      if (!encode_f32_out(&map_o, gh_acc, H, N, H)) return FLCE_ERR_UNSUPPORTED;
+      GemmParams b{};
+      std::memset(&b, 0, sizeof(b));
+      b.M = N;
+      b.N = H;
+      b.K = V;
+      b.m_tiles = (N + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (V + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = N;
+      b.N_valid = H;
+      b.out = gh_acc;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
+                                               std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+    }
+    if (grad_W) {
+      CUtensorMap map_a, map_b, map_o;
+      if (!encode_bf16(&map_a, dz, V, N, Ls.ldd, 64)) return FLCE_ERR_UNSUPPORTED;    // dz MN-major
+      if (!encode_bf16(&map_b, h, H, N, n.ld_h, 64)) return FLCE_ERR_UNSUPPORTED;     // h MN-major
+      if (!encode_f32_out(&map_o, grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
+      GemmParams b{};
+      std::memset(&b, 0, sizeof(b));
+      b.M = V;
+      b.N = H;
+      b.K = N;
+      b.m_tiles = (V + kBM - 1) / kBM;
+      b.n_tiles = (H + kBN - 1) / kBN;
+      b.k_iters = (N + kBK - 1) / kBK;
+      b.group_m = std::min(b.m_tiles, 16);
+      b.alpha = p.out_mult;
+      b.M_valid = V;
+      b.N_valid = H;
+      b.out = grad_W;
+      b.ldo = H;
+      b.status = &hdr->status;
+      b.timeout_ns = timeout;
+      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
+                                               std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+    }
+    return FLCE_OK;
+  }
   for (int64_t r0 = 0; r0 < p.n_rows; r0 += L.C) {
     SlabArgs sa;
     sa.rows = static_cast<int>(std::min<int64_t>(L.C, p.n_rows - r0));
@@ -1496,6 +1602,14 @@ int flce_ce_only_from_host(const flce_params* p, const void* h_host, const void*
 size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_h, int need_grad_W) {
   Norm n;
   if (normalise(p, &n) != FLCE_OK) return 0;
+  if (n.p.flags & FLCE_FLAG_VP_STORED) {  // one size for both calls: the stored logits, then the backward's part
+    if (check_vp_stored(n.p) != FLCE_OK) return 0;
+    Layout Ls;
+    make_vp_stored_layout(n, &Ls);
+    VpLayout L;
+    make_vp_layout(n, false, &L);
+    return Ls.total + L.total;
+  }
   if (!backward) {
     Layout L;
     make_layout(n, FLCE_MODE_CE_ONLY, false, false, &L);
@@ -1513,12 +1627,15 @@ int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_to
   const int rc = check_shards(vocab_offset, p->vocab, vocab_total, 0, nullptr);
   if (rc != FLCE_OK) return rc;
   if (p->dtype != FLCE_DTYPE_BF16 || (p->flags & FLCE_FLAG_SIMT_GEMM)) return FLCE_ERR_UNSUPPORTED;
+  const bool stored = (p->flags & FLCE_FLAG_VP_STORED) != 0;
+  if (stored && check_vp_stored(*p) != FLCE_OK) return FLCE_ERR_ARG;
   Call c{FLCE_MODE_CE_ONLY, h, W_shard, labels, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
          workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.vocab_offset = vocab_offset;
   c.vocab_total = vocab_total;
   c.shard_partials = partials;  // NULL only with no rows, which write none
   c.shard_call = true;
+  c.vp_stored = stored;
   return run(p, c);
 }
 

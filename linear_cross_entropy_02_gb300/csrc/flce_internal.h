@@ -215,6 +215,7 @@ struct DlogitParams {
   int64_t ldg;
   const float* lse; // [rows]
   const int64_t* labels;
+  int64_t label_offset;  // vocab id of column 0 (a vocab shard's offset; 0 otherwise)
   int64_t ignore_index;
   float softcap, inv_softcap;
   float grad_scale;

@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(256) dlogits_rows_kernel(const DlogitParams p)
   for (int i = 0; i < 4; ++i) {
     const int c = c_base + i * 2048;
     if (c >= p.vocab) break;
-    const int64_t dl = y - c;
+    const int64_t dl = y - p.label_offset - c;
     const int label_local = (dl >= 0 && dl < 8) ? static_cast<int>(dl) : -1;
     if (p.softcap > 0.f)
       dlogits_piece<true, HALF>(p, srow, s16row, grow, drow, c, ci, lse_l2e, label_local);

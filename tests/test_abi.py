@@ -306,3 +306,30 @@ def test_vocab_parallel_host_errors(L):
     assert bwd_rc([0, 300, 600], ws=bwd - 256) == B.FLCE_ERR_WORKSPACE
     assert bwd_rc([0, 300, 600], params=pf) == B.FLCE_ERR_UNSUPPORTED
     assert bwd_rc(list(range(0, 600, 9)) + [600]) == B.FLCE_ERR_ARG          # 67 shards: more than 64
+
+
+def test_vocab_parallel_stored_host_errors(L):
+    """FLCE_FLAG_VP_STORED: one workspace size for both calls, larger than
+    either call's without it (it holds the logits and their dlogits); the flag
+    is refused with the recompute or K-major backward and above 32768 rows,
+    and a short workspace is refused, all before any device call."""
+    from linear_cross_entropy_02_gb300 import _lib as B
+    fake = ctypes.c_void_p(1 << 20)
+    p = _params(L, n_rows=64, hidden=32, vocab=300)
+    ps = _params(L, n_rows=64, hidden=32, vocab=300, flags=B.FLCE_FLAG_VP_STORED)
+    fwd_s = L.flce_vp_workspace_size(ctypes.byref(ps), 0, 0, 0)
+    bwd_s = L.flce_vp_workspace_size(ctypes.byref(ps), 1, 1, 1)
+    assert fwd_s == bwd_s > L.flce_vp_workspace_size(ctypes.byref(p), 1, 1, 1)
+    assert fwd_s > L.flce_vp_workspace_size(ctypes.byref(p), 0, 0, 0) + 64 * 300 * 4   # fp16 logits + bf16 dz
+    for extra in (B.FLCE_FLAG_RECOMPUTE, B.FLCE_FLAG_KMAJOR_BWD):
+        pb = _params(L, n_rows=64, hidden=32, vocab=300, flags=B.FLCE_FLAG_VP_STORED | extra)
+        assert L.flce_vp_workspace_size(ctypes.byref(pb), 0, 0, 0) == 0
+        assert L.flce_vp_forward(ctypes.byref(pb), 0, 600, fake, fake, fake, fake, fake, 1 << 40, None) == \
+            B.FLCE_ERR_ARG
+    pn = _params(L, n_rows=32769, hidden=32, vocab=300, flags=B.FLCE_FLAG_VP_STORED)
+    assert L.flce_vp_workspace_size(ctypes.byref(pn), 0, 0, 0) == 0
+    assert L.flce_vp_forward(ctypes.byref(pn), 0, 600, fake, fake, fake, fake, fake, 1 << 40, None) == B.FLCE_ERR_ARG
+    arr = (ctypes.c_int64 * 3)(0, 300, 600)
+    rc = L.flce_vp_backward(ctypes.byref(ps), 0, 600, 2, arr, fake, fake, fake, fake, fake, None, None, None, fake,
+                            fake, fake, bwd_s - 256, None)
+    assert rc == B.FLCE_ERR_WORKSPACE

@@ -31,15 +31,21 @@ def _inputs(N, H, V, seed, ign=0.1, std=0.05):
             workloads.make_labels(N, V, seed, ign))
 
 
-def _run_shards(flce, h, W, y, offsets, grad_h=True, grad_W=True, **kw):
+def _run_shards(flce, h, W, y, offsets, grad_h=True, grad_W=True, stored=False, **kw):
     """Every shard's forward, the gather (stacking in shard order), every
     shard's backward; returns the partials, the first shard's outputs, the
-    summed grad_h (bf16, rounded by the library) and the full grad_W."""
+    summed grad_h (bf16, rounded by the library) and the full grad_W. With
+    stored, each shard keeps its logits between its two calls
+    (FLCE_FLAG_VP_STORED) in a workspace of its own."""
     V = offsets[-1]
     hd, yd = h.to(DEV), y.to(DEV)
+    if stored:
+        kw = dict(kw, flags=kw.get("flags", 0) | flce.FLCE_FLAG_VP_STORED)
     fwd_kw = {k: v for k, v in kw.items() if k in ("softcap", "out_mult", "chunk_rows", "flags")}
     shards = [W[offsets[k]:offsets[k + 1]].to(DEV) for k in range(len(offsets) - 1)]
-    parts = [flce.flce_vp_forward(hd, Wk, yd, offsets[k], V, **fwd_kw) for k, Wk in enumerate(shards)]
+    wss = [flce.flce_vp_workspace(hd, Wk, keep_logits=True) if stored else None for Wk in shards]
+    parts = [flce.flce_vp_forward(hd, Wk, yd, offsets[k], V, workspace=wss[k], **fwd_kw)
+             for k, Wk in enumerate(shards)]
     allp = torch.stack(parts)
     gh32 = torch.zeros((h.shape[0], h.shape[1]), dtype=torch.float32, device=DEV) if grad_h else None
     gW = torch.zeros((V, h.shape[1]), dtype=torch.float32, device=DEV) if grad_W else None
@@ -47,9 +53,11 @@ def _run_shards(flce, h, W, y, offsets, grad_h=True, grad_W=True, **kw):
     for k, Wk in enumerate(shards):
         outs.append(flce.flce_vp_backward(hd, Wk, yd, allp, offsets, offsets[k], V, grad_h_partial=gh32,
                                           grad_W=None if gW is None else gW[offsets[k]:offsets[k + 1]],
-                                          return_lse=True, **kw))
+                                          return_lse=True, workspace=wss[k], **kw))
     torch.cuda.synchronize()
     assert flce.flce_get_status() == 0
+    for ws in wss:
+        assert ws is None or flce.flce_get_status(workspace=ws) == 0
     gh = flce.flce_scale_gradient(gh32, None, out_dtype=torch.bfloat16) if grad_h else None
     return allp, outs, gh, gW
 
@@ -62,13 +70,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "stored"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"S{len(c['offsets']) - 1}-N{c['N']}-V{c['V']}")
-def test_shards_match_oracle_and_unsharded(flce, case):
+def test_shards_match_oracle_and_unsharded(flce, case, stored):
     N, H, V, offsets = case["N"], case["H"], case["V"], case["offsets"]
     kw = {k: case[k] for k in ("softcap", "out_mult", "chunk_rows") if k in case}
     okw = {k: case[k] for k in ("softcap", "out_mult") if k in case}
     h, W, y = _inputs(N, H, V, case["seed"])
-    allp, outs, gh, gW = _run_shards(flce, h, W, y, offsets, **kw)
+    allp, outs, gh, gW = _run_shards(flce, h, W, y, offsets, stored=stored, **kw)
 
     # each shard's partials against the oracle's
     ref_p = oracle_shard_partials(h, W, y, offsets, **okw)
@@ -108,7 +117,8 @@ def test_shards_match_oracle_and_unsharded(flce, case):
     assert np.abs(gw - ref["grad_W"]).max() <= 1e-2 * np.abs(ref["grad_W"]).max()
 
 
-def test_two_shards_of_the_dsv3_head(flce):
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "stored"])
+def test_two_shards_of_the_dsv3_head(flce, stored):
     """The DeepSeek-V3-shaped head (H = 7168, V = 129280) on 4096 rows in two
     vocab shards: merged loss and predictions against the unsharded low-memory
     call, grad_h and grad_W against it at bf16 rounding, and sampled rows against
@@ -117,7 +127,7 @@ def test_two_shards_of_the_dsv3_head(flce):
     N = 4096
     h, W, y = workloads.make_inputs(w, n_rows=N)
     offsets = [0, 64640, w.vocab]
-    allp, outs, gh, gW = _run_shards(flce, h, W, y, offsets)
+    allp, outs, gh, gW = _run_shards(flce, h, W, y, offsets, stored=stored)
     gW1 = torch.zeros(W.shape, dtype=torch.float32, device=DEV)
     o = flce.flce_forward_backward(h.to(DEV), W.to(DEV), y.to(DEV), grad_W=gW1, return_predicted=True,
                                    low_memory=True)
@@ -137,17 +147,18 @@ def test_two_shards_of_the_dsv3_head(flce):
     flce.flce_release_workspaces()
 
 
-def test_forward_only_and_frozen_shards(flce):
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "stored"])
+def test_forward_only_and_frozen_shards(flce, stored):
     """A backward with neither gradient (loss and predictions only) and one
     with grad_W alone (grad_h not wanted)."""
     N, H, V = 500, 64, 2500
     h, W, y = _inputs(N, H, V, 55)
     offsets = [0, 1200, 2500]
-    _, outs, gh, gW = _run_shards(flce, h, W, y, offsets, grad_h=False, grad_W=False)
+    _, outs, gh, gW = _run_shards(flce, h, W, y, offsets, grad_h=False, grad_W=False, stored=stored)
     assert gh is None and gW is None
     ref = flce_oracle(h, W, y, need_grad_h=False, need_grad_W=False)
     assert abs(float(outs[0]["loss"]) - ref["loss"]) <= 2e-3 * abs(ref["loss"])
-    _, outs2, gh2, gW2 = _run_shards(flce, h, W, y, offsets, grad_h=False, grad_W=True)
+    _, outs2, gh2, gW2 = _run_shards(flce, h, W, y, offsets, grad_h=False, grad_W=True, stored=stored)
     assert float(outs2[0]["loss"]) == float(outs[0]["loss"])
     ref = flce_oracle(h, W, y, need_grad_h=False, need_grad_W=True)
     gw = gW2.double().cpu().numpy()
@@ -219,3 +230,33 @@ def test_empty_and_all_ignored_batches(flce):
         _, outs, gh, gW = _run_shards(flce, h, W, y, offsets)
         assert float(outs[0]["loss"]) == 0.0 and float(outs[0]["token_accuracy"]) == 0.0
         assert torch.count_nonzero(gh).item() == 0 and torch.count_nonzero(gW).item() == 0
+
+
+def test_stored_and_recomputed_shards_agree(flce):
+    """The two backward forms of the same shards: the forward outputs (the
+    partials, then the merged loss, accuracy, predictions and lse) are the
+    same bits, since the forward GEMM's statistics do not depend on whether
+    the logits are also stored; the gradients agree to the bf16 rounding of
+    dz, taken from fp16 stored logits in one form and fp32 recomputed ones in
+    the other."""
+    N, H, V = 900, 192, 6000
+    h, W, y = _inputs(N, H, V, 57)
+    offsets = [0, 2048, 4000, 6000]
+    kw = dict(softcap=30.0, out_mult=0.5)
+    p1, o1, gh1, gW1 = _run_shards(flce, h, W, y, offsets, **kw)
+    p2, o2, gh2, gW2 = _run_shards(flce, h, W, y, offsets, stored=True, **kw)
+    assert torch.equal(p1, p2)
+    for a, b in zip(o1, o2):
+        assert float(a["loss"]) == float(b["loss"]) and float(a["token_accuracy"]) == float(b["token_accuracy"])
+        assert torch.equal(a["predicted"], b["predicted"]) and torch.equal(a["lse"], b["lse"])
+    assert (gh1.float() - gh2.float()).abs().max().item() <= 2.0 ** -6 * gh1.float().abs().max().item()
+    assert (gW1 - gW2).abs().max().item() <= 1e-2 * gW1.abs().max().item()
+
+
+def test_stored_shard_needs_its_workspace(flce):
+    """FLCE_FLAG_VP_STORED without an explicit workspace is refused on the
+    host: the cached one could be reused between the two calls."""
+    N, H, V = 64, 32, 600
+    h, W, y = _inputs(N, H, V, 58)
+    with pytest.raises(ValueError):
+        flce.flce_vp_forward(h.to(DEV), W[:300].to(DEV), y.to(DEV), 0, V, flags=flce.FLCE_FLAG_VP_STORED)
