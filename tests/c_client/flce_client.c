@@ -17,6 +17,9 @@
  *       partials buffer, then every shard's flce_vp_backward, adding into one
  *       fp32 grad_h and into its own rows of grad_W. OUT as for gpu, except
  *       that grad_h is fp32 (float grad_h[N*H]).
+ *   flce_client vps IN OUT S
+ *       as vp, with FLCE_FLAG_VP_STORED: every shard keeps its logits between
+ *       its two calls, in a workspace of its own.
  *
  * IN (little endian): int64 N, H, V, chunk_rows; float softcap, out_mult;
  *   uint16 h[N*H] (bf16 bits), uint16 W[V*H], int64 labels[N], float gW0[V*H].
@@ -157,7 +160,7 @@ static int gpu_mode(const char* in_path, const char* out_path) {
   }
 }
 
-static int vp_mode(const char* in_path, const char* out_path, int S) {
+static int vp_mode(const char* in_path, const char* out_path, int S, int stored) {
   int64_t hdr[4];
   float fl[2];
   FILE* f = fopen(in_path, "rb");
@@ -174,6 +177,8 @@ static int vp_mode(const char* in_path, const char* out_path, int S) {
     float* gh_h = malloc(nh * 4);
     int64_t offsets[65];
     void *h_d, *w_d, *y_d, *gw_d, *pred_d, *gh_d, *ws_d, *sc_d, *part_d;
+    void* ws_k[64];        /* the workspace of each shard's calls */
+    size_t wsb_k[64];
     float sc[2];
     int32_t status = -1;
     int rc = FLCE_OK;
@@ -193,14 +198,15 @@ static int vp_mode(const char* in_path, const char* out_path, int S) {
     p.chunk_rows = hdr[3];
     p.softcap = fl[0];
     p.out_mult = fl[1];
-    for (k = 0; k < S; ++k) { /* one workspace, as large as any shard's call needs */
+    if (stored) p.flags |= FLCE_FLAG_VP_STORED;
+    for (k = 0; k < S; ++k) { /* one workspace as large as any shard's call needs, or one per shard */
       size_t a, b;
       p.vocab = offsets[k + 1] - offsets[k];
       a = flce_vp_workspace_size(&p, 0, 0, 0);
       b = flce_vp_workspace_size(&p, 1, 1, 1);
       if (a == 0 || b == 0) return 5;
-      if (a > ws_bytes) ws_bytes = a;
-      if (b > ws_bytes) ws_bytes = b;
+      wsb_k[k] = a > b ? a : b;
+      if (wsb_k[k] > ws_bytes) ws_bytes = wsb_k[k];
     }
 
     CK(cudaMalloc(&h_d, nh * 2));
@@ -210,6 +216,14 @@ static int vp_mode(const char* in_path, const char* out_path, int S) {
     CK(cudaMalloc(&pred_d, (size_t)n * 8));
     CK(cudaMalloc(&gh_d, nh * 4));
     CK(cudaMalloc(&ws_d, ws_bytes));
+    for (k = 0; k < S; ++k) {
+      if (stored) {
+        CK(cudaMalloc(&ws_k[k], wsb_k[k]));
+      } else {
+        ws_k[k] = ws_d;
+        wsb_k[k] = ws_bytes;
+      }
+    }
     CK(cudaMalloc(&sc_d, 2 * sizeof(float)));
     CK(cudaMalloc(&part_d, (size_t)S * 4 * (size_t)n * sizeof(float)));
     CK(cudaMemcpy(h_d, h_h, nh * 2, cudaMemcpyHostToDevice));
@@ -221,16 +235,20 @@ static int vp_mode(const char* in_path, const char* out_path, int S) {
     for (k = 0; k < S && rc == FLCE_OK; ++k) {
       p.vocab = offsets[k + 1] - offsets[k];
       rc = flce_vp_forward(&p, offsets[k], v, h_d, (const uint16_t*)w_d + offsets[k] * h, (const int64_t*)y_d,
-                           (float*)part_d + (size_t)k * 4 * (size_t)n, ws_d, ws_bytes, NULL);
+                           (float*)part_d + (size_t)k * 4 * (size_t)n, ws_k[k], wsb_k[k], NULL);
     }
     for (k = 0; k < S && rc == FLCE_OK; ++k) {
       p.vocab = offsets[k + 1] - offsets[k];
       rc = flce_vp_backward(&p, offsets[k], v, S, offsets, (const float*)part_d, h_d,
                             (const uint16_t*)w_d + offsets[k] * h, (const int64_t*)y_d, (float*)sc_d,
                             (float*)sc_d + 1, (int64_t*)pred_d, NULL, (float*)gh_d, (float*)gw_d + offsets[k] * h,
-                            ws_d, ws_bytes, NULL);
+                            ws_k[k], wsb_k[k], NULL);
     }
-    if (rc == FLCE_OK) rc = flce_get_status(ws_d, NULL, &status);
+    for (k = 0; k < S && rc == FLCE_OK; ++k) { /* every shard's status word (one shared word without stored) */
+      int32_t st = 0;
+      rc = flce_get_status(ws_k[k], NULL, &st);
+      status = (k == 0 ? 0 : status) | st;
+    }
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(sc, sc_d, sizeof sc, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(pred_h, pred_d, (size_t)n * 8, cudaMemcpyDeviceToHost));
@@ -253,6 +271,8 @@ static int vp_mode(const char* in_path, const char* out_path, int S) {
     cudaFree(pred_d);
     cudaFree(gh_d);
     cudaFree(ws_d);
+    if (stored)
+      for (k = 0; k < S; ++k) cudaFree(ws_k[k]);
     cudaFree(sc_d);
     cudaFree(part_d);
     free(h_h);
@@ -270,7 +290,8 @@ int main(int argc, char** argv) {
   if (argc == 5 && strcmp(argv[1], "host") == 0)
     return host_mode(strtoll(argv[2], NULL, 10), strtoll(argv[3], NULL, 10), strtoll(argv[4], NULL, 10));
   if (argc == 4 && strcmp(argv[1], "gpu") == 0) return gpu_mode(argv[2], argv[3]);
-  if (argc == 5 && strcmp(argv[1], "vp") == 0) return vp_mode(argv[2], argv[3], atoi(argv[4]));
-  fprintf(stderr, "usage: flce_client host N H V | flce_client gpu IN OUT | flce_client vp IN OUT S\n");
+  if (argc == 5 && strcmp(argv[1], "vp") == 0) return vp_mode(argv[2], argv[3], atoi(argv[4]), 0);
+  if (argc == 5 && strcmp(argv[1], "vps") == 0) return vp_mode(argv[2], argv[3], atoi(argv[4]), 1);
+  fprintf(stderr, "usage: flce_client host N H V | flce_client gpu IN OUT | flce_client vp|vps IN OUT S\n");
   return 64;
 }

@@ -109,11 +109,14 @@ def test_forward_backward_from_c(client, tmp_path):
 
 
 @pytest.mark.gpu
-def test_vocab_parallel_from_c(client, tmp_path):
+@pytest.mark.parametrize("mode", ["vp", "vps"])
+def test_vocab_parallel_from_c(client, tmp_path, mode):
     """The vocabulary-parallel entry points driven from C alone: three shards
-    run in turn on buffers the C program allocates. Predictions and accuracy
-    equal the unsharded call's, the loss agrees to the fp32 merge order, and
-    grad_h (summed in fp32 over the shards) and grad_W match the oracle."""
+    run in turn on buffers the C program allocates (vps: each shard keeps its
+    logits between its calls, FLCE_FLAG_VP_STORED, in a workspace of its own).
+    Predictions and accuracy equal the unsharded call's, the loss agrees to
+    the fp32 merge order, and grad_h (summed in fp32 over the shards) and
+    grad_W match the oracle."""
     import linear_cross_entropy_02_gb300 as flce
     N, H, V, C, T, m, S = 300, 136, 777, 128, 30.0, 0.5, 3
     h = workloads.make_hidden(N, H, 82)
@@ -128,7 +131,7 @@ def test_vocab_parallel_from_c(client, tmp_path):
         f.write(W.view(torch.int16).numpy().astype("<i2").tobytes())
         f.write(y.numpy().astype("<i8").tobytes())
         f.write(G0.astype("<f4").tobytes())
-    r = subprocess.run([client, "vp", str(inp), str(out), str(S)], capture_output=True, text=True, timeout=300)
+    r = subprocess.run([client, mode, str(inp), str(out), str(S)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     raw = open(out, "rb").read()
     o = 0
