@@ -135,9 +135,10 @@ extern "C" {
                                         fused backward stores them) and the backward forms
                                         dlogits from them instead of recomputing the logits:
                                         6 N H V_k tensor flops per shard instead of 8, and
-                                        O(N * V_k) workspace. N <= 32768 per call pair; the two
-                                        calls take the same params and the same workspace, which
-                                        nothing else may use in between */
+                                        O(N * V_k) workspace (the logits of all N rows; dlogits
+                                        one chunk at a time). The two calls take the same params
+                                        and the same workspace, which nothing else may use in
+                                        between */
 
 typedef struct flce_params {
   int64_t n_rows;        /* N >= 0 */
@@ -302,8 +303,7 @@ int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_
  * FLCE_FLAG_RECOMPUTE does, so only the partials cross shards and no logits
  * are kept between the calls: 8 N H V_k tensor flops per shard, transient
  * memory O(C * vocab_slab + N). With FLCE_FLAG_VP_STORED the forward keeps
- * them in the workspace instead (6 N H V_k flops, O(N * V_k) memory; a caller
- * with more rows makes one call pair per block of rows). bf16 operands only (FLCE_ERR_UNSUPPORTED for
+ * them in the workspace instead (6 N H V_k flops, O(N * V_k) memory). bf16 operands only (FLCE_ERR_UNSUPPORTED for
  * fp32, FLCE_FLAG_SIMT_GEMM and FLCE_FLAG_KMAJOR_BWD).
  * In both calls p->vocab is V_k, the shard's row count, and W_shard is
  * [V_k, ld_w]; labels are checked against [0, vocab_total) (FLCE_ERR_LABEL).
@@ -316,13 +316,13 @@ int flce_scale_gradient(const void* x, int x_dtype, void* y, int y_dtype, int64_
  * (backward = 1; need_grad_h / need_grad_W as that call will have them). The
  * backward's includes 4 bytes of lse per row (all N rows). With
  * FLCE_FLAG_VP_STORED both calls need the same size, which holds the kept
- * logits (about N * V_k * 4.1 bytes with their dlogits). 0 if invalid. */
+ * logits (about N * V_k * 2.1 bytes, and C * V_k * 2 for one chunk's
+ * dlogits). 0 if invalid. */
 size_t flce_vp_workspace_size(const flce_params* p, int backward, int need_grad_h, int need_grad_W);
 
 /* Forward of one shard: writes partials [4][N] (device). FLCE_ERR_ARG when
- * [vocab_offset, vocab_offset + V_k) is not inside [0, vocab_total), and with
- * FLCE_FLAG_VP_STORED when N > 32768 or with FLCE_FLAG_RECOMPUTE or
- * FLCE_FLAG_KMAJOR_BWD. */
+ * [vocab_offset, vocab_offset + V_k) is not inside [0, vocab_total), and for
+ * FLCE_FLAG_VP_STORED with FLCE_FLAG_RECOMPUTE or FLCE_FLAG_KMAJOR_BWD. */
 int flce_vp_forward(const flce_params* p, int64_t vocab_offset, int64_t vocab_total, const void* h,
                     const void* W_shard, const int64_t* labels, float* partials, void* workspace,
                     size_t workspace_bytes, void* stream);

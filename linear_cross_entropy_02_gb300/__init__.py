@@ -449,8 +449,7 @@ def vocab_parallel_linear_cross_entropy(h, W_shard, labels, vocab_offset: int, *
     rank gets the same loss, token accuracy and predictions; grad_W (this
     rank's fp32 [V_k, H], optional) is accumulated in place. keep_logits keeps
     each shard's logits between its forward and backward
-    (FLCE_FLAG_VP_STORED: 6 N H V_k flops instead of 8, O(N V_k) memory; at
-    most 32768 rows)."""
+    (FLCE_FLAG_VP_STORED: 6 N H V_k flops instead of 8, O(N V_k) memory)."""
     offsets, order = vp_shard_table(vocab_offset, W_shard.shape[0], group)
     V = offsets[-1]
     flags = FLCE_FLAG_VP_STORED if keep_logits else 0

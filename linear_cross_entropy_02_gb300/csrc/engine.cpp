@@ -287,7 +287,9 @@ int64_t default_chunk_rows(int64_t N, int64_t H, int64_t V, bool gh, bool gw, in
   return best;
 }
 
-void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
+// z_rows: rows of the stored-logit region (0: one chunk, C; the kept logits of
+// FLCE_FLAG_VP_STORED hold all N rows).
+void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L, int64_t z_rows = 0) {
   const flce_params& p = n.p;
   L->host_in = mode == FLCE_MODE_FORWARD_BACKWARD_HOST || mode == FLCE_MODE_CE_ONLY_HOST;
   if (mode == FLCE_MODE_FORWARD_BACKWARD_HOST) mode = FLCE_MODE_FORWARD_BACKWARD;
@@ -349,8 +351,9 @@ void make_layout(const Norm& n, int mode, bool gh, bool gw, Layout* L) {
   L->off_pidx = take(sizeof(int32_t) * L->n_vtiles * L->ldp);
   L->off_tgt = take(sizeof(float) * L->C);
   L->off_lse = take(sizeof(float) * L->C);
-  L->off_z = L->need_z ? take((L->z16 ? 2 : sizeof(float)) * L->C * L->ldz) : 0;
-  L->off_gmax = L->z16 ? take(sizeof(float) * L->C * L->ldg) : 0;
+  const int64_t zr = z_rows > 0 ? z_rows : L->C;
+  L->off_z = L->need_z ? take((L->z16 ? 2 : sizeof(float)) * zr * L->ldz) : 0;
+  L->off_gmax = L->z16 ? take(sizeof(float) * zr * L->ldg) : 0;
   L->off_dz = L->need_dz ? take(es * L->C * (recompute ? L->slab : L->ldd)) : 0;
   L->off_dzt = L->need_dzt ? take(es * round_up(p.vocab, kBM) * L->ldt) : 0;
   L->off_wt = L->need_wt ? take(es * p.hidden * L->ldwt) : 0;
@@ -617,18 +620,15 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
 }
 
 // The workspace layout that FLCE_FLAG_VP_STORED shares between a shard's
-// forward and backward: the fused forward + backward layout with one chunk of
-// all N rows, so the fp16 logits, their group maxima and the dlogits buffer
-// sit at the same offsets in both calls.
+// forward and backward: the fused forward + backward layout (chunks of C
+// rows) with the fp16 logits and their group maxima kept for all N rows, so
+// they and the chunk's dlogits buffer sit at the same offsets in both calls.
 void make_vp_stored_layout(const Norm& n, Layout* L) {
-  Norm ns = n;
-  ns.p.chunk_rows = std::max<int64_t>(ns.p.n_rows, 1);
-  make_layout(ns, FLCE_MODE_FORWARD_BACKWARD, true, true, L);
+  make_layout(n, FLCE_MODE_FORWARD_BACKWARD, true, true, L, std::max<int64_t>(n.p.n_rows, 1));
 }
 
 int check_vp_stored(const flce_params& p) {
   if (p.flags & (FLCE_FLAG_RECOMPUTE | FLCE_FLAG_KMAJOR_BWD | FLCE_FLAG_SIMT_GEMM)) return FLCE_ERR_ARG;
-  if (p.n_rows > 32768) return FLCE_ERR_ARG;
   return FLCE_OK;
 }
 
@@ -651,7 +651,7 @@ int run(const flce_params* params, const Call& c) {
   make_layout(n, !c.host_in ? c.mode
                              : c.mode == FLCE_MODE_CE_ONLY ? FLCE_MODE_CE_ONLY_HOST : FLCE_MODE_FORWARD_BACKWARD_HOST,
               gh, gw, &L);
-  if (c.vp_stored) make_vp_stored_layout(n, &L);  // one chunk; the logits are stored for the backward
+  if (c.vp_stored) make_vp_stored_layout(n, &L);  // the logits of all rows are kept for the backward
   if (c.ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   int sms = 0, cc = 0;
   rc = device_info(&sms, &cc);
@@ -767,9 +767,12 @@ int run(const flce_params* params, const Call& c) {
     g.part_idx = pidx;
     g.tgt = tgt;
     g.ldp = static_cast<int>(L.ldp);
+    // kept logits (FLCE_FLAG_VP_STORED): this chunk's rows of the all-row store
+    uint16_t* z16_c = z16 && c.vp_stored ? z16 + r0 * L.ldz : z16;
+    float* gmax_c = gmax && c.vp_stored ? gmax + r0 * L.ldg : gmax;
     g.zbuf = L.z16 ? nullptr : zbuf;
     g.ldz = L.ldz;
-    g.gmax = gmax;
+    g.gmax = gmax_c;
     g.ldg = L.ldg;
     g.status = &hdr->status;
     g.timeout_ns = timeout;
@@ -786,7 +789,7 @@ int run(const flce_params* params, const Call& c) {
     } else {
       const int tiles = g.m_tiles * g.n_tiles;
       CUtensorMap map_z;
-      if (store && L.z16 && !encode_f16_out(&map_z, z16, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
+      if (store && L.z16 && !encode_f16_out(&map_z, z16_c, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
       if (store && !L.z16 && !encode_f32_out(&map_z, zbuf, L.ldz, rows, L.ldz)) return FLCE_ERR_UNSUPPORTED;
       const int mode = !store ? EPI_STATS : L.z16 ? EPI_STATS_STORE16 : EPI_STATS_STORE;
       const bool wg = wide_for(g);
@@ -1090,78 +1093,84 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
   if (pair && !encode_bf16(&map_w_pair, W, H, V, n.ld_w, kBN / 2)) return FLCE_ERR_UNSUPPORTED;
   const uint64_t timeout = p.timeout_ns > 0 ? static_cast<uint64_t>(p.timeout_ns) : kDefaultTimeoutNs;
   if (stored) {
-    // dlogits from the stored logits (labels relative to the shard), then
-    // grad_h_partial += m dz W_k and grad_W_k += m dz^T h, as the fused path
+    // per chunk of C rows: dlogits from the kept logits (labels relative to
+    // the shard), then grad_h_partial += m dz W_k and grad_W_k += m dz^T h_c,
+    // as the fused path does
     uint16_t* z16 = reinterpret_cast<uint16_t*>(ws_all + Ls.off_z);
     float* gmax = reinterpret_cast<float*>(ws_all + Ls.off_gmax);
     uint16_t* dz = reinterpret_cast<uint16_t*>(ws_all + Ls.off_dz);
     auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, sms); };
-    DlogitParams dp{};
-    dp.rows = N;
-    dp.vocab = V;
-    dp.s16 = z16;
-    dp.lds = Ls.ldz;
-    dp.gmax = gmax;
-    dp.ldg = Ls.ldg;
-    dp.lse = lse_all;
-    dp.labels = labels;
-    dp.label_offset = vocab_offset;
-    dp.ignore_index = p.ignore_index;
-    dp.softcap = p.softcap;
-    dp.inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
-    dp.grad_scale = p.grad_scale;
-    dp.reduction = p.reduction;
-    dp.hdr = hdr;
-    dp.dz = dz;
-    dp.ldd = Ls.ldd;
-    FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
-    if (gh_acc) {
-      CUtensorMap map_a, map_b, map_o;
-      if (!encode_bf16(&map_a, dz, V, N, Ls.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;   // dz K-major
-      if (!encode_bf16(&map_b, W, H, V, n.ld_w, 64)) return FLCE_ERR_UNSUPPORTED;     // W MN-major
-      if (!encode_f32_out(&map_o, gh_acc, H, N, H)) return FLCE_ERR_UNSUPPORTED;
-      GemmParams b{};
-      std::memset(&b, 0, sizeof(b));
-      b.M = N;
-      b.N = H;
-      b.K = V;
-      b.m_tiles = (N + kBM - 1) / kBM;
-      b.n_tiles = (H + kBN - 1) / kBN;
-      b.k_iters = (V + kBK - 1) / kBK;
-      b.group_m = std::min(b.m_tiles, 16);
-      b.alpha = p.out_mult;
-      b.M_valid = N;
-      b.N_valid = H;
-      b.out = gh_acc;
-      b.ldo = H;
-      b.status = &hdr->status;
-      b.timeout_ns = timeout;
-      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
-    }
-    if (grad_W) {
-      CUtensorMap map_a, map_b, map_o;
-      if (!encode_bf16(&map_a, dz, V, N, Ls.ldd, 64)) return FLCE_ERR_UNSUPPORTED;    // dz MN-major
-      if (!encode_bf16(&map_b, h, H, N, n.ld_h, 64)) return FLCE_ERR_UNSUPPORTED;     // h MN-major
-      if (!encode_f32_out(&map_o, grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-      GemmParams b{};
-      std::memset(&b, 0, sizeof(b));
-      b.M = V;
-      b.N = H;
-      b.K = N;
-      b.m_tiles = (V + kBM - 1) / kBM;
-      b.n_tiles = (H + kBN - 1) / kBN;
-      b.k_iters = (N + kBK - 1) / kBK;
-      b.group_m = std::min(b.m_tiles, 16);
-      b.alpha = p.out_mult;
-      b.M_valid = V;
-      b.N_valid = H;
-      b.out = grad_W;
-      b.ldo = H;
-      b.status = &hdr->status;
-      b.timeout_ns = timeout;
-      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+    CUtensorMap map_w_mn;
+    if (gh_acc && !encode_bf16(&map_w_mn, W, H, V, n.ld_w, 64)) return FLCE_ERR_UNSUPPORTED;  // W MN-major
+    for (int64_t r0 = 0; r0 < p.n_rows; r0 += Ls.C) {
+      const int rows = static_cast<int>(std::min<int64_t>(Ls.C, p.n_rows - r0));
+      DlogitParams dp{};
+      dp.rows = rows;
+      dp.vocab = V;
+      dp.s16 = z16 + r0 * Ls.ldz;
+      dp.lds = Ls.ldz;
+      dp.gmax = gmax + r0 * Ls.ldg;
+      dp.ldg = Ls.ldg;
+      dp.lse = lse_all + r0;
+      dp.labels = labels + r0;
+      dp.label_offset = vocab_offset;
+      dp.ignore_index = p.ignore_index;
+      dp.softcap = p.softcap;
+      dp.inv_softcap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+      dp.grad_scale = p.grad_scale;
+      dp.reduction = p.reduction;
+      dp.hdr = hdr;
+      dp.dz = dz;
+      dp.ldd = Ls.ldd;
+      FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
+      if (gh_acc) {
+        CUtensorMap map_a, map_o;
+        if (!encode_bf16(&map_a, dz, V, rows, Ls.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;   // dz K-major
+        if (!encode_f32_out(&map_o, gh_acc + r0 * H, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
+        GemmParams b{};
+        std::memset(&b, 0, sizeof(b));
+        b.M = rows;
+        b.N = H;
+        b.K = V;
+        b.m_tiles = (rows + kBM - 1) / kBM;
+        b.n_tiles = (H + kBN - 1) / kBN;
+        b.k_iters = (V + kBK - 1) / kBK;
+        b.group_m = std::min(b.m_tiles, 16);
+        b.alpha = p.out_mult;
+        b.M_valid = rows;
+        b.N_valid = H;
+        b.out = gh_acc + r0 * H;
+        b.ldo = H;
+        b.status = &hdr->status;
+        b.timeout_ns = timeout;
+        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_w_mn, &map_o,
+                                                 b, std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+      }
+      if (grad_W) {
+        CUtensorMap map_a, map_b, map_o;
+        if (!encode_bf16(&map_a, dz, V, rows, Ls.ldd, 64)) return FLCE_ERR_UNSUPPORTED;    // dz MN-major
+        if (!encode_bf16(&map_b, static_cast<const uint16_t*>(h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
+          return FLCE_ERR_UNSUPPORTED;                                                      // h_c MN-major
+        if (!encode_f32_out(&map_o, grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
+        GemmParams b{};
+        std::memset(&b, 0, sizeof(b));
+        b.M = V;
+        b.N = H;
+        b.K = rows;
+        b.m_tiles = (V + kBM - 1) / kBM;
+        b.n_tiles = (H + kBN - 1) / kBN;
+        b.k_iters = (rows + kBK - 1) / kBK;
+        b.group_m = std::min(b.m_tiles, 16);
+        b.alpha = p.out_mult;
+        b.M_valid = V;
+        b.N_valid = H;
+        b.out = grad_W;
+        b.ldo = H;
+        b.status = &hdr->status;
+        b.timeout_ns = timeout;
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+      }
     }
     return FLCE_OK;
   }
