@@ -106,6 +106,41 @@ def test_pair_ce_only_and_vocab_shards(flce):
     assert np.abs(g - ref["grad_h"]).max() <= 1e-2 * np.abs(ref["grad_h"]).max()
 
 
+def test_pair_vocab_shards_with_kept_logits(flce):
+    """Vocab shards that keep their logits between their calls
+    (FLCE_FLAG_VP_STORED), on CTA pairs and on single CTAs: the same bits
+    (the same products in the same K order), and the oracle's values."""
+    from linear_cross_entropy_02_gb300 import _lib
+    N, H, V = 1500, 256, 9000
+    h, W, y = _inputs(N, H, V, 73)
+    hd, Wd, yd = h.to(DEV), W.to(DEV), y.to(DEV)
+    offsets = [0, 4000, V]
+    res = []
+    for flags in (TILE256 | PAIR | _lib.FLCE_FLAG_VP_STORED, TILE256 | _lib.FLCE_FLAG_VP_STORED):
+        shards = [Wd[offsets[k]:offsets[k + 1]] for k in range(2)]
+        wss = [flce.flce_vp_workspace(hd, shards[k], keep_logits=True, chunk_rows=512) for k in range(2)]
+        parts = [flce.flce_vp_forward(hd, shards[k], yd, offsets[k], V, flags=flags, chunk_rows=512,
+                                      workspace=wss[k]) for k in range(2)]
+        allp = torch.stack(parts)
+        gh = torch.zeros((N, H), dtype=torch.float32, device=DEV)
+        gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
+        for k in range(2):
+            o = flce.flce_vp_backward(hd, shards[k], yd, allp, offsets, offsets[k], V, grad_h_partial=gh,
+                                      grad_W=gW[offsets[k]:offsets[k + 1]], flags=flags, chunk_rows=512,
+                                      workspace=wss[k])
+        torch.cuda.synchronize()
+        assert all(flce.flce_get_status(workspace=ws) == 0 for ws in wss)
+        res.append((allp, o, gh, gW))
+    (p1, o1, gh1, gW1), (p2, o2, gh2, gW2) = res
+    assert torch.equal(p1, p2) and float(o1["loss"]) == float(o2["loss"])
+    assert torch.equal(o1["predicted"], o2["predicted"])
+    assert torch.equal(gh1, gh2) and torch.equal(gW1, gW2)
+    ref = flce_oracle(h, W, y)
+    assert abs(float(o1["loss"]) - ref["loss"]) <= 2e-3 * abs(ref["loss"])
+    assert np.abs(gh1.double().cpu().numpy() - ref["grad_h"]).max() <= 1e-2 * np.abs(ref["grad_h"]).max()
+    assert np.abs(gW1.double().cpu().numpy() - ref["grad_W"]).max() <= 1e-2 * np.abs(ref["grad_W"]).max()
+
+
 def test_pair_bounded_waits_time_out_and_context_survives(flce):
     """The test hook makes both CTAs' loaders issue nothing: the leader's MMA
     waits and both CTAs' epilogue waits give up after the limit, each CTA on
