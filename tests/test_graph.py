@@ -64,29 +64,33 @@ def test_two_streams_use_separate_workspaces(flce):
     assert [float(o) for o in outs] == refs
 
 
-def test_vocab_parallel_step_on_cta_pairs_captured_and_replayed(flce):
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "kept_logits"])
+def test_vocab_parallel_step_on_cta_pairs_captured_and_replayed(flce, stored):
     """Two vocab shards' forwards, the gather (a stack), the two backwards and
     the rounding of grad_h, all on CTA-pair GEMMs, captured once in a CUDA graph
-    and replayed: the same bits as the uncaptured step."""
+    and replayed: the same bits as the uncaptured step. kept_logits: each shard
+    keeps its logits between its calls, in a workspace allocated beforehand."""
     N, H, V = 768, 256, 9000
     offs = [0, 4000, V]
     h = workloads.make_hidden(N, H, 22).to(DEV)
     W = workloads.make_weight(V, H, 22).to(DEV)
     y = workloads.make_labels(N, V, 22, 0.05).to(DEV)
-    flags = flce.FLCE_FLAG_TILE256 | flce.FLCE_FLAG_CTA_PAIR
+    flags = flce.FLCE_FLAG_TILE256 | flce.FLCE_FLAG_CTA_PAIR | (flce.FLCE_FLAG_VP_STORED if stored else 0)
     gh32 = torch.zeros((N, H), dtype=torch.float32, device=DEV)
     gW = torch.zeros((V, H), dtype=torch.float32, device=DEV)
+    wss = [flce.flce_vp_workspace(h, W[offs[k]:offs[k + 1]], keep_logits=True) if stored else None
+           for k in range(2)]
 
     def step():
         parts = [flce.flce_vp_forward(h, W[offs[k]:offs[k + 1]], y, offs[k], V, softcap=30.0, out_mult=0.5,
-                                      flags=flags) for k in range(2)]
+                                      flags=flags, workspace=wss[k]) for k in range(2)]
         allp = torch.stack(parts)
         gh32.zero_()
         out = None
         for k in range(2):
             out = flce.flce_vp_backward(h, W[offs[k]:offs[k + 1]], y, allp, offs, offs[k], V, grad_h_partial=gh32,
                                         grad_W=gW[offs[k]:offs[k + 1]], softcap=30.0, out_mult=0.5, flags=flags,
-                                        vocab_slab=2048)
+                                        vocab_slab=2048, workspace=wss[k])
         return out, flce.flce_scale_gradient(gh32, None, out_dtype=torch.bfloat16)
 
     s = torch.cuda.Stream(DEV)
