@@ -500,6 +500,80 @@ struct HostStaging {
 // z is recomputed on the tensor cores and the EPI_DZ epilogue forms bf16
 // dlogits from it with the rows' lse; then grad_h += m dz W_slab (fp32
 // reduce-add into gh_acc) and grad_W_slab += m dz^T h_c.
+// What the backward GEMMs that accumulate in fp32 share: the scale, the
+// status word, the wait limit, the tile choice and the stream.
+struct AccCtx {
+  float alpha;
+  Header* hdr;
+  uint64_t timeout;
+  int flags, sms;
+  bool pair;
+  cudaStream_t stream;
+};
+
+// grad_h part += alpha * dz W over K = V columns: dz [rows][ldd] bf16 (K-major
+// A), W [V][ld_w] bf16 read in place (MN-major B); out [rows][H] fp32 gets a
+// TMA bulk reduce-add.
+int grad_h_acc_gemm(const AccCtx& x, const uint16_t* dz, int64_t ldd, int rows, int V, const uint16_t* W,
+                    int64_t ld_w, int H, float* out, int group_m) {
+  CUtensorMap map_a, map_b, map_o;
+  if (!encode_bf16(&map_a, dz, V, rows, ldd, kBM)) return FLCE_ERR_UNSUPPORTED;
+  if (!encode_bf16(&map_b, W, H, V, ld_w, 64)) return FLCE_ERR_UNSUPPORTED;
+  if (!encode_f32_out(&map_o, out, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
+  GemmParams b{};
+  std::memset(&b, 0, sizeof(b));
+  b.M = rows;
+  b.N = H;
+  b.K = V;
+  b.m_tiles = (rows + kBM - 1) / kBM;
+  b.n_tiles = (H + kBN - 1) / kBN;
+  b.k_iters = (V + kBK - 1) / kBK;
+  b.group_m = std::min(b.m_tiles, group_m);
+  b.alpha = x.alpha;
+  b.M_valid = rows;
+  b.N_valid = H;
+  b.out = out;
+  b.ldo = H;
+  b.status = &x.hdr->status;
+  b.timeout_ns = x.timeout;
+  cudaStream_t stream = x.stream;
+  FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, pick_wide(x.flags, b, x.sms), &map_a, &map_b,
+                                           &map_o, b, std::min(b.m_tiles * b.n_tiles, x.sms), stream, x.pair));
+  return FLCE_OK;
+}
+
+// grad_W [V][H] fp32 += alpha * dz^T h_c over K = rows: dz [rows][ldd] and
+// h_c [rows][ld_hc] bf16 read in place (both MN-major).
+int grad_W_acc_gemm(const AccCtx& x, const uint16_t* dz, int64_t ldd, int rows, int V, const uint16_t* h_c,
+                    int64_t ld_hc, int H, float* grad_W) {
+  CUtensorMap map_a, map_b, map_o;
+  if (!encode_bf16(&map_a, dz, V, rows, ldd, 64)) return FLCE_ERR_UNSUPPORTED;
+  if (!encode_bf16(&map_b, h_c, H, rows, ld_hc, 64)) return FLCE_ERR_UNSUPPORTED;
+  if (!encode_f32_out(&map_o, grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
+  GemmParams b{};
+  std::memset(&b, 0, sizeof(b));
+  b.M = V;
+  b.N = H;
+  b.K = rows;
+  b.m_tiles = (V + kBM - 1) / kBM;
+  b.n_tiles = (H + kBN - 1) / kBN;
+  b.k_iters = (rows + kBK - 1) / kBK;
+  // Groups of 16 vocab tiles: on the DSV3 head this beat an N-fastest walk
+  // with h_c kept in L2 and evict-first dz loads.
+  b.group_m = std::min(b.m_tiles, 16);
+  b.alpha = x.alpha;
+  b.M_valid = V;
+  b.N_valid = H;
+  b.out = grad_W;
+  b.ldo = H;
+  b.status = &x.hdr->status;
+  b.timeout_ns = x.timeout;
+  cudaStream_t stream = x.stream;
+  FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, pick_wide(x.flags, b, x.sms), &map_a, &map_b,
+                                           &map_o, b, std::min(b.m_tiles * b.n_tiles, x.sms), stream, x.pair));
+  return FLCE_OK;
+}
+
 struct SlabArgs {
   int rows, H, V, slab;
   int col_base;              // vocab id of W's row 0 (the shard offset)
@@ -562,58 +636,17 @@ int recompute_slabs(const SlabArgs& a, cudaStream_t stream) {
     FLCE_LAUNCH(K_RECOMPUTE_GEMM, launch_gemm_tc(EPI_DZ, false, false, wr, a.map_hc,
                                                  wr && pair ? a.map_w_pair : a.map_w, nullptr, r,
                                                  std::min(r.m_tiles * r.n_tiles, a.sms), stream, pair));
+    const AccCtx x{p.out_mult, hdr, a.timeout, p.flags, a.sms, pair, stream};
+    // grad_h_c += m dz_slab W_slab, then grad_W_slab += m dz_slab^T h_c
     if (a.gh_acc) {
-      // grad_h_c += m dz_slab W_slab   (dz K-major, W rows of the slab MN-major)
-      CUtensorMap map_a, map_b;
-      if (!encode_bf16(&map_a, a.dz, vs, rows, slab, kBM)) return FLCE_ERR_UNSUPPORTED;
-      if (!encode_bf16(&map_b, a.W + static_cast<int64_t>(v0) * a.ld_w, H, vs, a.ld_w, 64))
-        return FLCE_ERR_UNSUPPORTED;
-      GemmParams b{};
-      std::memset(&b, 0, sizeof(b));
-      b.M = rows;
-      b.N = H;
-      b.K = vs;
-      b.m_tiles = (rows + kBM - 1) / kBM;
-      b.n_tiles = (H + kBN - 1) / kBN;
-      b.k_iters = (vs + kBK - 1) / kBK;
-      b.group_m = std::min(b.m_tiles, 8);
-      b.alpha = p.out_mult;
-      b.M_valid = rows;
-      b.N_valid = H;
-      b.out = a.gh_acc;
-      b.ldo = H;
-      b.status = &hdr->status;
-      b.timeout_ns = a.timeout;
-      CUtensorMap map_o;
-      if (!encode_f32_out(&map_o, a.gh_acc, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream, pair));
+      const int rc = grad_h_acc_gemm(x, a.dz, slab, rows, vs, a.W + static_cast<int64_t>(v0) * a.ld_w, a.ld_w, H,
+                                     a.gh_acc, 8);
+      if (rc != FLCE_OK) return rc;
     }
     if (a.grad_W) {
-      // grad_W_slab += m dz_slab^T h_c   (both MN-major, K = chunk rows)
-      CUtensorMap map_a, map_b;
-      if (!encode_bf16(&map_a, a.dz, vs, rows, slab, 64)) return FLCE_ERR_UNSUPPORTED;
-      if (!encode_bf16(&map_b, a.h_c, H, rows, a.ld_hc, 64)) return FLCE_ERR_UNSUPPORTED;
-      GemmParams b{};
-      std::memset(&b, 0, sizeof(b));
-      b.M = vs;
-      b.N = H;
-      b.K = rows;
-      b.m_tiles = (vs + kBM - 1) / kBM;
-      b.n_tiles = (H + kBN - 1) / kBN;
-      b.k_iters = (rows + kBK - 1) / kBK;
-      b.group_m = std::min(b.m_tiles, 16);
-      b.alpha = p.out_mult;
-      b.M_valid = vs;
-      b.N_valid = H;
-      b.out = a.grad_W + static_cast<int64_t>(v0) * H;
-      b.ldo = H;
-      b.status = &hdr->status;
-      b.timeout_ns = a.timeout;
-      CUtensorMap map_o;
-      if (!encode_f32_out(&map_o, a.grad_W + static_cast<int64_t>(v0) * H, H, vs, H)) return FLCE_ERR_UNSUPPORTED;
-      FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                               std::min(b.m_tiles * b.n_tiles, a.sms), stream, pair));
+      const int rc = grad_W_acc_gemm(x, a.dz, slab, rows, vs, a.h_c, a.ld_hc, H,
+                                     a.grad_W + static_cast<int64_t>(v0) * H);
+      if (rc != FLCE_OK) return rc;
     }
   }
   return FLCE_OK;
@@ -919,7 +952,11 @@ int run(const flce_params* params, const Call& c) {
     }
 
     // ---- grad_W += m dz^T h_c
-    if (gw) {
+    if (gw && !simt && !kmajor) {  // dz and h_c read in place
+      const AccCtx x{p.out_mult, hdr, timeout, p.flags, sms, pair, stream};
+      rc = grad_W_acc_gemm(x, dz, L.ldd, rows, V, h_c, ld_hc, H, c.grad_W);
+      if (rc != FLCE_OK) return rc;
+    } else if (gw) {  // the debug paths: transposed copies
       if (kmajor) {
         FLCE_LAUNCH(K_TRANSPOSE_H, launch_transpose_bf16(static_cast<const uint16_t*>(c.h) + r0 * n.ld_h,
                                                          n.ld_h, rows, H, ht, L.ldht, stream));
@@ -932,8 +969,6 @@ int run(const flce_params* params, const Call& c) {
       b.m_tiles = (V + kBM - 1) / kBM;
       b.n_tiles = (H + kBN - 1) / kBN;
       b.k_iters = (rows + kBK - 1) / kBK;
-      // Groups of 16 vocab tiles: on the DSV3 head this beat an N-fastest walk
-      // with h_c kept in L2 and evict-first dz loads.
       b.group_m = std::min(b.m_tiles, 16);
       b.alpha = p.out_mult;
       b.M_valid = V;
@@ -945,21 +980,13 @@ int run(const flce_params* params, const Call& c) {
       if (simt) {
         FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_simt(EPI_ACC_F32, dzt, L.ldt, ht, L.ldht, b, stream));
       } else {
-        CUtensorMap map_a, map_b;
-        if (kmajor) {
-          // dz^T [V][C] and h_c^T [H][C]: K-major A and B
-          if (!encode_bf16(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
-        } else {
-          // dz [C][V] and h_c [C][H] read in place: MN-major A and B (K = chunk rows)
-          if (!encode_bf16(&map_a, dz, V, rows, L.ldd, 64)) return FLCE_ERR_UNSUPPORTED;
-          if (!encode_bf16(&map_b, h_c, H, rows, ld_hc, 64))
-            return FLCE_ERR_UNSUPPORTED;
-        }
-        CUtensorMap map_o;
+        // dz^T [V][C] and h_c^T [H][C]: K-major A and B
+        CUtensorMap map_a, map_b, map_o;
+        if (!encode_bf16(&map_a, dzt, rows, V, L.ldt, kBM)) return FLCE_ERR_UNSUPPORTED;
+        if (!encode_bf16(&map_b, ht, rows, H, L.ldht, kBN)) return FLCE_ERR_UNSUPPORTED;
         if (!encode_f32_out(&map_o, c.grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, !kmajor, !kmajor, wide_for(b), &map_a, &map_b, &map_o, b,
-                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, pair && !kmajor));
+        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, false, false, wide_for(b), &map_a, &map_b, &map_o, b,
+                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, false));
       }
     }
   }
@@ -1099,9 +1126,7 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
     uint16_t* z16 = reinterpret_cast<uint16_t*>(ws_all + Ls.off_z);
     float* gmax = reinterpret_cast<float*>(ws_all + Ls.off_gmax);
     uint16_t* dz = reinterpret_cast<uint16_t*>(ws_all + Ls.off_dz);
-    auto wide_for = [&](const GemmParams& g) { return pick_wide(p.flags, g, sms); };
-    CUtensorMap map_w_mn;
-    if (gh_acc && !encode_bf16(&map_w_mn, W, H, V, n.ld_w, 64)) return FLCE_ERR_UNSUPPORTED;  // W MN-major
+    const AccCtx x{p.out_mult, hdr, timeout, p.flags, sms, pair, stream};
     for (int64_t r0 = 0; r0 < p.n_rows; r0 += Ls.C) {
       const int rows = static_cast<int>(std::min<int64_t>(Ls.C, p.n_rows - r0));
       DlogitParams dp{};
@@ -1124,52 +1149,12 @@ int run_vp_backward(const flce_params* params, int64_t vocab_offset, int64_t voc
       dp.ldd = Ls.ldd;
       FLCE_LAUNCH(K_DLOGITS, launch_dlogits(dp, stream));
       if (gh_acc) {
-        CUtensorMap map_a, map_o;
-        if (!encode_bf16(&map_a, dz, V, rows, Ls.ldd, kBM)) return FLCE_ERR_UNSUPPORTED;   // dz K-major
-        if (!encode_f32_out(&map_o, gh_acc + r0 * H, H, rows, H)) return FLCE_ERR_UNSUPPORTED;
-        GemmParams b{};
-        std::memset(&b, 0, sizeof(b));
-        b.M = rows;
-        b.N = H;
-        b.K = V;
-        b.m_tiles = (rows + kBM - 1) / kBM;
-        b.n_tiles = (H + kBN - 1) / kBN;
-        b.k_iters = (V + kBK - 1) / kBK;
-        b.group_m = std::min(b.m_tiles, 16);
-        b.alpha = p.out_mult;
-        b.M_valid = rows;
-        b.N_valid = H;
-        b.out = gh_acc + r0 * H;
-        b.ldo = H;
-        b.status = &hdr->status;
-        b.timeout_ns = timeout;
-        FLCE_LAUNCH(K_GRADH_GEMM, launch_gemm_tc(EPI_ACC_F32, false, true, wide_for(b), &map_a, &map_w_mn, &map_o,
-                                                 b, std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+        rc = grad_h_acc_gemm(x, dz, Ls.ldd, rows, V, static_cast<const uint16_t*>(W), n.ld_w, H, gh_acc + r0 * H, 16);
+        if (rc != FLCE_OK) return rc;
       }
       if (grad_W) {
-        CUtensorMap map_a, map_b, map_o;
-        if (!encode_bf16(&map_a, dz, V, rows, Ls.ldd, 64)) return FLCE_ERR_UNSUPPORTED;    // dz MN-major
-        if (!encode_bf16(&map_b, static_cast<const uint16_t*>(h) + r0 * n.ld_h, H, rows, n.ld_h, 64))
-          return FLCE_ERR_UNSUPPORTED;                                                      // h_c MN-major
-        if (!encode_f32_out(&map_o, grad_W, H, V, H)) return FLCE_ERR_UNSUPPORTED;
-        GemmParams b{};
-        std::memset(&b, 0, sizeof(b));
-        b.M = V;
-        b.N = H;
-        b.K = rows;
-        b.m_tiles = (V + kBM - 1) / kBM;
-        b.n_tiles = (H + kBN - 1) / kBN;
-        b.k_iters = (rows + kBK - 1) / kBK;
-        b.group_m = std::min(b.m_tiles, 16);
-        b.alpha = p.out_mult;
-        b.M_valid = V;
-        b.N_valid = H;
-        b.out = grad_W;
-        b.ldo = H;
-        b.status = &hdr->status;
-        b.timeout_ns = timeout;
-        FLCE_LAUNCH(K_GRADW_GEMM, launch_gemm_tc(EPI_ACC_F32, true, true, wide_for(b), &map_a, &map_b, &map_o, b,
-                                                 std::min(b.m_tiles * b.n_tiles, sms), stream, pair));
+        rc = grad_W_acc_gemm(x, dz, Ls.ldd, rows, V, static_cast<const uint16_t*>(h) + r0 * n.ld_h, n.ld_h, H, grad_W);
+        if (rc != FLCE_OK) return rc;
       }
     }
     return FLCE_OK;
