@@ -198,13 +198,16 @@ def _fuzz(n=10, seed=90):
 
 
 @pytest.mark.parametrize("case", _fuzz(), ids=lambda c: f"N{c['N']}-H{c['H']}-V{c['V']}-S{len(c['offsets']) - 1}")
-def test_fuzzed_shard_tables(flce, case):
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "stored"])
+def test_fuzzed_shard_tables(flce, case, stored):
     """Seeded random shapes, options and shard boundaries (none aligned to the
-    256-column tiles), against the fp64 oracle and the unsharded call."""
+    256-column tiles), against the fp64 oracle and the unsharded call, in both
+    backward forms."""
     kw = {k: case[k] for k in ("softcap", "out_mult", "chunk_rows")}
     okw = {k: case[k] for k in ("softcap", "out_mult")}
     h, W, y = _inputs(case["N"], case["H"], case["V"], case["seed"])
-    _, outs, gh, gW = _run_shards(flce, h, W, y, case["offsets"], vocab_slab=case["vocab_slab"], **kw)
+    _, outs, gh, gW = _run_shards(flce, h, W, y, case["offsets"], vocab_slab=case["vocab_slab"], stored=stored,
+                                  **kw)
     f = flce.flce_forward(h.to(DEV), W.to(DEV), y.to(DEV), **kw)
     torch.cuda.synchronize()
     assert torch.equal(outs[0]["predicted"], f["predicted"])
@@ -218,7 +221,8 @@ def test_fuzzed_shard_tables(flce, case):
     assert np.abs(gw - ref["grad_W"]).max() <= 1e-2 * max(np.abs(ref["grad_W"]).max(), 1e-30)
 
 
-def test_empty_and_all_ignored_batches(flce):
+@pytest.mark.parametrize("stored", [False, True], ids=["recompute", "stored"])
+def test_empty_and_all_ignored_batches(flce, stored):
     """No rows, and rows that are all ignored: the loss and accuracy are 0, the
     gradients stay 0 and nothing reads outside the (empty) inputs."""
     H, V = 64, 1000
@@ -227,7 +231,7 @@ def test_empty_and_all_ignored_batches(flce):
     for N, ign in ((0, 0.0), (70, 1.0)):
         h = workloads.make_hidden(max(N, 1), H, 57)[:N]
         y = workloads.make_labels(max(N, 1), V, 57, ign)[:N]
-        _, outs, gh, gW = _run_shards(flce, h, W, y, offsets)
+        _, outs, gh, gW = _run_shards(flce, h, W, y, offsets, stored=stored)
         assert float(outs[0]["loss"]) == 0.0 and float(outs[0]["token_accuracy"]) == 0.0
         assert torch.count_nonzero(gh).item() == 0 and torch.count_nonzero(gW).item() == 0
 
